@@ -1,0 +1,339 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test pins the oracle to something other than itself: a closed form
+derived by hand (tests/golden/closed_form.json), an invariant of softmax
+attention, the pages' own streaming algorithm under every block split,
+a special case, or central finite differences.  A plausible slip in the
+oracle (a dropped term, a wrong sign or index, a transposed operand, log2
+instead of ln, an off-by-one causal mask) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form.json")
+
+
+def _rand(rng, B, H, N, d, scale=1.0):
+    return rng.standard_normal((B, H, N, d)) * scale
+
+
+def _mask_for(rng, N, blk, density=0.5):
+    nb = -(-N // blk)
+    m = (rng.random((nb, nb)) < density).astype(np.uint8)
+    np.fill_diagonal(m, 1)
+    return m
+
+
+VARIANTS = [
+    dict(),
+    dict(causal=True),
+    dict(kv_len=True),
+    dict(mask=True),
+    dict(causal=True, kv_len=True, mask=True),
+]
+
+
+def _variant_args(rng, B, N, blk, v):
+    kw = {"causal": v.get("causal", False)}
+    if v.get("kv_len"):
+        kw["kv_len"] = rng.integers(1, N + 1, size=B).astype(np.int32)
+    if v.get("mask"):
+        kw["block_mask"] = _mask_for(rng, N, blk)
+        kw["block"] = blk
+    return kw
+
+
+def _allowed_np(B, N, causal=False, kv_len=None, block_mask=None, block=128):
+    """Boolean [B, N, N] allowed set, written from the mask definitions."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    out = np.ones((B, N, N), bool)
+    if causal:
+        out &= (j <= i)[None]
+    if kv_len is not None:
+        out &= (j[None] < np.minimum(np.asarray(kv_len), N)[:, None, None])
+    if block_mask is not None:
+        out &= block_mask[(i // block), (j // block)].astype(bool)[None]
+    return out
+
+
+def _evalnum(x):
+    if isinstance(x, str):
+        if "*" in x:
+            a, b = x.split("*")
+            return float(a) * _evalnum(b)
+        assert x.startswith("ln")
+        return math.log(float(x[2:]))
+    return float(x)
+
+
+def _arr(nested):
+    return np.array([[_evalnum(e) for e in row] for row in nested], np.float64)
+
+
+# ---------------------------------------------------------------- golden
+
+
+@pytest.mark.parametrize("case", json.load(open(GOLDEN))["cases"], ids=lambda c: c["name"])
+def test_closed_form_golden(oracle_mod, case):
+    B, H, N, d = case["B"], case["H"], case["N"], case["d"]
+    q = _arr(case["q"]).reshape(B, H, N, d)
+    k = _arr(case["k"]).reshape(B, H, N, d)
+    v = _arr(case["v"]).reshape(B, H, N, d)
+    do = _arr(case["do"]).reshape(B, H, N, d)
+    kv_len = None if case["kv_len"] is None else np.array(case["kv_len"], np.int32)
+    o, lse = oracle_mod.forward(q, k, v, case["scale"], causal=case["causal"], kv_len=kv_len)
+    np.testing.assert_allclose(o.reshape(N, d), _arr(case["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse.reshape(N), [_evalnum(x) for x in case["lse"]], rtol=0,
+                               atol=1e-12)
+    dq, dk, dv = oracle_mod.backward(q, k, v, do, case["scale"], causal=case["causal"],
+                                     kv_len=kv_len)
+    np.testing.assert_allclose(dq.reshape(N, d), _arr(case["dq"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.reshape(N, d), _arr(case["dk"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv.reshape(N, d), _arr(case["dv"]), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- invariants
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_probability_rows_sum_to_one_and_masked_are_zero(oracle_mod, v):
+    rng = np.random.default_rng(11)
+    B, H, N, d, blk = 2, 2, 23, 5, 4
+    q, k = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    kw = _variant_args(rng, B, N, blk, v)
+    allowed = _allowed_np(B, N, kw["causal"], kw.get("kv_len"), kw.get("block_mask"), blk)
+    for bh in range(B * H):
+        P = oracle_mod.probs(q, k, 0.7, bh=bh, **kw)
+        al = allowed[bh // H]
+        assert np.all(P[~al] == 0.0)
+        assert np.all(P[al] > 0.0)
+        rows = al.any(axis=1)
+        np.testing.assert_allclose(P[rows].sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert np.all(P[~rows] == 0.0)
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_constant_values_give_that_constant(oracle_mod, v):
+    rng = np.random.default_rng(12)
+    B, H, N, d, blk = 2, 3, 19, 4, 4
+    q, k = _rand(rng, B, H, N, d, 2.0), _rand(rng, B, H, N, d, 2.0)
+    c = rng.standard_normal(d)
+    vv = np.broadcast_to(c, (B, H, N, d)).copy()
+    kw = _variant_args(rng, B, N, blk, v)
+    o, lse = oracle_mod.forward(q, k, vv, 0.3, **kw)
+    allowed = _allowed_np(B, N, kw["causal"], kw.get("kv_len"), kw.get("block_mask"), blk)
+    for b in range(B):
+        rows = allowed[b].any(axis=1)
+        np.testing.assert_allclose(o[b][:, rows], np.broadcast_to(c, o[b][:, rows].shape),
+                                   rtol=0, atol=1e-13)
+        assert np.all(o[b][:, ~rows] == 0.0)
+        assert np.all(np.isneginf(lse[b][:, ~rows]))
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_every_block_split_of_the_streaming_forward_equals_one_shot(oracle_mod, v):
+    """The explainer's running (m, l) merge and O update, steps 1-4, give the
+    one-shot softmax for every block size (query and key/value)."""
+    rng = np.random.default_rng(13)
+    B, H, N, d, blk = 1, 2, 9, 3, 3
+    q, k, vv = (_rand(rng, B, H, N, d, 1.5) for _ in range(3))
+    kw = _variant_args(rng, B, N, blk, v)
+    o_ref, lse_ref = oracle_mod.forward(q, k, vv, 0.9, **kw)
+    for Br in range(1, N + 1):
+        for Bc in range(1, N + 1):
+            o, lse = oracle_mod.forward_tiled(q, k, vv, 0.9, Br, Bc, **kw)
+            np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
+            np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_zero_queries_average_the_allowed_values(oracle_mod, v):
+    """Q = 0 makes every score 0: o_i is the mean of v over A_i, lse_i = ln |A_i|."""
+    rng = np.random.default_rng(14)
+    B, H, N, d, blk = 2, 2, 21, 3, 4
+    q = np.zeros((B, H, N, d))
+    k, vv = _rand(rng, B, H, N, d), _rand(rng, B, H, N, d)
+    kw = _variant_args(rng, B, N, blk, v)
+    o, lse = oracle_mod.forward(q, k, vv, 1.3, **kw)
+    allowed = _allowed_np(B, N, kw["causal"], kw.get("kv_len"), kw.get("block_mask"), blk)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                a = np.flatnonzero(allowed[b, i])
+                if len(a) == 0:
+                    continue
+                np.testing.assert_allclose(o[b, h, i], vv[b, h, a].mean(axis=0), rtol=0,
+                                           atol=1e-13)
+                assert abs(lse[b, h, i] - math.log(len(a))) < 1e-13
+
+
+def test_single_allowed_key_returns_its_value(oracle_mod):
+    """Causal row 0 attends only to key 0 (top-left aligned mask)."""
+    rng = np.random.default_rng(15)
+    B, H, N, d = 1, 3, 17, 6
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    o, lse = oracle_mod.forward(q, k, vv, 0.4, causal=True)
+    np.testing.assert_allclose(o[:, :, 0], vv[:, :, 0], rtol=0, atol=1e-15)
+    s00 = 0.4 * np.einsum("bhc,bhc->bh", q[:, :, 0], k[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], s00, rtol=0, atol=1e-14)
+    # row 1 attends exactly to keys {0, 1}: two-way softmax
+    s = 0.4 * np.einsum("bhc,bhjc->bhj", q[:, :, 1], k[:, :, :2])
+    w = np.exp(s - s.max(-1, keepdims=True))
+    w /= w.sum(-1, keepdims=True)
+    np.testing.assert_allclose(o[:, :, 1], np.einsum("bhj,bhjc->bhc", w, vv[:, :, :2]),
+                               rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_key_shift_moves_lse_by_scaled_query_dot(oracle_mod, v):
+    """K + 1 c^T adds scale*<q_i, c> to every score of row i: O unchanged,
+    lse_i shifted by exactly that amount (pins where the scale is applied)."""
+    rng = np.random.default_rng(16)
+    B, H, N, d, blk = 2, 2, 15, 4, 4
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    c = rng.standard_normal(d)
+    kw = _variant_args(rng, B, N, blk, v)
+    o1, l1 = oracle_mod.forward(q, k, vv, 0.6, **kw)
+    o2, l2 = oracle_mod.forward(q, k + c, vv, 0.6, **kw)
+    fin = np.isfinite(l1)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    shift = 0.6 * np.einsum("bhic,c->bhi", q, c)
+    np.testing.assert_allclose((l2 - l1)[fin], shift[fin], rtol=0, atol=1e-12)
+
+
+def test_joint_key_value_permutation_leaves_output_unchanged(oracle_mod):
+    rng = np.random.default_rng(17)
+    B, H, N, d = 2, 2, 25, 5
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    perm = rng.permutation(N)
+    o1, l1 = oracle_mod.forward(q, k, vv, 0.5)
+    o2, l2 = oracle_mod.forward(q, k[:, :, perm], vv[:, :, perm], 0.5)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-13)
+
+
+def test_all_ones_block_mask_equals_no_mask(oracle_mod):
+    rng = np.random.default_rng(18)
+    B, H, N, d, blk = 1, 2, 30, 4, 8
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    ones = np.ones((4, 4), np.uint8)
+    o1, l1 = oracle_mod.forward(q, k, vv, 0.5, causal=True)
+    o2, l2 = oracle_mod.forward(q, k, vv, 0.5, causal=True, block_mask=ones, block=blk)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    g1 = oracle_mod.backward(q, k, vv, do, 0.5, causal=True)
+    g2 = oracle_mod.backward(q, k, vv, do, 0.5, causal=True, block_mask=ones, block=blk)
+    for a, b in zip(g1, g2):
+        assert np.array_equal(a, b)
+
+
+def test_masked_blocks_and_padded_keys_contribute_nothing(oracle_mod):
+    """Values in masked-out blocks or past kv_len never reach O, lse, dQ; the
+    gradients of keys no query attends to are exactly zero."""
+    rng = np.random.default_rng(19)
+    B, H, N, d, blk = 2, 2, 24, 4, 8
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    mask = np.array([[1, 0, 1], [0, 1, 0], [1, 0, 0]], np.uint8)
+    kv_len = np.array([20, 13], np.int32)
+    kw = dict(block_mask=mask, block=blk, kv_len=kv_len)
+    allowed = _allowed_np(B, N, False, kv_len, mask, blk)
+    k2, v2 = k.copy(), vv.copy()
+    for b in range(B):
+        dead = ~allowed[b].any(axis=0)   # keys no query row attends to
+        k2[b, :, dead] += 100.0
+        v2[b, :, dead] -= 50.0
+    o1, l1 = oracle_mod.forward(q, k, vv, 0.5, **kw)
+    o2, l2 = oracle_mod.forward(q, k2, v2, 0.5, **kw)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    dq, dk, dv = oracle_mod.backward(q, k, vv, do, 0.5, **kw)
+    for b in range(B):
+        dead = ~allowed[b].any(axis=0)
+        assert np.all(dk[b][:, dead] == 0.0) and np.all(dv[b][:, dead] == 0.0)
+        empty = ~allowed[b].any(axis=1)
+        assert np.all(dq[b][:, empty] == 0.0)
+
+
+# ---------------------------------------------------------------- backward
+
+
+@pytest.mark.parametrize("v", VARIANTS, ids=str)
+def test_backward_matches_central_finite_differences(oracle_mod, v):
+    """dQ, dK, dV of L = sum(dO o O) against central differences of the forward."""
+    rng = np.random.default_rng(20)
+    B, H, N, d, blk, scale, h = 2, 1, 9, 3, 4, 0.8, 1e-6
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    kw = _variant_args(rng, B, N, blk, v)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle_mod.forward(q_, k_, v_, scale, **kw)
+        return float(np.sum(do * o))
+
+    dq, dk, dv = oracle_mod.backward(q, k, vv, do, scale, **kw)
+    for which, grad in (("q", dq), ("k", dk), ("v", dv)):
+        num = np.zeros_like(grad)
+        base = {"q": q, "k": k, "v": vv}
+        for idx in np.ndindex(*grad.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (loss(plus["q"], plus["k"], plus["v"])
+                        - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.linalg.norm(num - grad) / max(np.linalg.norm(grad), 1e-30)
+        assert err < 1e-6, (which, err)
+
+
+def test_row_selection_matches_full_results(oracle_mod):
+    rng = np.random.default_rng(21)
+    B, H, N, d, blk = 2, 2, 20, 4, 8
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    kw = dict(causal=True, kv_len=np.array([17, 9], np.int32),
+              block_mask=np.array([[1, 0, 1], [1, 1, 0], [0, 1, 1]], np.uint8), block=blk)
+    o, lse = oracle_mod.forward(q, k, vv, 0.5, **kw)
+    dq, dk, dv = oracle_mod.backward(q, k, vv, do, 0.5, **kw)
+    rows = np.array([0, 5, 19, 20 + 3, 40 + 11, 79], np.int64)
+    o_r, l_r = oracle_mod.forward(q, k, vv, 0.5, rows=rows, **kw)
+    np.testing.assert_array_equal(o_r, o.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(l_r, lse.reshape(-1)[rows])
+    keys = np.array([1, 8, 16, 33, 61, 70], np.int64)
+    dq_r, dk_r, dv_r = oracle_mod.backward(q, k, vv, do, 0.5, q_rows=rows, k_rows=keys, **kw)
+    np.testing.assert_array_equal(dq_r, dq.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(dk_r, dk.reshape(-1, d)[keys])
+    np.testing.assert_array_equal(dv_r, dv.reshape(-1, d)[keys])
+
+
+def test_cross_check_with_numpy_definition(oracle_mod):
+    """Independent numpy restatement (matrix form) on tiny masked cases."""
+    rng = np.random.default_rng(22)
+    B, H, N, d, blk, scale = 2, 2, 13, 4, 4, 0.7
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    kv_len = np.array([13, 6], np.int32)
+    mask = np.array([[1, 1, 0, 1], [0, 1, 1, 0], [1, 0, 1, 1], [1, 1, 1, 1]], np.uint8)
+    allowed = _allowed_np(B, N, True, kv_len, mask, blk)
+    o, lse = oracle_mod.forward(q, k, vv, scale, causal=True, kv_len=kv_len, block_mask=mask,
+                                block=blk)
+    dq, dk, dv = oracle_mod.backward(q, k, vv, do, scale, causal=True, kv_len=kv_len,
+                                     block_mask=mask, block=blk)
+    for b in range(B):
+        for h in range(H):
+            S = scale * q[b, h] @ k[b, h].T
+            S = np.where(allowed[b], S, -np.inf)
+            rows = allowed[b].any(1)
+            m = np.where(rows, S.max(1), 0.0)
+            E = np.exp(S - m[:, None])
+            P = E / np.where(rows, E.sum(1), 1.0)[:, None]
+            O = P @ vv[b, h]
+            np.testing.assert_allclose(o[b, h], O, rtol=0, atol=1e-12)
+            L = np.where(rows, m + np.log(np.where(rows, E.sum(1), 1.0)), -np.inf)
+            np.testing.assert_allclose(lse[b, h], L, rtol=0, atol=1e-12)
+            dV = P.T @ do[b, h]
+            dP = do[b, h] @ vv[b, h].T
+            Dv = (do[b, h] * O).sum(1)
+            dS = P * (dP - Dv[:, None])
+            np.testing.assert_allclose(dv[b, h], dV, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(dq[b, h], scale * dS @ k[b, h], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(dk[b, h], scale * dS.T @ q[b, h], rtol=0, atol=1e-12)
