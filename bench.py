@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark: exact attention forward + backward on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch: fa_fwd (forward
+kernel) then fa_bwd (D preprocess, dK/dV/dQ kernel, dQ convert), on the
+BERT-large-shaped encoder workload B=16 H=16 N=512 d=64 with per-sequence key
+padding (kv_len uniform in [256, 512]), bf16 storage, fp32 accumulation.
+Inputs are synthetic (seeded normals, see workloads.py).
+
+Timing: W warm-up steps, then exactly K steps, each bracketed by CUDA events
+on the launching stream; L2 is flushed (a 256 MiB buffer is rewritten)
+between steps, outside the events.  A barrier and a device synchronise
+bracket the timed loop; the per-rank time is the sum of the step events and
+the job time is the maximum over ranks.  value = counted FLOPs of all ranks
+/ job time.  FLOPs: 4*N*kv_len*d per (b, h) forward, 2.5x that backward.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs an independent replica (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "bert"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 4  # forward, D preprocess, dK/dV/dQ, dQ convert
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if one matches."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(f"{kernel}:{workload}")
+    except (OSError, ValueError):
+        return None
+
+
+def counted_flops(spec, kv_len):
+    """Forward FLOPs 4*N*L*d per (b, h) with L the key bound of batch b
+    (N*N for no padding, halved under causal), backward 2.5x forward."""
+    N, d, H = spec.N, spec.d, spec.H
+    lens = [min(int(x), N) for x in kv_len] if kv_len is not None else [N] * spec.B
+    fwd = sum(4.0 * N * L * d * H for L in lens)
+    nominal = 4.0 * N * N * d * H * spec.B
+    if spec.causal:
+        fwd *= 0.5
+        nominal *= 0.5
+    return {"fwd": fwd, "bwd": 2.5 * fwd, "step": 3.5 * fwd, "nominal_step": 3.5 * nominal}
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (ctypes) while the
+    timed region runs; falls back to `nvidia-smi -lms` if NVML is missing."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._h = None
+        self._proc = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            idx = cuda_index
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            parts = [p for p in vis.split(",") if p.strip()]
+            if parts and all(p.strip().isdigit() for p in parts) and cuda_index < len(parts):
+                idx = int(parts[cuda_index])
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+        except OSError:
+            self._nvml = None
+        self._index = cuda_index
+
+    def _poll_nvml(self):
+        nv, h = self._nvml, self._h
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if get_r(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self._thread.start()
+        else:
+            import subprocess
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown")
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self._index), f"--query-gpu={q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            names = ["sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6 or not f[0].isdigit():
+                    continue
+                self.samples.append(int(f[0]))
+                self.max_mhz = int(f[1]) if f[1].isdigit() else self.max_mhz
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar (timing only; no data-path exchange)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- oracle timing
+
+
+def time_oracle(w, budget_s: float, max_units=None):
+    """Times the fp64 oracle (forward + backward) on whole (b, h) heads of the
+    workload until budget_s has elapsed; returns (flops counted, seconds,
+    heads, threads)."""
+    import numpy as np
+    import oracle
+    import workloads as W
+    spec = w.spec
+    threads = os.cpu_count() or 1
+    q, k, v, do = (w.f64(n) for n in ("q", "k", "v", "do"))
+    done_flops, elapsed, heads = 0.0, 0.0, 0
+    order = [(b, h) for b in range(spec.B) for h in range(spec.H)]
+    for (b, h) in order:
+        if elapsed >= budget_s or (max_units is not None and heads >= max_units):
+            break
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        kv = None if w.kv_len is None else w.kv_len[b:b + 1]
+        qs, ks, vs, ds = (x[sl] for x in (q, k, v, do))
+        t0 = time.perf_counter()
+        oracle.forward(qs, ks, vs, spec.scale, causal=spec.causal, kv_len=kv,
+                       block_mask=w.block_mask, nthreads=threads)
+        oracle.backward(qs, ks, vs, ds, spec.scale, causal=spec.causal, kv_len=kv,
+                        block_mask=w.block_mask, nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        one = W.Spec(**{**spec.__dict__, "B": 1, "H": 1})
+        done_flops += counted_flops(one, kv)["step"]
+        heads += 1
+    del np
+    return done_flops, elapsed, heads, threads
+
+
+# ---------------------------------------------------------------- arms
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.make(WORKLOAD)
+    # calibrate one head, then size each step to keep the whole run to ~2 minutes
+    f1, t1, _, threads = time_oracle(w, 0.0, max_units=1)
+    per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    heads_per_step = max(1, min(w.spec.B * w.spec.H, int(per_step_budget / max(t1, 1e-6))))
+    for _ in range(args.warmup):
+        time_oracle(w, 0.0, max_units=heads_per_step)
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t, _, _ = time_oracle(w, float("inf"), max_units=heads_per_step)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    sample = (f"{heads_per_step} of {w.spec.B * w.spec.H} (b, h) heads per step "
+              f"(forward + backward, full rows)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    s = w.spec
+    return {"workload": "BERT-large-shaped encoder attention, fwd+bwd",
+            "B": s.B, "H": s.H, "N": s.N, "d": s.d, "causal": s.causal, "scale": s.scale,
+            "kv_len": "uniform [256, 512] per sequence (seed 2), keys past it masked",
+            "block_mask": None, "flops": "algorithmic: 4*N*kv_len*d per head fwd, x3.5 fwd+bwd",
+            "l2": "flushed between timed steps (256 MiB write outside the events)",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+
+    fa.lib()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = W.make(WORKLOAD)
+    s = w.spec
+    B, H, N, d = s.B, s.H, s.N, s.d
+    fl = counted_flops(s, w.kv_len)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+
+    q, k, v, do = dev(w.q), dev(w.k), dev(w.v), dev(w.do)
+    kv_len = torch.from_numpy(w.kv_len).to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, None, stream)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, None,
+                  ws, ws_bytes, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    fa.fa_check(stream)
+
+    K = args.steps
+    ev_step0, ev_step1, ev_fwd1 = ([torch.cuda.Event(enable_timing=True) for _ in range(K)]
+                                   for _ in range(3))
+    bm0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    bm1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev_step0[i].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, None, stream)
+        ev_fwd1[i].record(stream)
+        fa.fa_set_bwd_main_events(bm0[i], bm1[i])
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, None,
+                  ws, ws_bytes, stream)
+        ev_step1[i].record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    fa.fa_set_bwd_main_events(None, None)
+    barrier(world, device)
+    fa.fa_check(stream)
+
+    step_ms = [ev_step0[i].elapsed_time(ev_step1[i]) for i in range(K)]
+    fwd_ms = [ev_step0[i].elapsed_time(ev_fwd1[i]) for i in range(K)]
+    bwd_main_ms = [bm0[i].elapsed_time(bm1[i]) for i in range(K)]
+    t_rank = sum(step_ms) / 1e3
+    t_job = max_over_ranks(t_rank, world, device)
+    value = fl["step"] * K * world / t_job / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    fwd_avg = statistics.mean(fwd_ms) / 1e3
+    bwd_avg = statistics.mean(bwd_main_ms) / 1e3
+    dominant = "fa_bwd_main_kernel" if bwd_avg >= fwd_avg else "fa_fwd_kernel"
+    dom_flops = fl["bwd"] if dominant == "fa_bwd_main_kernel" else fl["fwd"]
+    dom_t = bwd_avg if dominant == "fa_bwd_main_kernel" else fwd_avg
+    achieved = dom_flops / dom_t / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(dominant, WORKLOAD),
+                "kernel": dominant, "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "algorithmic_flops_per_launch": dom_flops,
+                "avg_launch_ms": dom_t * 1e3}
+
+    # ---- end to end through the public API: pinned host in, host out
+    e2e_steps = max(3, min(args.e2e_steps, K))
+    hq, hk, hv, hdo = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (w.q, w.k, w.v, w.do))
+    hkv = torch.from_numpy(w.kv_len).pin_memory()
+    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=torch.int16).pin_memory() for _ in range(4))
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    dq_i, dk_i, dv_i, do_i = (t.view(torch.int16) for t in (dq, dk, dv, do))
+    qi, ki, vi, oi = (t.view(torch.int16) for t in (q, k, v, o))
+
+    def e2e_step():
+        qi.copy_(hq, non_blocking=True)
+        ki.copy_(hk, non_blocking=True)
+        vi.copy_(hv, non_blocking=True)
+        do_i.copy_(hdo, non_blocking=True)
+        kv_len.copy_(hkv, non_blocking=True)
+        step()
+        ho.copy_(oi, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq_i, non_blocking=True)
+        hdk.copy_(dk_i, non_blocking=True)
+        hdv.copy_(dv_i, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    barrier(world, device)
+    for i in range(e2e_steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        e2e_step()
+        e1[i].record(stream)
+    torch.cuda.synchronize(device)
+    fa.fa_check(stream)
+    e2e_t = max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
+                           world, device)
+    t_bytes = q.numel() * 2
+    h2d = 4 * t_bytes + hkv.numel() * 4
+    d2h = 4 * t_bytes + hlse.numel() * 4
+    e2e = {"value": fl["step"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": 1e3 * e2e_t / e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, t, heads, threads = time_oracle(w, args.cpu_budget)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{heads} of {B * H} (b, h) heads, forward + backward, full rows; "
+                         f"{t:.1f} s of fp64 C oracle work",
+               "seconds": t}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_job / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w),
+            "pct_of_peak": value / peak,
+            "fwd": {"tflops": fl["fwd"] / fwd_avg / 1e12, "ms": fwd_avg * 1e3},
+            "bwd_main": {"tflops": fl["bwd"] / bwd_avg / 1e12, "ms": bwd_avg * 1e3},
+            "nominal_tflops": fl["nominal_step"] * K * world / t_job / 1e12,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * K,
+            "clocks": sampler.summary(),
+            "wall_s_timed_region": wall,
+            "peak_aux_bytes": ws_bytes,
+            "materialised_s_p_bytes": 2 * B * H * N * N * 2,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

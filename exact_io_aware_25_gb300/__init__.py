@@ -1,0 +1,149 @@
+"""Exact, IO-aware tiled attention for GB300 (sm_103a) -- Python binding.
+
+A thin ctypes layer over ``libfa.so`` (C ABI in ``include/fa.h``).  The
+functions carry the C names and only marshal arguments: tensors may be given
+as objects with ``data_ptr()`` (e.g. torch CUDA tensors) or as integer device
+addresses; ``stream`` is a ``torch.cuda.Stream``, an integer ``cudaStream_t``
+or None (legacy default stream).  Every computation runs in the library's
+CUDA kernels; there is no fallback of any kind.  A non-OK status raises
+:class:`FaError`.
+
+Build the library with ``python -m exact_io_aware_25_gb300.build`` (done by
+``__graft_entry__.build()``); importing this package does not compile
+anything, and :func:`lib` raises if ``libfa.so`` is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "FaError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check",
+    "fa_status_string", "fa_set_wait_timeout_ns", "fa_debug_starve_next_fwd",
+    "fa_set_bwd_main_events",
+    "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA",
+    "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_MISALIGNED = -3
+FA_ERR_CUDA = -4
+FA_ERR_TIMEOUT = -5
+FA_ERR_WORKSPACE = -6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m exact_io_aware_25_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp, vp, vp]
+            L.fa_fwd.restype = ci
+            L.fa_bwd_workspace_size.argtypes = [ci, ci, ci, ci]
+            L.fa_bwd_workspace_size.restype = sz
+            L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp,
+                                 vp, vp, sz, vp]
+            L.fa_bwd.restype = ci
+            L.fa_check.argtypes = [vp]
+            L.fa_check.restype = ci
+            L.fa_status_string.argtypes = [ci]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_set_wait_timeout_ns.argtypes = [ctypes.c_longlong]
+            L.fa_set_wait_timeout_ns.restype = None
+            L.fa_set_bwd_main_events.argtypes = [vp, vp]
+            L.fa_set_bwd_main_events.restype = None
+            L.fa_debug_starve_next_fwd.argtypes = [ci]
+            L.fa_debug_starve_next_fwd.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    return x.data_ptr() or None
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    return getattr(s, "cuda_stream", s) or None
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FaError(status, where)
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal=0, kv_len=None, block_mask=None,
+           stream=None) -> None:
+    """Enqueue the forward pass (see include/fa.h for shapes and rules)."""
+    _check(lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                        int(d), float(scale), int(bool(causal)), _ptr(kv_len), _ptr(block_mask),
+                        _stream(stream)), "fa_fwd")
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(lib().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0, kv_len=None,
+           block_mask=None, workspace=None, workspace_bytes=0, stream=None) -> None:
+    """Enqueue the backward pass; ``workspace`` holds >= fa_bwd_workspace_size bytes."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                        _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
+                        int(bool(causal)), _ptr(kv_len), _ptr(block_mask), _ptr(workspace),
+                        int(workspace_bytes), _stream(stream)), "fa_bwd")
+
+
+def fa_check(stream=None) -> None:
+    """Synchronise ``stream``; raise FaError if a kernel recorded an error."""
+    _check(lib().fa_check(_stream(stream)), "fa_check")
+
+
+def fa_set_wait_timeout_ns(ns: int) -> None:
+    lib().fa_set_wait_timeout_ns(int(ns))
+
+
+def fa_set_bwd_main_events(start_event=None, stop_event=None) -> None:
+    """Record these events (torch.cuda.Event or raw cudaEvent_t) around the
+    main backward kernel of later fa_bwd calls; None, None stops it."""
+    def raw(e):
+        if e is None:
+            return None
+        return e if isinstance(e, int) else e.cuda_event
+    lib().fa_set_bwd_main_events(raw(start_event), raw(stop_event))
+
+
+def fa_debug_starve_next_fwd(enable: bool = True) -> None:
+    lib().fa_debug_starve_next_fwd(int(bool(enable)))

@@ -1,0 +1,266 @@
+// fa_api.cu -- host side of libfa.so: argument validation, TMA tensor-map
+// encoding, kernel launches on the caller's stream and the device error word.
+// The C ABI is declared in include/fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernels.cuh"
+
+namespace fa {
+
+// Device error word written by kernels whose bounded waits ran out.
+__device__ int g_dev_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultTimeoutNs = 2000000000LL;
+
+std::mutex g_mu;
+long long g_timeout_ns = kDefaultTimeoutNs;
+int g_starve_next = 0;
+cudaEvent_t g_bwd_ev_start = nullptr, g_bwd_ev_stop = nullptr;
+int *g_err_ptr[kMaxDevices] = {};
+int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Current device, checked to be sm_103; fills the error-word pointer.
+fa_status device_setup(int *dev_out, int **err_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return FA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int *>(p);
+  }
+  *dev_out = dev;
+  *err_out = g_err_ptr[dev];
+  return FA_OK;
+}
+
+// [B*H, N, 64] bf16 viewed as a 3-D tensor {d, N, B*H}; 128 x 64 boxes,
+// 128-byte swizzle; rows past N read as zeros and are dropped on store.
+bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                 static_cast<cuuint64_t>(N) * kHeadDim * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows >= (1LL << 31) || static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
+  if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  const int nt = (N + kTile - 1) / kTile;
+  if (block_mask && nt > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t *kv_len,
+                     const uint8_t *block_mask, int *err) {
+  Problem p{};
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.nt = (N + kTile - 1) / kTile;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.kv_len = kv_len;
+  p.block_mask = block_mask;
+  std::lock_guard<std::mutex> lk(g_mu);
+  p.wait.err = err;
+  p.wait.timeout_ns = static_cast<uint64_t>(g_timeout_ns);
+  return p;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t dsum, lse2, dq_acc, total;
+};
+
+WsLayout ws_layout(int B, int H, int N) {
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t n_pad = align_up(static_cast<size_t>(N), kTile);
+  WsLayout w{};
+  w.dsum = 0;
+  w.lse2 = align_up(w.dsum + bh * n_pad * sizeof(float), 256);
+  w.dq_acc = align_up(w.lse2 + bh * n_pad * sizeof(float), 256);
+  w.total = align_up(w.dq_acc + bh * n_pad * kHeadDim * sizeof(float), 256);
+  return w;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int N, int d, float scale, int causal, const int32_t *kv_len,
+                 const uint8_t *block_mask, void *stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = validate_common(B, H, N, d, scale, block_mask);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int *err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_bhnd(&tq, q, BH, N) || !encode_bhnd(&tk, k, BH, N) || !encode_bhnd(&tv, v, BH, N) ||
+      !encode_bhnd(&to, o, BH, N))
+    return FA_ERR_CUDA;
+  FwdArgs a{};
+  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err);
+  a.lse = lse;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    a.starve = g_starve_next;
+    g_starve_next = 0;
+  }
+  return launch_fwd(tq, tk, tv, to, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != kHeadDim) return 0;
+  return ws_layout(B, H, N).total;
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t *kv_len, const uint8_t *block_mask,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa_status st = validate_common(B, H, N, d, scale, block_mask);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const WsLayout wl = ws_layout(B, H, N);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
+  int dev = 0;
+  int *err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!encode_bhnd(&tq, q, BH, N) || !encode_bhnd(&tk, k, BH, N) || !encode_bhnd(&tv, v, BH, N) ||
+      !encode_bhnd(&tdo, dout, BH, N) || !encode_bhnd(&tdk, dk, BH, N) ||
+      !encode_bhnd(&tdv, dv, BH, N))
+    return FA_ERR_CUDA;
+  BwdArgs a{};
+  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err);
+  a.n_pad = static_cast<int>(align_up(static_cast<size_t>(N), kTile));
+  a.o = static_cast<const uint16_t *>(o);
+  a.dout = static_cast<const uint16_t *>(dout);
+  a.lse = lse;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.dsum = reinterpret_cast<float *>(ws + wl.dsum);
+  a.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
+  a.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
+  a.dq = static_cast<uint16_t *>(dq);
+  cudaEvent_t ev0, ev1;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ev0 = g_bwd_ev_start;
+    ev1 = g_bwd_ev_stop;
+  }
+  return launch_bwd(tq, tk, tv, tdo, tdk, tdv, a, static_cast<cudaStream_t>(stream), ev0, ev1) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status fa_check(void *stream) {
+  int dev = 0;
+  int *err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return h == kDevTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, bad size or bad scale";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 on an sm_103 GPU";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    default: return "unknown fa_status";
+  }
+}
+
+void fa_set_wait_timeout_ns(long long ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timeout_ns = ns > 0 ? ns : kDefaultTimeoutNs;
+}
+
+void fa_set_bwd_main_events(void *start_event, void *stop_event) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_bwd_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_bwd_ev_stop = static_cast<cudaEvent_t>(stop_event);
+}
+
+void fa_debug_starve_next_fwd(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_starve_next = enable ? 1 : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,441 @@
+// fa_bwd.cu -- backward kernels of exact tiled attention for sm_103a.
+//
+// The backward recomputes S and P tile by tile from Q, K, V and the stored
+// per-row statistic instead of reading a stored N x N matrix ("FlashAttention:
+// Fast and Memory-Efficient Exact Attention with IO-Awareness" explainer,
+// "Key ideas", recomputation; "Mathematical Properties Behind FlashAttention",
+// section 5, re-materialization).  The gradient formulas are the textbook
+// ones for O = softmax(scale Q K^T) V:
+//   dV = P^T dO, dP = dO V^T, D_i = <dO_i, O_i>, dS = P o (dP - D),
+//   dQ = scale dS K, dK = scale dS^T Q.
+//
+// Three kernels on the caller's stream:
+//   fa_bwd_pre_kernel   D_i, lse_i * log2(e) (+inf on padding / empty rows)
+//                       into the workspace, and zeroes the fp32 dQ
+//                       accumulators.  HBM-bound.
+//   fa_bwd_main_kernel  one CTA per (key tile j, b*h); K_j, V_j stay in shared
+//                       memory while the allowed query tiles stream past:
+//                         S^T = K_j Q_i^T, dP^T = V_j dO_i^T  (tcgen05, TMEM)
+//                         P^T = 2^(S^T scale log2e - lse2_i), dS^T = P^T o (dP^T - D_i)
+//                         dV += P^T dO_i, dK += dS^T Q_i      (TMEM accumulators)
+//                         dQ_i partial = dS K_j -> fp32 atomics into the workspace
+//   fa_bwd_dq_kernel    dQ = scale * accumulator -> bf16.
+#include "fa_kernels.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kThreads = 320;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- preprocess
+
+// 8 threads per row: each reads 8 bf16 of O and dO (16 bytes each) and
+// zeroes 8 fp32 accumulators.
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
+  const Problem &pr = a.pr;
+  const long long rows = static_cast<long long>(pr.B) * pr.H * a.n_pad;
+  const int sub = threadIdx.x & 7;
+  // rows is a multiple of 128 and every warp handles 4 consecutive rows, so
+  // the loop below is warp-uniform and the shuffles see all 32 lanes.
+  for (long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; g < rows;
+       g += (static_cast<long long>(gridDim.x) * blockDim.x) >> 3) {
+    const int bh = static_cast<int>(g / a.n_pad);
+    const int i = static_cast<int>(g % a.n_pad);
+    float dsum = 0.f;
+    if (i < pr.N) {
+      const size_t off = (static_cast<size_t>(bh) * pr.N + i) * kHeadDim + sub * 8;
+      const uint4 ov = __ldg(reinterpret_cast<const uint4 *>(a.o + off));
+      const uint4 dv = __ldg(reinterpret_cast<const uint4 *>(a.dout + off));
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(dw[t] << 16), dsum);
+        dsum = fmaf(__uint_as_float(ow[t] & 0xFFFF0000u), __uint_as_float(dw[t] & 0xFFFF0000u), dsum);
+      }
+    }
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
+    dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + static_cast<size_t>(g) * kHeadDim + sub * 8);
+    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sub == 0) {
+      a.dsum[g] = dsum;
+      float l2 = INFINITY;  // padding rows and rows with no allowed key: P = 0
+      if (i < pr.N) {
+        const float lse = a.lse[static_cast<size_t>(bh) * pr.N + i];
+        if (lse != -INFINITY) l2 = lse * kLog2e;
+      }
+      a.lse2[g] = l2;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dQ convert
+
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
+  const Problem &pr = a.pr;
+  const long long chunks = static_cast<long long>(pr.B) * pr.H * pr.N * (kHeadDim / 8);
+  for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = c / (kHeadDim / 8);
+    const int part = static_cast<int>(c % (kHeadDim / 8));
+    const int bh = static_cast<int>(row / pr.N);
+    const int i = static_cast<int>(row % pr.N);
+    const float4 *src = reinterpret_cast<const float4 *>(
+        a.dq_acc + (static_cast<size_t>(bh) * a.n_pad + i) * kHeadDim + part * 8);
+    const float4 x = __ldg(src), y = __ldg(src + 1);
+    const float s = pr.scale;
+    uint4 out;
+    out.x = pack_bf16(x.x * s, x.y * s);
+    out.y = pack_bf16(x.z * s, x.w * s);
+    out.z = pack_bf16(y.x * s, y.y * s);
+    out.w = pack_bf16(y.z * s, y.w * s);
+    *reinterpret_cast<uint4 *>(a.dq + static_cast<size_t>(row) * kHeadDim + part * 8) = out;
+  }
+}
+
+// ---------------------------------------------------------------- main kernel
+
+struct __align__(1024) BwdSmem {
+  uint8_t k[kTileBytes];                 // K_j (resident); later dK staging
+  uint8_t v[kTileBytes];                 // V_j (resident); later dV staging
+  uint8_t q[kStages][kTileBytes];
+  uint8_t dout[kStages][kTileBytes];
+  uint8_t pt[2][kTileBytes];             // P^T bf16: queries 0-63 | 64-127, rows = keys
+  uint8_t dst[2][kTileBytes];            // dS^T bf16, same layout
+  float lse2[kStages][kTile];
+  float dsum[kStages][kTile];
+  uint64_t bar_kv;
+  uint64_t bar_q_full[kStages];
+  uint64_t bar_q_empty[kStages];
+  uint64_t bar_s_full;
+  uint64_t bar_pds_full;
+  uint64_t bar_pds_free;
+  uint64_t bar_dq_full;
+  uint64_t bar_dq_free;
+  uint64_t bar_done;
+  uint64_t bar_final;
+  uint32_t tmem_base;
+  int abort;
+  int n_tiles;
+  int16_t tiles[kMaxMaskTiles];
+};
+
+// TMEM columns.
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) { return s.tiles[it]; }
+
+// Writes 32 consecutive bf16 (four 16-byte chunks) of row `row` into a
+// [128 rows][128 cols] bf16 tile stored as two 128-byte-swizzled halves.
+__device__ __forceinline__ void store_row32(uint8_t (*tile)[kTileBytes], int row, int c4,
+                                            const uint32_t *w) {
+  const uint32_t base = smem_u32(tile[c4 >> 1]) + row * 128;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t ch = (c4 & 1) * 4 + t;
+    st_shared_v4(base + ((ch ^ (row & 7)) << 4), w[4 * t], w[4 * t + 1], w[4 * t + 2],
+                 w[4 * t + 3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                       const BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem &s = *reinterpret_cast<BwdSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const Problem &pr = a.pr;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kt = blockIdx.x;  // key tile; small kt = most query tiles under causal
+  const int bh = blockIdx.y;
+  const int b = bh / pr.H;
+  const int kv_bound = key_bound(pr, b);
+  const bool kv_live = kt * kTile < kv_bound;
+  const int i_begin = pr.causal ? kt : 0;
+
+  if (tid == 0) {
+    mbar_init(&s.bar_kv, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.bar_q_full[i], 1);
+      mbar_init(&s.bar_q_empty[i], 1);
+    }
+    mbar_init(&s.bar_s_full, 1);
+    mbar_init(&s.bar_pds_full, 128);
+    mbar_init(&s.bar_pds_free, 1);
+    mbar_init(&s.bar_dq_full, 1);
+    mbar_init(&s.bar_dq_free, 128);
+    mbar_init(&s.bar_done, 1);
+    mbar_init(&s.bar_final, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc(&s.tmem_base, kTmemCols);
+  // Query tiles that attend to this key tile: i >= i_begin (causal), the
+  // block mask's column kt, nothing at all when the tile is past kv_len.
+  if (warp == 0) {
+    int count = 0;
+    if (kv_live) {
+      for (int base = i_begin; base < pr.nt; base += 32) {
+        const int i = base + lane;
+        bool keep = i < pr.nt;
+        if (keep && pr.block_mask)
+          keep = __ldg(pr.block_mask + static_cast<size_t>(i) * pr.nt + kt) != 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) s.tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(i);
+        count += __popc(bal);
+      }
+    }
+    if (lane == 0) s.n_tiles = count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int n = s.n_tiles;
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
+      tma_load_3d(s.k, &tm_k, &s.bar_kv, 0, kt * kTile, bh);
+      tma_load_3d(s.v, &tm_v, &s.bar_kv, 0, kt * kTile, bh);
+      for (int it = 0; it < n; ++it) {
+        const int st = it % kStages;
+        const uint32_t use = it / kStages;
+        if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
+        const int i = qtile_at(s, it);
+        const size_t stat = static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile;
+        mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
+        tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, bh);
+        tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, bh);
+        bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
+        bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
+      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort);
+      for (int it = 0; ok && it < n; ++it) {
+        const int st = it % kStages;
+        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
+        mma_commit(&s.bar_s_full);
+        if (!mbar_wait(&s.bar_pds_full, it & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smem_u32(s.pt[kk >> 2]) + off, 16, 1024),
+                      sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[kk >> 2]) + off, 16, 1024),
+                      sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
+        }
+        if (it > 0 && !mbar_wait(&s.bar_dq_free, (it - 1) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major operand
+        // (queries contiguous, two 64-query halves 16 KiB apart); B = K_j,
+        // MN-major (d contiguous).  K dimension = keys, 16 per instruction.
+        const uint32_t ds_addr = smem_u32(s.dst[0]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
+                      sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
+        mma_commit(&s.bar_dq_full);
+        mma_commit(&s.bar_q_empty[st]);
+        mma_commit(&s.bar_pds_free);
+      }
+      mma_commit(&s.bar_done);
+    }
+    if (lane == 0) {
+      mma_commit(&s.bar_final);
+      mbar_wait_drain(&s.bar_final, 0, pr.wait);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T / dS^T (rows = keys)
+    const int kr = tid;
+    const int key = kt * kTile + kr;
+    const bool key_ok = key < kv_bound;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = pr.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int st = it % kStages;
+      const int i = qtile_at(s, it);
+      if (!mbar_wait_warp(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort) ||
+          !mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort) ||
+          (it > 0 && !mbar_wait_warp(&s.bar_pds_free, (it - 1) & 1, pr.wait, &s.abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = pr.causal && (i == kt);
+      const float *lse2 = s.lse2[st];
+      const float *dsum = s.dsum[st];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_base + kColST + c4 * 32, sr);
+        tmem_ld32(tmem + lane_base + kColDPT + c4 * 32, dr);
+        tmem_wait_ld();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int ql = c4 * 32 + t + u;
+            float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lse2[ql]));
+            const bool masked = !key_ok || (diag && kr > ql);
+            p = masked ? 0.f : p;
+            p2[u] = p;
+            d2[u] = p * (__uint_as_float(dr[t + u]) - dsum[ql]);
+          }
+          pw[t >> 1] = pack_bf16(p2[0], p2[1]);
+          dw[t >> 1] = pack_bf16(d2[0], d2[1]);
+        }
+        store_row32(s.pt, kr, c4, pw);
+        store_row32(s.dst, kr, c4, dw);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.bar_pds_full);
+    }
+    // ---------------------------------------------------------- epilogue: dV, dK
+    if (ok && n > 0) ok = mbar_wait_warp(&s.bar_done, 0, pr.wait, &s.abort);
+    if (ok) {
+      tc_fence_after();
+      // dV -> s.v, dK * scale -> s.k (both no longer read by any MMA)
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? kColDV : kColDK;
+        const float mul = which == 0 ? 1.f : pr.scale;
+        const uint32_t dst = smem_u32(which == 0 ? s.v : s.k) + kr * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld32(tmem + lane_base + col + half * 32, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = 0u;
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int c0 = ch * 8;
+            st_shared_v4(dst + (((half * 4 + ch) ^ (kr & 7)) << 4),
+                         pack_bf16(__uint_as_float(r[c0]) * mul, __uint_as_float(r[c0 + 1]) * mul),
+                         pack_bf16(__uint_as_float(r[c0 + 2]) * mul, __uint_as_float(r[c0 + 3]) * mul),
+                         pack_bf16(__uint_as_float(r[c0 + 4]) * mul, __uint_as_float(r[c0 + 5]) * mul),
+                         pack_bf16(__uint_as_float(r[c0 + 6]) * mul, __uint_as_float(r[c0 + 7]) * mul));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 128);
+    if (tid == 0 && ok && !s.abort) {
+      tma_store_3d(&tm_dv, s.v, 0, kt * kTile, bh);
+      tma_store_3d(&tm_dk, s.k, 0, kt * kTile, bh);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  } else {
+    // ------------------------------------------------------------ dQ partials (rows = queries)
+    const int qr = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int it = 0; it < n; ++it) {
+      const int i = qtile_at(s, it);
+      if (!mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort)) break;
+      tc_fence_after();
+      uint32_t r[64];
+      tmem_ld32(tmem + lane_base + kColDQ, r);
+      tmem_ld32(tmem + lane_base + kColDQ + 32, r + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s.bar_dq_free);
+      float4 *dst = reinterpret_cast<float4 *>(
+          a.dq_acc + (static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile + qr) *
+                         kHeadDim);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        atomicAdd(dst + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                       __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes() { return sizeof(BwdSmem) + 1024; }
+
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                       const BwdArgs &a, cudaStream_t st, cudaEvent_t ev_start,
+                       cudaEvent_t ev_stop) {
+  static int configured_dev = -1;
+  static int num_sms = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = bwd_smem_bytes();
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(fa_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  const long long pre_rows = static_cast<long long>(a.pr.B) * a.pr.H * a.n_pad;
+  const long long pre_blocks = (pre_rows * 8 + 255) / 256;
+  const int pre_grid = static_cast<int>(pre_blocks < num_sms * 16LL ? pre_blocks : num_sms * 16LL);
+  fa_bwd_pre_kernel<<<pre_grid, 256, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
+  if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
+  fa_bwd_main_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
+  const long long chunks = static_cast<long long>(a.pr.B) * a.pr.H * a.pr.N * (kHeadDim / 8);
+  const long long dq_blocks = (chunks + 255) / 256;
+  const int dq_grid = static_cast<int>(dq_blocks < num_sms * 16LL ? dq_blocks : num_sms * 16LL);
+  fa_bwd_dq_kernel<<<dq_grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

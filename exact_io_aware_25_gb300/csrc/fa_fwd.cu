@@ -1,0 +1,350 @@
+// fa_fwd.cu -- forward kernel of exact tiled attention for sm_103a.
+//
+// Follows "FlashAttention: Fast and Memory-Efficient Exact Attention with
+// IO-Awareness" (explainer page), "Method": for query tile i and each allowed
+// key/value tile j,
+//   1. S_ij = Q_i K_j^T on chip (here scaled: S = scale * Q K^T),
+//   2. block row max / exponentials / row sums,
+//   3. running max m and exponential sum l updated with the merge rule of
+//      "online softmax tracking",
+//   4. the partial output rescaled and P~_ij V_j accumulated,
+// then only O and the per-row statistic (lse = m + ln l) are written.
+//
+// GB300 mapping (one CTA per (query tile, b*h); 6 warps):
+//   warp 4   TMA producer: Q once, then K_j / V_j into a 3-stage ring.
+//   warp 5   TMEM owner and MMA issuer: S = Q K_j^T (M=128, N=128, K=64)
+//            into one of two TMEM S buffers, O += P~ V_j (M=128, N=64,
+//            K=128) into the TMEM O accumulator.  S_{j+1} is issued before
+//            waiting for P~_j, so the tensor core overlaps the softmax.
+//   warps 0-3 softmax: thread t owns query row t.  Reads its S row from TMEM,
+//            applies the masks, keeps (m, l) in base-2 units, writes
+//            P~ = 2^(S*scale*log2e - m) as bf16 into a 128-byte-swizzled
+//            shared tile (the MMA's A operand), rescales its O row in TMEM
+//            when m grew, and runs the epilogue (O / l -> bf16 -> TMA store,
+//            lse).
+// Division by l is deferred to the epilogue; the result equals the pages'
+// per-step normalised update because both use the same running max.
+#include "fa_kernels.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
+
+struct __align__(1024) FwdSmem {
+  uint8_t q[kTileBytes];              // Q_i; reused to stage O for the TMA store
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint8_t p[2][kTileBytes];           // P~ (bf16): keys 0-63 and 64-127
+  uint64_t bar_q;
+  uint64_t bar_k_full[kStages];
+  uint64_t bar_v_full[kStages];
+  uint64_t bar_kv_empty[kStages];
+  uint64_t bar_s_full[2];
+  uint64_t bar_p_full;
+  uint64_t bar_o_done;
+  uint64_t bar_final;
+  uint32_t tmem_base;
+  int abort;
+  int n_tiles;
+  int16_t tiles[kMaxMaskTiles];
+};
+
+// TMEM columns: S buffers at 0 and 128, O accumulator at 256.
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kTmemCols = 512;
+
+__device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
+  return sparse ? static_cast<int>(s.tiles[it]) : it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem &s = *reinterpret_cast<FwdSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const Problem &pr = args.pr;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.x);  // heavy causal tiles first
+  const int bh = blockIdx.y;
+  const int b = bh / pr.H;
+  const int kv_bound = key_bound(pr, b);
+  const int n_kv = (kv_bound + kTile - 1) / kTile;
+  const int j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
+  const bool sparse = pr.block_mask != nullptr;
+
+  if (tid == 0) {
+    mbar_init(&s.bar_q, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.bar_k_full[i], 1);
+      mbar_init(&s.bar_v_full[i], 1);
+      mbar_init(&s.bar_kv_empty[i], 1);
+    }
+    mbar_init(&s.bar_s_full[0], 1);
+    mbar_init(&s.bar_s_full[1], 1);
+    mbar_init(&s.bar_p_full, 128);
+    mbar_init(&s.bar_o_done, 1);
+    mbar_init(&s.bar_final, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  // Block-sparse: compact the allowed key tiles of this query-tile row
+  // ([EXPL] "Extension: Block-Sparse FlashAttention": only nonzero blocks
+  // are evaluated).
+  if (warp == 0) {
+    int count = 0;
+    if (sparse) {
+      const uint8_t *row = pr.block_mask + static_cast<size_t>(qt) * pr.nt;
+      for (int base = 0; base < j_end; base += 32) {
+        const int j = base + lane;
+        const bool keep = j < j_end && __ldg(row + j) != 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) s.tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(j);
+        count += __popc(bal);
+      }
+    } else {
+      count = j_end;
+    }
+    if (lane == 0) s.n_tiles = count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int n = s.n_tiles;
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(&s.bar_q, kTileBytes);
+      tma_load_3d(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      if (!args.starve) {
+        for (int it = 0; it < n; ++it) {
+          const int st = it % kStages;
+          const uint32_t use = it / kStages;
+          if (use > 0 && !mbar_wait(&s.bar_kv_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
+          const int j = tile_at(s, sparse, it);
+          mbar_arrive_expect_tx(&s.bar_k_full[st], kTileBytes);
+          tma_load_3d(s.k[st], &tm_k, &s.bar_k_full[st], 0, j * kTile, bh);
+          mbar_arrive_expect_tx(&s.bar_v_full[st], kTileBytes);
+          tma_load_3d(s.v[st], &tm_v, &s.bar_v_full[st], 0, j * kTile, bh);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 64, false, true);
+      const uint32_t q_addr = smem_u32(s.q);
+      bool ok = mbar_wait(&s.bar_q, 0, pr.wait, &s.abort);
+      // S_it = Q K_it^T into S buffer it % 2.
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % kStages;
+        if (!mbar_wait(&s.bar_k_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(s.k[st]);
+        const uint32_t d_tmem = tmem + ((it & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          mma_bf16_ss(d_tmem, sdesc_sw128(q_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0);
+        }
+        mma_commit(&s.bar_s_full[it & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int it = 0; ok && it < n; ++it) {
+        if (it + 1 < n && !issue_s(it + 1)) break;
+        if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
+        const int st = it % kStages;
+        if (!mbar_wait(&s.bar_v_full[st], (it / kStages) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(s.v[st]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t p_addr = smem_u32(s.p[kk >> 2]) + (kk & 3) * 32;
+          // V_j is [keys][d] with d contiguous: an MN-major B operand; one
+          // 64-wide swizzle atom along N, 8-key groups 1024 bytes apart.
+          mma_bf16_ss(tmem + kColO, sdesc_sw128(p_addr, 16, 1024),
+                      sdesc_sw128(v_addr + kk * 2048, 1024, 1024), idesc_o, (it > 0 || kk > 0));
+        }
+        mma_commit(&s.bar_o_done);
+        mma_commit(&s.bar_kv_empty[st]);
+      }
+    }
+    if (lane == 0) {
+      // make sure no MMA is in flight before TMEM is released
+      mma_commit(&s.bar_final);
+      mbar_wait_drain(&s.bar_final, 0, pr.wait);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (rows)
+    const int row = tid;                   // 0..127 == TMEM lane
+    const int qrow = qt * kTile + row;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = pr.scale_log2;
+    float m = -INFINITY;  // running max of S*scale*log2e
+    float l = 0.f;        // running sum of 2^(S*scale*log2e - m)
+    bool ok = true;
+    const uint32_t p_base0 = smem_u32(s.p[0]) + row * 128;
+    const uint32_t p_base1 = smem_u32(s.p[1]) + row * 128;
+    for (int it = 0; it < n; ++it) {
+      const int j = tile_at(s, sparse, it);
+      if (!mbar_wait_warp(&s.bar_s_full[it & 1], (it >> 1) & 1, pr.wait, &s.abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[kTile];
+      {
+        uint32_t raw[kTile];
+        const uint32_t t0 = tmem + lane_base + ((it & 1) ? kColS1 : kColS0);
+        tmem_ld32(t0 + 0, raw + 0);
+        tmem_ld32(t0 + 32, raw + 32);
+        tmem_ld32(t0 + 64, raw + 64);
+        tmem_ld32(t0 + 96, raw + 96);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
+      }
+      const int key0 = j * kTile;
+      const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
+      if (edge) {
+        const int lim_kv = kv_bound - key0;                        // keys >= this are padding
+        const int lim_c = pr.causal ? (qrow - key0) : kTile;       // keys > this are in the future
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          if (c >= lim_kv || c > lim_c) sv[c] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_new = fmaxf(m, mx * sl2);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);  // 0 when m = -inf
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        sv[c] = ex2_approx(fmaf(sv[c], sl2, -m_use));
+        rs += sv[c];
+      }
+      // PV_{it-1} must be complete before P~ is overwritten and O rescaled.
+      if (it > 0) {
+        if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const float *x = sv + ch * 8;
+        const uint32_t addr = ((ch < 8) ? p_base0 : p_base1) + (((ch & 7) ^ (row & 7)) << 4);
+        st_shared_v4(addr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                     pack_bf16(x[6], x[7]));
+      }
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t to = tmem + lane_base + kColO;
+        uint32_t ov[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(to + half * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(to + half * 32, ov);
+        }
+        tmem_wait_st();
+      }
+      l = l * alpha + rs;
+      m = m_new;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.bar_p_full);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) {
+      float ov[kHeadDim];
+      if (n > 0) {
+        ok = mbar_wait_warp(&s.bar_o_done, (n - 1) & 1, pr.wait, &s.abort);
+        tc_fence_after();
+      }
+      if (ok) {
+        if (n > 0) {
+          uint32_t raw[kHeadDim];
+          const uint32_t to = tmem + lane_base + kColO;
+          tmem_ld32(to, raw);
+          tmem_ld32(to + 32, raw + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < kHeadDim; ++c) ov[c] = __uint_as_float(raw[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kHeadDim; ++c) ov[c] = 0.f;
+        }
+        const float inv = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const uint32_t q_base = smem_u32(s.q) + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const float *x = ov + ch * 8;
+          st_shared_v4(q_base + ((ch ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                       pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                       pack_bf16(x[6] * inv, x[7] * inv));
+        }
+        if (qrow < pr.N) {
+          const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
+        }
+        fence_proxy_async_smem();
+      }
+    }
+    named_bar_sync(1, 128);
+    if (tid == 0 && ok && !s.abort) {
+      tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes() { return sizeof(FwdSmem) + 1024; }
+
+cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st) {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = fwd_smem_bytes();
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(fa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
+  fa_fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

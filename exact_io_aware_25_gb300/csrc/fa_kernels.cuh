@@ -1,0 +1,65 @@
+// fa_kernels.cuh -- parameter blocks and launch entry points shared between
+// the host launcher (fa_api.cu) and the kernels (fa_fwd.cu, fa_bwd.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_sm103.cuh"
+
+namespace fa {
+
+constexpr int kTile = 128;      // B_r = B_c = 128 query / key rows per tile
+constexpr int kHeadDim = 64;    // d
+constexpr int kMaxMaskTiles = 1024;  // block-sparse: at most 1024 tiles per row (N <= 131072)
+
+struct Problem {
+  int B, H, N;
+  int nt;                 // ceil(N / 128) tiles per head
+  float scale;            // S = scale * Q K^T
+  float scale_log2;       // scale * log2(e)
+  int causal;
+  const int32_t *kv_len;  // device [B] or nullptr
+  const uint8_t *block_mask;  // device [nt * nt] or nullptr
+  WaitCtl wait;
+};
+
+struct FwdArgs {
+  Problem pr;
+  float *lse;             // [B, H, N]
+  int starve;             // test hook: producer issues no K/V loads
+};
+
+struct BwdArgs {
+  Problem pr;
+  int n_pad;              // N rounded up to a multiple of 128
+  const uint16_t *o;      // [B, H, N, 64] bf16
+  const uint16_t *dout;   // [B, H, N, 64] bf16
+  const float *lse;       // [B, H, N]
+  float *dsum;            // workspace D   [B*H, n_pad]
+  float *lse2;            // workspace lse * log2(e) [B*H, n_pad] (+inf in padding rows)
+  float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, 64]
+  uint16_t *dq;           // [B, H, N, 64] bf16
+};
+
+// Key bound of batch b: kv_len[b] clamped to [0, N].
+__device__ __forceinline__ int key_bound(const Problem &p, int b) {
+  if (!p.kv_len) return p.N;
+  int L = __ldg(p.kv_len + b);
+  return L < 0 ? 0 : (L > p.N ? p.N : L);
+}
+
+size_t fwd_smem_bytes();
+size_t bwd_smem_bytes();
+
+cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
+
+// ev_start / ev_stop (may be null) are recorded around the main kernel.
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                       const BwdArgs &a, cudaStream_t st, cudaEvent_t ev_start,
+                       cudaEvent_t ev_stop);
+
+}  // namespace fa

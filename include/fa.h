@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact, IO-aware tiled attention on GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [EXPL] "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *          IO-Awareness" (paper explainer page).
+ *   [MATH] "Mathematical Properties Behind FlashAttention - Streaming
+ *          Transformations for Memory-Efficient Computation" (blog).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16 (stored as 16-bit words),
+ *     contiguous row-major [B, H, N, d]; lse is float32 [B, H, N].  The
+ *     pages fix no layout; this one keeps each head's N x d matrix
+ *     contiguous, so one (b, h) is a plain N x d operand of [EXPL] "Method".
+ *   - All tensor pointers are DEVICE pointers owned by the caller, and must be
+ *     16-byte aligned (TMA requirement).  The library never frees them.
+ *   - d must be 64.  N >= 1, B >= 1, H >= 1, B*H*N < 2^31.
+ *   - scale multiplies Q K^T (S = scale * Q K^T); it must be finite and > 0.
+ *   - causal != 0 keeps key j for query i iff j <= i (top-left aligned).
+ *   - kv_len: NULL, or a DEVICE int32 array [B]; keys j >= kv_len[b] of batch b
+ *     are masked (values are clamped to [0, N]).  Query rows are never masked.
+ *   - block_mask: NULL, or a DEVICE uint8 array [nb * nb], nb = ceil(N / 128),
+ *     row-major; entry (I, J) = 0 removes the 128 x 128 block of query tile I
+ *     and key tile J for every (b, h) ([EXPL] "Extension: Block-Sparse
+ *     FlashAttention": a fixed mask over N/B_r x N/B_c blocks; here
+ *     B_r = B_c = 128).
+ *   - Masks combine by AND.  A query row with no allowed key gets O = 0,
+ *     lse = -inf, dQ = 0, and adds nothing to dK, dV.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call is asynchronous on it; outputs are fully overwritten, never
+ *     accumulated.
+ *   - Every argument is validated before anything is launched; a failed call
+ *     launches nothing.  There is no CPU fallback and no other backend.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, non-finite or non-positive scale */
+    FA_ERR_UNSUPPORTED = -2,  /* d != 64, or no sm_103 device */
+    FA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
+    FA_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed */
+    FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait ran out (reported by fa_check) */
+    FA_ERR_WORKSPACE = -6     /* workspace NULL, misaligned or smaller than required */
+} fa_status;
+
+/*
+ * Forward pass ([EXPL] "Method", online softmax tracking and steps 1-4;
+ * [MATH] section 7).  For each query tile the kernel streams the allowed
+ * key/value tiles, computes S_ij = scale * Q_i K_j^T on chip, keeps the
+ * running row maximum m and exponential sum l, rescales the partial output
+ * and accumulates P~_ij V_j.  Only O and the per-row statistic are written
+ * ([EXPL] "Key ideas": O plus (l, m) are kept, O(N) extra memory).
+ *   q, k, v  in : bf16 [B, H, N, d]
+ *   o        out: bf16 [B, H, N, d], O = softmax(scale Q K^T, masked) V
+ *   lse      out: fp32 [B, H, N], lse_i = m_i + ln(l_i) (natural log; the pages'
+ *                 (m, l) pair folded into one number)
+ * Returns FA_OK once the kernel is enqueued.
+ */
+FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 const int32_t *kv_len, const uint8_t *block_mask, void *stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape: per (b, h) and
+ * query row (padded to a multiple of 128) one fp32 D_i = <dO_i, O_i>, one
+ * fp32 base-2 log-sum-exp, and d fp32 dQ accumulators; O(N) per head
+ * ([EXPL] "Complexity analysis": O(N) extra memory).  Returns 0 for
+ * invalid sizes.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation ([EXPL] "Key ideas", recomputation; [MATH]
+ * section 5): S and P are rebuilt tile by tile from Q, K, V and lse; the
+ * N x N matrices are never stored.  Gradient of L = <dO, O> for
+ * O = softmax(scale Q K^T) V:
+ *     dV = P^T dO, dP = dO V^T, D = rowsum(dO o O), dS = P o (dP - D),
+ *     dQ = scale dS K, dK = scale dS^T Q.
+ *   q, k, v, o, dO in : bf16 [B, H, N, d]; o is fa_fwd's output for the same
+ *                       inputs and masks
+ *   lse            in : fp32 [B, H, N], fa_fwd's output
+ *   dq, dk, dv     out: bf16 [B, H, N, d]
+ *   workspace      in : device scratch of >= fa_bwd_workspace_size() bytes,
+ *                       16-byte aligned, owned by the caller; its contents
+ *                       on entry do not matter and are garbage on return.
+ * Masks and scale must be the ones given to fa_fwd.
+ */
+FA_API fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                 int B, int H, int N, int d, float scale, int causal,
+                 const int32_t *kv_len, const uint8_t *block_mask,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises stream and reports the first device-side error recorded since
+ * the previous fa_check: FA_ERR_TIMEOUT when a bounded wait inside a kernel
+ * ran out (the kernel then returned early and its outputs are invalid),
+ * FA_ERR_CUDA for an asynchronous CUDA error, FA_OK otherwise.  Clears the
+ * recorded error.
+ */
+FA_API fa_status fa_check(void *stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+FA_API const char *fa_status_string(int status);
+
+/*
+ * Upper bound, in nanoseconds, on every spin-wait inside the kernels
+ * (default 2e9).  Values <= 0 restore the default.  Affects launches issued
+ * after the call.  Intended for tests of the timeout path.
+ */
+FA_API void fa_set_wait_timeout_ns(long long ns);
+
+/*
+ * Test hook for the failure-detection path: when enabled (nonzero), the next
+ * fa_fwd launches its kernel with the key/value producer told never to
+ * issue its loads, so that the consumers' bounded waits run out and the
+ * kernel returns FA_ERR_TIMEOUT through fa_check.  No GPU fault is raised.
+ * The flag clears itself after one launch.
+ */
+FA_API void fa_debug_starve_next_fwd(int enable);
+
+/*
+ * Measurement hook: when both are non-NULL, subsequent fa_bwd calls record
+ * the two cudaEvent_t handles on their stream immediately before and after
+ * the main backward kernel (the dK/dV/dQ kernel), so a caller can time that
+ * kernel alone with cudaEventElapsedTime.  Pass NULLs to stop.  The events
+ * are owned by the caller.
+ */
+FA_API void fa_set_bwd_main_events(void *start_event, void *stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H */

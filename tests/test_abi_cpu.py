@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/fa.h declares, and rejects bad arguments before touching CUDA
+(these calls return from host-side validation; nothing is launched)."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+FAKE = 0x10000  # a 16-byte aligned non-null address that is never dereferenced
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check", "fa_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(fa_lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa_lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(fa_\w+)", out))
+    missing = set(declared_symbols()) - exported
+    assert not missing, missing
+    lib = fa_lib.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name)
+
+
+def test_status_strings(fa_lib):
+    for code in range(0, -7, -1):
+        s = fa_lib.fa_status_string(code)
+        assert s.startswith("FA_")
+    assert fa_lib.fa_status_string(42) == "unknown fa_status"
+
+
+def test_workspace_size_formula(fa_lib):
+    # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + 64 fp32 dQ accumulators
+    for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536)]:
+        n_pad = -(-N // 128) * 128
+        bh = B * H
+        want = 0
+        want = -(-(bh * n_pad * 4) // 256) * 256
+        want = -(-(want + bh * n_pad * 4) // 256) * 256
+        want = -(-(want + bh * n_pad * 64 * 4) // 256) * 256
+        assert fa_lib.fa_bwd_workspace_size(B, H, N, 64) == want
+    assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 128) == 0
+    assert fa_lib.fa_bwd_workspace_size(0, 1, 128, 64) == 0
+
+
+def _fwd_status(fa, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+             causal=0, kv_len=None, block_mask=None, stream=None)
+    a.update(kw)
+    L = fa.lib()
+    return L.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                    a["scale"], a["causal"], a["kv_len"], a["block_mask"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(lse=None), -1), (dict(B=0), -1), (dict(N=0), -1),
+    (dict(H=-1), -1), (dict(scale=0.0), -1), (dict(scale=-1.0), -1),
+    (dict(scale=float("inf")), -1), (dict(scale=float("nan")), -1),
+    (dict(d=128), -2), (dict(d=32), -2), (dict(N=1 << 20, block_mask=FAKE), -2),
+    (dict(k=FAKE + 8), -3), (dict(lse=FAKE + 4), -3),
+    (dict(B=1 << 16, H=1 << 16, N=1), -1),
+])
+def test_forward_validation_without_gpu(fa_lib, kw, status):
+    assert _fwd_status(fa_lib, **kw) == status
+
+
+def test_backward_validation_without_gpu(fa_lib):
+    L = fa_lib.lib()
+    need = fa_lib.fa_bwd_workspace_size(1, 1, 128, 64)
+
+    def call(ws=FAKE, nbytes=need, d=64, dq=FAKE):
+        return L.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, 1, 1, 128, d, 0.125,
+                        0, None, None, ws, nbytes, None)
+
+    assert call(dq=None) == -1
+    assert call(d=96) == -2
+    assert call(dq=FAKE + 2) == -3
+    assert call(ws=None) == -6
+    assert call(nbytes=need - 1) == -6
+    assert call(ws=FAKE + 8) == -6
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and the header neither import, load nor name the oracle."""
+    bad = []
+    for base in ("exact_io_aware_25_gb300", "include"):
+        for dirpath, _, files in os.walk(os.path.join(ROOT, base)):
+            for f in files:
+                if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                    text = open(os.path.join(dirpath, f)).read()
+                    if re.search(r"\boracle\b|fa_oracle", text):
+                        bad.append(os.path.join(dirpath, f))
+    assert not bad, bad
