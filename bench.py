@@ -327,6 +327,8 @@ def run_ours(args, rank, world, local):
                                    for _ in range(3))
     bm0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     bm1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in bm0 + bm1:  # torch creates the CUDA event on first record
+        e.record(stream)
     sampler = ClockSampler(local)
     barrier(world, device)
     torch.cuda.synchronize(device)
