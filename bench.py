@@ -66,9 +66,10 @@ def load_traffic(kernel: str, workload: str):
         return None
 
 
-def counted_flops(spec, kv_len):
+def counted_flops(spec, kv_len, block_mask=None):
     """Forward FLOPs 4*N*L*d per (b, h) with L the key bound of batch b
-    (N*N for no padding, halved under causal), backward 2.5x forward."""
+    (N*N for no padding, halved under causal, times the nonzero-block
+    fraction under a block mask), backward 2.5x forward."""
     N, d, H = spec.N, spec.d, spec.H
     lens = [min(int(x), N) for x in kv_len] if kv_len is not None else [N] * spec.B
     fwd = sum(4.0 * N * L * d * H for L in lens)
@@ -76,6 +77,10 @@ def counted_flops(spec, kv_len):
     if spec.causal:
         fwd *= 0.5
         nominal *= 0.5
+    if block_mask is not None:
+        frac = float((block_mask != 0).sum()) / block_mask.size
+        fwd *= frac
+        nominal *= frac
     return {"fwd": fwd, "bwd": 2.5 * fwd, "step": 3.5 * fwd, "nominal_step": 3.5 * nominal}
 
 
@@ -231,7 +236,7 @@ def time_oracle(w, budget_s: float, max_units=None):
                         block_mask=w.block_mask, nthreads=threads)
         elapsed += time.perf_counter() - t0
         one = W.Spec(**{**spec.__dict__, "B": 1, "H": 1})
-        done_flops += counted_flops(one, kv)["step"]
+        done_flops += counted_flops(one, kv, w.block_mask)["step"]
         heads += 1
     del np
     return done_flops, elapsed, heads, threads
@@ -245,7 +250,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import workloads as W
-    w = W.make(WORKLOAD)
+    w = W.make(args.workload)
     # calibrate one head, then size each step to keep the whole run to ~2 minutes
     f1, t1, _, threads = time_oracle(w, 0.0, max_units=1)
     per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
@@ -274,14 +279,30 @@ def run_reference(args, rank, world):
     return 0
 
 
+WORKLOAD_NAMES = {
+    "tiny": "tiny exact-attention check, fwd+bwd",
+    "bert": "BERT-large-shaped encoder attention, fwd+bwd",
+    "gpt2": "GPT-2-small-shaped causal decoder attention, fwd+bwd",
+    "gpt2_4k": "long-context GPT-2-shaped causal attention with peaky keys, fwd+bwd",
+    "sparse64k": "block-sparse long-sequence attention (s=0.05), fwd+bwd",
+}
+
+
 def workload_config(w):
     s = w.spec
-    return {"workload": "BERT-large-shaped encoder attention, fwd+bwd",
-            "B": s.B, "H": s.H, "N": s.N, "d": s.d, "causal": s.causal, "scale": s.scale,
-            "kv_len": "uniform [256, 512] per sequence (seed 2), keys past it masked",
-            "block_mask": None, "flops": "algorithmic: 4*N*kv_len*d per head fwd, x3.5 fwd+bwd",
-            "l2": "flushed between timed steps (256 MiB write outside the events)",
-            "parallelism": "replicas"}
+    cfg = {"workload": WORKLOAD_NAMES.get(s.name, s.name),
+           "B": s.B, "H": s.H, "N": s.N, "d": s.d, "causal": s.causal, "scale": s.scale,
+           "kv_len": None, "block_mask": None,
+           "flops": "algorithmic: 4*N*L*d per head fwd (L = key bound; x0.5 causal; x nonzero "
+                    "block fraction), x3.5 fwd+bwd",
+           "l2": "flushed between timed steps (256 MiB write outside the events)",
+           "parallelism": "replicas"}
+    if w.kv_len is not None:
+        cfg["kv_len"] = "uniform [256, 512] per sequence (seed 2), keys past it masked"
+    if w.block_mask is not None:
+        cfg["block_mask"] = (f"{w.block_mask.shape[0]}x{w.block_mask.shape[1]} of 128x128 blocks, "
+                             f"{int(w.block_mask.sum())} nonzero")
+    return cfg
 
 
 def run_ours(args, rank, world, local):
@@ -294,16 +315,17 @@ def run_ours(args, rank, world, local):
     fa.lib()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    w = W.make(WORKLOAD)
+    w = W.make(args.workload)
     s = w.spec
     B, H, N, d = s.B, s.H, s.N, s.d
-    fl = counted_flops(s, w.kv_len)
+    fl = counted_flops(s, w.kv_len, w.block_mask)
 
     def dev(bits):
         return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
 
     q, k, v, do = dev(w.q), dev(w.k), dev(w.v), dev(w.do)
-    kv_len = torch.from_numpy(w.kv_len).to(device)
+    kv_len = torch.from_numpy(w.kv_len).to(device) if w.kv_len is not None else None
+    mask = (torch.from_numpy(w.block_mask).to(device) if w.block_mask is not None else None)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
@@ -313,8 +335,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(device)
 
     def step():
-        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, None, stream)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, None,
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, mask,
                   ws, ws_bytes, stream)
 
     for _ in range(max(3, args.warmup)):
@@ -337,10 +359,10 @@ def run_ours(args, rank, world, local):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev_step0[i].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, None, stream)
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
         ev_fwd1[i].record(stream)
         fa.fa_set_bwd_main_events(bm0[i], bm1[i])
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, None,
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, mask,
                   ws, ws_bytes, stream)
         ev_step1[i].record(stream)
     torch.cuda.synchronize(device)
@@ -366,7 +388,7 @@ def run_ours(args, rank, world, local):
     dom_t = bwd_avg if dominant == "fa_bwd_main_kernel" else fwd_avg
     achieved = dom_flops / dom_t / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic(dominant, WORKLOAD),
+                "frac": achieved / peak, "traffic": load_traffic(dominant, args.workload),
                 "kernel": dominant, "peak_source": f"bf16_tflops (burst) of {peak_src}",
                 "algorithmic_flops_per_launch": dom_flops,
                 "avg_launch_ms": dom_t * 1e3}
@@ -374,7 +396,7 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the public API: pinned host in, host out
     e2e_steps = max(3, min(args.e2e_steps, K))
     hq, hk, hv, hdo = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (w.q, w.k, w.v, w.do))
-    hkv = torch.from_numpy(w.kv_len).pin_memory()
+    hkv = torch.from_numpy(w.kv_len).pin_memory() if w.kv_len is not None else None
     ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=torch.int16).pin_memory() for _ in range(4))
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     dq_i, dk_i, dv_i, do_i = (t.view(torch.int16) for t in (dq, dk, dv, do))
@@ -385,7 +407,8 @@ def run_ours(args, rank, world, local):
         ki.copy_(hk, non_blocking=True)
         vi.copy_(hv, non_blocking=True)
         do_i.copy_(hdo, non_blocking=True)
-        kv_len.copy_(hkv, non_blocking=True)
+        if hkv is not None:
+            kv_len.copy_(hkv, non_blocking=True)
         step()
         ho.copy_(oi, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
@@ -409,7 +432,7 @@ def run_ours(args, rank, world, local):
     e2e_t = max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
                            world, device)
     t_bytes = q.numel() * 2
-    h2d = 4 * t_bytes + hkv.numel() * 4
+    h2d = 4 * t_bytes + (hkv.numel() * 4 if hkv is not None else 0)
     d2h = 4 * t_bytes + hlse.numel() * 4
     e2e = {"value": fl["step"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -450,6 +473,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name from workloads.py (the reported line uses bert)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -26,7 +26,6 @@ namespace fa {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -101,13 +100,20 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- main kernel
 
+// Warp roles (14 warps):
+//   warps 0-3   P^T / dS^T for queries 0-63 of the step (thread = key row)
+//   warps 4-7   P^T / dS^T for queries 64-127 (same key rows, other columns)
+//   warps 8-11  dQ partials: TMEM -> fp32 vector reductions (thread = query row)
+//   warp 12     TMA producer
+//   warp 13     TMEM owner and MMA issuer
+constexpr int kMainThreads = 448;
+
 struct __align__(1024) BwdSmem {
   uint8_t k[kTileBytes];                 // K_j (resident); later dK staging
   uint8_t v[kTileBytes];                 // V_j (resident); later dV staging
   uint8_t q[kStages][kTileBytes];
   uint8_t dout[kStages][kTileBytes];
-  uint8_t pt[2][kTileBytes];             // P^T bf16: queries 0-63 | 64-127, rows = keys
-  uint8_t dst[2][kTileBytes];            // dS^T bf16, same layout
+  uint8_t dst[2][2][kTileBytes];         // dS^T bf16, double-buffered; [buf][query half], rows = keys
   float lse2[kStages][kTile];
   float dsum[kStages][kTile];
   uint64_t bar_kv;
@@ -115,7 +121,8 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_q_empty[kStages];
   uint64_t bar_s_full;
   uint64_t bar_pds_full;
-  uint64_t bar_pds_free;
+  uint64_t bar_pt_free;
+  uint64_t bar_ds_free[2];
   uint64_t bar_dq_full;
   uint64_t bar_dq_free;
   uint64_t bar_done;
@@ -126,8 +133,10 @@ struct __align__(1024) BwdSmem {
   int16_t tiles[kMaxMaskTiles];
 };
 
-// TMEM columns.
-constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+// TMEM columns: S^T, dP^T (fp32, lanes = keys), dV, dK (fp32 accumulators,
+// lanes = keys), dQ partial (fp32, lanes = queries), P^T (bf16 pairs).
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
+                   kColPT = 448;
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) { return s.tiles[it]; }
@@ -145,7 +154,7 @@ __device__ __forceinline__ void store_row32(uint8_t (*tile)[kTileBytes], int row
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -169,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.bar_q_empty[i], 1);
     }
     mbar_init(&s.bar_s_full, 1);
-    mbar_init(&s.bar_pds_full, 128);
-    mbar_init(&s.bar_pds_free, 1);
+    mbar_init(&s.bar_pds_full, 256);
+    mbar_init(&s.bar_pt_free, 1);
+    mbar_init(&s.bar_ds_free[0], 1);
+    mbar_init(&s.bar_ds_free[1], 1);
     mbar_init(&s.bar_dq_full, 1);
     mbar_init(&s.bar_dq_free, 128);
     mbar_init(&s.bar_done, 1);
@@ -178,7 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 13) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 12 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
   // Query tiles that attend to this key tile: i >= i_begin (causal), the
   // block mask's column kt, nothing at all when the tile is past kv_len.
   if (warp == 0) {
@@ -202,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
@@ -221,17 +238,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
       constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
       const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort);
-      for (int it = 0; ok && it < n; ++it) {
+      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step it.
+      auto issue_s = [&](int it) -> bool {
         const int st = it % kStages;
-        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) break;
+        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
 #pragma unroll
@@ -243,33 +260,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
                       sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
         mma_commit(&s.bar_s_full);
+        return true;
+      };
+      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort) && issue_s(0);
+      for (int it = 0; ok && it < n; ++it) {
+        const int st = it % kStages;
+        const int buf = it & 1;
+        // P^T(it) is in TMEM, dS^T(it) in shared memory, and S^T / dP^T(it)
+        // have been read: start the next step's S^T, dP^T first so the
+        // elementwise warps can begin while dV, dK, dQ of this step run.
         if (!mbar_wait(&s.bar_pds_full, it & 1, pr.wait, &s.abort)) break;
         tc_fence_after();
+        if (it + 1 < n && !issue_s(it + 1)) break;
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+        // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per step),
+        // B = dO_i (queries x d, d contiguous: MN-major).
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDV, sdesc_sw128(smem_u32(s.pt[kk >> 2]) + off, 16, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
                       sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
-        }
+        mma_commit(&s.bar_pt_free);
+        // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[kk >> 2]) + off, 16, 1024),
+          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[buf][kk >> 2]) + off, 16, 1024),
                       sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
         }
+        mma_commit(&s.bar_q_empty[st]);
         if (it > 0 && !mbar_wait(&s.bar_dq_free, (it - 1) & 1, pr.wait, &s.abort)) break;
         tc_fence_after();
         // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major operand
         // (queries contiguous, two 64-query halves 16 KiB apart); B = K_j,
         // MN-major (d contiguous).  K dimension = keys, 16 per instruction.
-        const uint32_t ds_addr = smem_u32(s.dst[0]);
+        const uint32_t ds_addr = smem_u32(s.dst[buf][0]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
                       sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
         mma_commit(&s.bar_dq_full);
-        mma_commit(&s.bar_q_empty[st]);
-        mma_commit(&s.bar_pds_free);
+        mma_commit(&s.bar_ds_free[buf]);
       }
       mma_commit(&s.bar_done);
     }
@@ -278,20 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&s.bar_final, 0, pr.wait);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P^T / dS^T (rows = keys)
-    const int kr = tid;
+    const int half = warp >> 2;            // query columns 64*half .. 64*half+63
+    const int kr = (warp & 3) * 32 + lane; // key row == TMEM lane
     const int key = kt * kTile + kr;
     const bool key_ok = key < kv_bound;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = pr.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
+    for (int it = 0; it < n && ok; ++it) {
       const int st = it % kStages;
+      const int buf = it & 1;
       const int i = qtile_at(s, it);
       if (!mbar_wait_warp(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort) ||
-          !mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort) ||
-          (it > 0 && !mbar_wait_warp(&s.bar_pds_free, (it - 1) & 1, pr.wait, &s.abort))) {
+          !mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort)) {
         ok = false;
         break;
       }
@@ -300,10 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *lse2 = s.lse2[st];
       const float *dsum = s.dsum[st];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c = 0; c < 2; ++c) {
+        const int q0 = half * 64 + c * 32;  // first query column of this chunk
         uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + kColST + c4 * 32, sr);
-        tmem_ld32(tmem + lane_base + kColDPT + c4 * 32, dr);
+        tmem_ld32(tmem + lane_base + kColST + q0, sr);
+        tmem_ld32(tmem + lane_base + kColDPT + q0, dr);
         tmem_wait_ld();
         uint32_t pw[16], dw[16];
 #pragma unroll
@@ -311,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p2[2], d2[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int ql = c4 * 32 + t + u;
+            const int ql = q0 + t + u;
             float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lse2[ql]));
             const bool masked = !key_ok || (diag && kr > ql);
             p = masked ? 0.f : p;
@@ -321,47 +353,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           pw[t >> 1] = pack_bf16(p2[0], p2[1]);
           dw[t >> 1] = pack_bf16(d2[0], d2[1]);
         }
-        store_row32(s.pt, kr, c4, pw);
-        store_row32(s.dst, kr, c4, dw);
+        if (c == 0) {
+          // P^T columns free once dV(it-1) is done; dS^T buffer once dK/dQ(it-2) are
+          if ((it > 0 && !mbar_wait_warp(&s.bar_pt_free, (it - 1) & 1, pr.wait, &s.abort)) ||
+              (it > 1 && !mbar_wait_warp(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1, pr.wait,
+                                         &s.abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st16(tmem + lane_base + kColPT + (q0 >> 1), pw);
+        store_row32(s.dst[buf], kr, half * 2 + c, dw);
       }
+      if (!ok) break;
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.bar_pds_full);
     }
-    // ---------------------------------------------------------- epilogue: dV, dK
+    // ---------------------------------------------------------- epilogue: dV (warps 0-3), dK (4-7)
     if (ok && n > 0) ok = mbar_wait_warp(&s.bar_done, 0, pr.wait, &s.abort);
     if (ok) {
       tc_fence_after();
-      // dV -> s.v, dK * scale -> s.k (both no longer read by any MMA)
+      const uint32_t col = half == 0 ? kColDV : kColDK;
+      const float mul = half == 0 ? 1.f : pr.scale;
+      const uint32_t dst = smem_u32(half == 0 ? s.v : s.k) + kr * 128;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? kColDV : kColDK;
-        const float mul = which == 0 ? 1.f : pr.scale;
-        const uint32_t dst = smem_u32(which == 0 ? s.v : s.k) + kr * 128;
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tmem + lane_base + col + h2 * 32, r);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          if (n > 0) {
-            tmem_ld32(tmem + lane_base + col + half * 32, r);
-            tmem_wait_ld();
-          } else {
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = 0u;
-          }
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int c0 = ch * 8;
-            st_shared_v4(dst + (((half * 4 + ch) ^ (kr & 7)) << 4),
-                         pack_bf16(__uint_as_float(r[c0]) * mul, __uint_as_float(r[c0 + 1]) * mul),
-                         pack_bf16(__uint_as_float(r[c0 + 2]) * mul, __uint_as_float(r[c0 + 3]) * mul),
-                         pack_bf16(__uint_as_float(r[c0 + 4]) * mul, __uint_as_float(r[c0 + 5]) * mul),
-                         pack_bf16(__uint_as_float(r[c0 + 6]) * mul, __uint_as_float(r[c0 + 7]) * mul));
-          }
+        for (int ch = 0; ch < 4; ++ch) {
+          const int c0 = ch * 8;
+          st_shared_v4(dst + (((h2 * 4 + ch) ^ (kr & 7)) << 4),
+                       pack_bf16(__uint_as_float(r[c0]) * mul, __uint_as_float(r[c0 + 1]) * mul),
+                       pack_bf16(__uint_as_float(r[c0 + 2]) * mul, __uint_as_float(r[c0 + 3]) * mul),
+                       pack_bf16(__uint_as_float(r[c0 + 4]) * mul, __uint_as_float(r[c0 + 5]) * mul),
+                       pack_bf16(__uint_as_float(r[c0 + 6]) * mul, __uint_as_float(r[c0 + 7]) * mul));
         }
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 256);
     if (tid == 0 && ok && !s.abort) {
       tma_store_3d(&tm_dv, s.v, 0, kt * kTile, bh);
       tma_store_3d(&tm_dk, s.k, 0, kt * kTile, bh);
@@ -370,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ partials (rows = queries)
-    const int qr = tid - 128;
+    const int qr = tid - 256;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int it = 0; it < n; ++it) {
       const int i = qtile_at(s, it);
@@ -382,18 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s.bar_dq_free);
-      float4 *dst = reinterpret_cast<float4 *>(
-          a.dq_acc + (static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile + qr) *
-                         kHeadDim);
+      float *dst = a.dq_acc +
+                   (static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile + qr) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        atomicAdd(dst + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                       __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
+        red_add_v4(dst + 4 * c, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                   __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -428,7 +467,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
-  fa_bwd_main_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  fa_bwd_main_kernel<<<grid, kMainThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
   const long long chunks = static_cast<long long>(a.pr.B) * a.pr.H * a.pr.N * (kHeadDim / 8);

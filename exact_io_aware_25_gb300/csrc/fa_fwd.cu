@@ -10,18 +10,19 @@
 //   4. the partial output rescaled and P~_ij V_j accumulated,
 // then only O and the per-row statistic (lse = m + ln l) are written.
 //
-// GB300 mapping (one CTA per (query tile, b*h); 6 warps):
-//   warp 4   TMA producer: Q once, then K_j / V_j into a 3-stage ring.
+// GB300 mapping (one CTA per (query tile, b*h); 6 warps; two CTAs share an SM:
+// 256 TMEM columns and ~83 KB of shared memory each):
+//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring.
 //   warp 5   TMEM owner and MMA issuer: S = Q K_j^T (M=128, N=128, K=64)
-//            into one of two TMEM S buffers, O += P~ V_j (M=128, N=64,
-//            K=128) into the TMEM O accumulator.  S_{j+1} is issued before
-//            waiting for P~_j, so the tensor core overlaps the softmax.
+//            into TMEM, and O += P~ V_j (M=128, N=64, K=128) with P~ read
+//            straight from TMEM (A operand in tensor memory).  S_{j+1} is
+//            issued as soon as the softmax has pulled S_j into registers, so
+//            the tensor core overlaps the exponentials.
 //   warps 0-3 softmax: thread t owns query row t.  Reads its S row from TMEM,
 //            applies the masks, keeps (m, l) in base-2 units, writes
-//            P~ = 2^(S*scale*log2e - m) as bf16 into a 128-byte-swizzled
-//            shared tile (the MMA's A operand), rescales its O row in TMEM
-//            when m grew, and runs the epilogue (O / l -> bf16 -> TMA store,
-//            lse).
+//            P~ = 2^(S*scale*log2e - m) as packed bf16 pairs back into TMEM,
+//            rescales its O row in TMEM when m grew, and runs the epilogue
+//            (O / l -> bf16 -> TMA store, lse).
 // Division by l is deferred to the epilogue; the result equals the pages'
 // per-step normalised update because both use the same running max.
 #include "fa_kernels.cuh"
@@ -29,7 +30,7 @@
 namespace fa {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
 
@@ -37,12 +38,12 @@ struct __align__(1024) FwdSmem {
   uint8_t q[kTileBytes];              // Q_i; reused to stage O for the TMA store
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint8_t p[2][kTileBytes];           // P~ (bf16): keys 0-63 and 64-127
   uint64_t bar_q;
   uint64_t bar_k_full[kStages];
   uint64_t bar_v_full[kStages];
   uint64_t bar_kv_empty[kStages];
-  uint64_t bar_s_full[2];
+  uint64_t bar_s_full;
+  uint64_t bar_s_free;
   uint64_t bar_p_full;
   uint64_t bar_o_done;
   uint64_t bar_final;
@@ -52,14 +53,14 @@ struct __align__(1024) FwdSmem {
   int16_t tiles[kMaxMaskTiles];
 };
 
-// TMEM columns: S buffers at 0 and 128, O accumulator at 256.
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kTmemCols = 512;
+// TMEM columns: S (fp32) at 0, P~ (bf16 pairs) at 128, O accumulator at 192.
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192, kTmemCols = 256;
 
 __device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
   return sparse ? static_cast<int>(s.tiles[it]) : it;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdArgs args) {
@@ -83,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.bar_v_full[i], 1);
       mbar_init(&s.bar_kv_empty[i], 1);
     }
-    mbar_init(&s.bar_s_full[0], 1);
-    mbar_init(&s.bar_s_full[1], 1);
+    mbar_init(&s.bar_s_full, 1);
+    mbar_init(&s.bar_s_free, 128);
     mbar_init(&s.bar_p_full, 128);
     mbar_init(&s.bar_o_done, 1);
     mbar_init(&s.bar_final, 1);
@@ -148,23 +149,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16(128, 64, false, true);
       const uint32_t q_addr = smem_u32(s.q);
       bool ok = mbar_wait(&s.bar_q, 0, pr.wait, &s.abort);
-      // S_it = Q K_it^T into S buffer it % 2.
+      // S_it = Q K_it^T into the S columns.
       auto issue_s = [&](int it) -> bool {
         const int st = it % kStages;
         if (!mbar_wait(&s.bar_k_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]);
-        const uint32_t d_tmem = tmem + ((it & 1) ? kColS1 : kColS0);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          mma_bf16_ss(d_tmem, sdesc_sw128(q_addr + kk * 32, 16, 1024),
+          mma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + kk * 32, 16, 1024),
                       sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0);
         }
-        mma_commit(&s.bar_s_full[it & 1]);
+        mma_commit(&s.bar_s_full);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int it = 0; ok && it < n; ++it) {
+        // the softmax has copied S_it into registers: the S columns are free
+        if (!mbar_wait(&s.bar_s_free, it & 1, pr.wait, &s.abort)) break;
         if (it + 1 < n && !issue_s(it + 1)) break;
         if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
         const int st = it % kStages;
@@ -173,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_addr = smem_u32(s.v[st]);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t p_addr = smem_u32(s.p[kk >> 2]) + (kk & 3) * 32;
-          // V_j is [keys][d] with d contiguous: an MN-major B operand; one
-          // 64-wide swizzle atom along N, 8-key groups 1024 bytes apart.
-          mma_bf16_ss(tmem + kColO, sdesc_sw128(p_addr, 16, 1024),
+          // A = P~ from TMEM (16 keys = 8 packed columns per step); V_j is
+          // [keys][d] with d contiguous: an MN-major B operand, one 64-wide
+          // swizzle atom along N, 8-key groups 1024 bytes apart.
+          mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8,
                       sdesc_sw128(v_addr + kk * 2048, 1024, 1024), idesc_o, (it > 0 || kk > 0));
         }
         mma_commit(&s.bar_o_done);
@@ -198,11 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;  // running max of S*scale*log2e
     float l = 0.f;        // running sum of 2^(S*scale*log2e - m)
     bool ok = true;
-    const uint32_t p_base0 = smem_u32(s.p[0]) + row * 128;
-    const uint32_t p_base1 = smem_u32(s.p[1]) + row * 128;
     for (int it = 0; it < n; ++it) {
       const int j = tile_at(s, sparse, it);
-      if (!mbar_wait_warp(&s.bar_s_full[it & 1], (it >> 1) & 1, pr.wait, &s.abort)) {
+      if (!mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort)) {
         ok = false;
         break;
       }
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sv[kTile];
       {
         uint32_t raw[kTile];
-        const uint32_t t0 = tmem + lane_base + ((it & 1) ? kColS1 : kColS0);
+        const uint32_t t0 = tmem + lane_base + kColS;
         tmem_ld32(t0 + 0, raw + 0);
         tmem_ld32(t0 + 32, raw + 32);
         tmem_ld32(t0 + 64, raw + 64);
@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
       }
+      tc_fence_before();
+      mbar_arrive(&s.bar_s_free);
       const int key0 = j * kTile;
       const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
       if (edge) {
@@ -228,33 +230,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kTile; ++c)
           if (c >= lim_kv || c > lim_c) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      // row max: eight independent chains, then a tree
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, sv[c]);
+      for (int u = 0; u < 8; ++u) mx8[u] = sv[u];
+#pragma unroll
+      for (int c = 8; c < kTile; c += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], sv[c + u]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * sl2);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_use);  // 0 when m = -inf
-      float rs = 0.f;
+      float rs8[8];
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        sv[c] = ex2_approx(fmaf(sv[c], sl2, -m_use));
-        rs += sv[c];
-      }
-      // PV_{it-1} must be complete before P~ is overwritten and O rescaled.
-      if (it > 0) {
-        if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
-          ok = false;
-          break;
+      for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+      // P~ in two 64-key halves; the wait for PV_{it-1} (which still reads
+      // the P~ columns and accumulates into O) sits between them.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = half * 64; c < half * 64 + 64; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            sv[c + u] = ex2_approx(fmaf(sv[c + u], sl2, -m_use));
+            rs8[u] += sv[c + u];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) pk[((c - half * 64) + u) >> 1] = pack_bf16(sv[c + u], sv[c + u + 1]);
         }
-        tc_fence_after();
+        if (half == 0 && it > 0) {
+          if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tmem + lane_base + kColP + half * 32, pk);
       }
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const float *x = sv + ch * 8;
-        const uint32_t addr = ((ch < 8) ? p_base0 : p_base1) + (((ch & 7) ^ (row & 7)) << 4);
-        st_shared_v4(addr, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                     pack_bf16(x[6], x[7]));
-      }
+      if (!ok) break;
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const uint32_t to = tmem + lane_base + kColO;
         uint32_t ov[32];
@@ -266,11 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
           tmem_st32(to + half * 32, ov);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       l = l * alpha + rs;
       m = m_new;
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.bar_p_full);
     }
