@@ -21,7 +21,7 @@ import threading
 __all__ = [
     "FaError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check",
     "fa_status_string", "fa_set_wait_timeout_ns", "fa_debug_starve_next_fwd",
-    "fa_set_bwd_main_events",
+    "fa_set_bwd_main_events", "fa_bwd_noalloc", "fa_bwd_noalloc_max_scratch_bytes",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA",
     "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE", "LIB_PATH",
 ]
@@ -64,6 +64,11 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp,
                                  vp, vp, sz, vp]
             L.fa_bwd.restype = ci
+            L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
+                                         ci, vp, vp, vp]
+            L.fa_bwd_noalloc.restype = ci
+            L.fa_bwd_noalloc_max_scratch_bytes.argtypes = []
+            L.fa_bwd_noalloc_max_scratch_bytes.restype = sz
             L.fa_check.argtypes = [vp]
             L.fa_check.restype = ci
             L.fa_status_string.argtypes = [ci]
@@ -124,6 +129,21 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0, kv_le
                         _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
                         int(bool(causal)), _ptr(kv_len), _ptr(block_mask), _ptr(workspace),
                         int(workspace_bytes), _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0,
+                   kv_len=None, block_mask=None, stream=None) -> None:
+    """fa_bwd for callers that cannot allocate device memory: the scratch is a
+    fixed array inside the library (see include/fa.h for its limit and the
+    rule that overlapping calls race)."""
+    _check(lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d),
+                                float(scale), int(bool(causal)), _ptr(kv_len),
+                                _ptr(block_mask), _stream(stream)), "fa_bwd_noalloc")
+
+
+def fa_bwd_noalloc_max_scratch_bytes() -> int:
+    return int(lib().fa_bwd_noalloc_max_scratch_bytes())
 
 
 def fa_check(stream=None) -> None:

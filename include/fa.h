@@ -107,6 +107,33 @@ FA_API fa_status fa_bwd(const void *q, const void *k, const void *v, const void 
                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory when they run the backward pass (for instance a plugin whose
+ * host application owns every device allocation, or a latency-critical loop
+ * that must not allocate).  The paper has no counterpart: this is a
+ * deployment variant of fa_bwd with identical arguments, results and rules
+ * apart from the workspace.
+ *   Scratch comes from a fixed array inside the library's device image of
+ *   fa_bwd_noalloc_max_scratch_bytes() bytes (64 MiB), held on every GPU that
+ *   loads the library until the process exits.  A problem whose
+ *   fa_bwd_workspace_size() exceeds it is rejected with FA_ERR_WORKSPACE
+ *   before anything is launched.
+ *   The first call on a device looks the array's device address up (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU race and
+ *   must be ordered by the caller.  Nothing needs clearing between calls;
+ *   each call rewrites the scratch it reads.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+FA_API fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                const float *lse, const void *dout, void *dq, void *dk,
+                                void *dv, int B, int H, int N, int d, float scale, int causal,
+                                const int32_t *kv_len, const uint8_t *block_mask, void *stream);
+
+/* Size in bytes of fa_bwd_noalloc's fixed scratch array (its maximum workspace). */
+FA_API size_t fa_bwd_noalloc_max_scratch_bytes(void);
+
+/*
  * Synchronises stream and reports the first device-side error recorded since
  * the previous fa_check: FA_ERR_TIMEOUT when a bounded wait inside a kernel
  * ran out (the kernel then returned early and its outputs are invalid),
