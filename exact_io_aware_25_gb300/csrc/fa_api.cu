@@ -84,6 +84,20 @@ bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows, 64] dQ accumulators as a 2-D tensor {64, rows}; 128 x 32 boxes
+// (128 bytes wide) with 128-byte swizzle.
+bool encode_dq_acc(CUtensorMap *m, const void *ptr, size_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask) {
@@ -205,13 +219,16 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
   a.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
   a.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
   a.dq = static_cast<uint16_t *>(dq);
+  CUtensorMap tdq_acc;
+  if (!encode_dq_acc(&tdq_acc, a.dq_acc, static_cast<size_t>(BH) * a.n_pad)) return FA_ERR_CUDA;
   cudaEvent_t ev0, ev1;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     ev0 = g_bwd_ev_start;
     ev1 = g_bwd_ev_stop;
   }
-  return launch_bwd(tq, tk, tv, tdo, tdk, tdv, a, static_cast<cudaStream_t>(stream), ev0, ev1) ==
+  return launch_bwd(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a, static_cast<cudaStream_t>(stream), ev0,
+                    ev1) ==
                  cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;

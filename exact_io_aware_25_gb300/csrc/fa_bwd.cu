@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 // Warp roles (14 warps):
 //   warps 0-3   P^T / dS^T for queries 0-63 of the step (thread = key row)
 //   warps 4-7   P^T / dS^T for queries 64-127 (same key rows, other columns)
-//   warps 8-11  dQ partials: TMEM -> fp32 vector reductions (thread = query row)
+//   warps 8-11  dQ partials: TMEM -> swizzled shared tile -> TMA reduce-add into the
+//               fp32 accumulators (thread = query row)
 //   warp 12     TMA producer
 //   warp 13     TMEM owner and MMA issuer
 constexpr int kMainThreads = 448;
@@ -114,6 +115,7 @@ struct __align__(1024) BwdSmem {
   uint8_t q[kStages][kTileBytes];
   uint8_t dout[kStages][kTileBytes];
   uint8_t dst[2][2][kTileBytes];         // dS^T bf16, double-buffered; [buf][query half], rows = keys
+  uint8_t dq_stage[2][kTileBytes];       // dQ partial fp32, columns 0-31 | 32-63, rows = queries
   float lse2[kStages][kTile];
   float dsum[kStages][kTile];
   uint64_t bar_kv;
@@ -130,6 +132,7 @@ struct __align__(1024) BwdSmem {
   uint32_t tmem_base;
   int abort;
   int n_tiles;
+  int rot;
   int16_t tiles[kMaxMaskTiles];
 };
 
@@ -139,7 +142,14 @@ constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ
                    kColPT = 448;
 constexpr uint32_t kTmemCols = 512;
 
-__device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) { return s.tiles[it]; }
+// Step it visits query tile tiles[(it + rot) % n]: the key tiles of one head
+// start at different query tiles so their concurrent dQ reduce-adds land on
+// different accumulator rows.
+__device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) {
+  int k = it + s.rot;
+  if (k >= s.n_tiles) k -= s.n_tiles;
+  return s.tiles[k];
+}
 
 // Writes 32 consecutive bf16 (four 16-byte chunks) of row `row` into a
 // [128 rows][128 cols] bf16 tile stored as two 128-byte-swizzled halves.
@@ -158,7 +168,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                       const BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tm_dq_acc, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem &s = *reinterpret_cast<BwdSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -211,7 +221,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         count += __popc(bal);
       }
     }
-    if (lane == 0) s.n_tiles = count;
+    if (lane == 0) {
+      s.n_tiles = count;
+      s.rot = count > 0 ? kt % count : 0;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -414,7 +427,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int it = 0; it < n; ++it) {
       const int i = qtile_at(s, it);
-      if (!mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort)) break;
+      // one decision for all four warps: the barriers below must see all of them
+      if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort))) break;
       tc_fence_after();
       uint32_t r[64];
       tmem_ld32(tmem + lane_base + kColDQ, r);
@@ -422,13 +436,28 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s.bar_dq_free);
-      float *dst = a.dq_acc +
-                   (static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile + qr) * kHeadDim;
+      // the previous step's reduce-adds must have finished reading the stage
+      if (qr == 0) bulk_wait_read_all();
+      named_bar_sync(2, 128);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        red_add_v4(dst + 4 * c, __uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                   __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t base = smem_u32(s.dq_stage[h]);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const int c0 = h * 32 + ch * 4;
+          st_shared_v4(base + sw128_offset(qr, ch), r[c0], r[c0 + 1], r[c0 + 2], r[c0 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      if (qr == 0) {
+        const int row0 = bh * a.n_pad + i * kTile;
+        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
+        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
+        bulk_commit();
+      }
     }
+    if (qr == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -444,8 +473,8 @@ size_t bwd_smem_bytes() { return sizeof(BwdSmem) + 1024; }
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
-                       const BwdArgs &a, cudaStream_t st, cudaEvent_t ev_start,
-                       cudaEvent_t ev_stop) {
+                       const CUtensorMap &tdq_acc, const BwdArgs &a, cudaStream_t st,
+                       cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   static int configured_dev = -1;
   static int num_sms = 0;
   int dev = 0;
@@ -467,7 +496,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
-  fa_bwd_main_kernel<<<grid, kMainThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  fa_bwd_main_kernel<<<grid, kMainThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
   const long long chunks = static_cast<long long>(a.pr.B) * a.pr.H * a.pr.N * (kHeadDim / 8);

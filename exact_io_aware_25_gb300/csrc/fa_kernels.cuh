@@ -57,9 +57,11 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
 
 // ev_start / ev_stop (may be null) are recorded around the main kernel.
+// tdq_acc: the fp32 dQ accumulators [B*H*n_pad, 64] as a 2-D map with 128 x 32
+// boxes and 128-byte swizzle (target of the TMA reduce-adds).
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
-                       const BwdArgs &a, cudaStream_t st, cudaEvent_t ev_start,
-                       cudaEvent_t ev_stop);
+                       const CUtensorMap &tdq_acc, const BwdArgs &a, cudaStream_t st,
+                       cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace fa
