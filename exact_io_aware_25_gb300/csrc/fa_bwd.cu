@@ -100,14 +100,17 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- main kernel
 
-// Warp roles (14 warps):
-//   warps 0-3   P^T / dS^T for queries 0-63 of the step (thread = key row)
-//   warps 4-7   P^T / dS^T for queries 64-127 (same key rows, other columns)
-//   warps 8-11  dQ partials: TMEM -> swizzled shared tile -> TMA reduce-add into the
-//               fp32 accumulators (thread = query row)
-//   warp 12     TMA producer
-//   warp 13     TMEM owner and MMA issuer
-constexpr int kMainThreads = 448;
+// Warp roles (10 warps):
+//   warps 0-3   warpgroup 0: P^T / dS^T for queries 0-63 of the step (thread =
+//               key row), then columns 0-31 of the previous step's dQ partial
+//               (thread = query row): TMEM -> swizzled shared tile -> TMA
+//               reduce-add into the fp32 accumulators
+//   warps 4-7   warpgroup 1: the same for queries 64-127 and dQ columns 32-63
+//   warp 8      TMA producer
+//   warp 9      TMEM owner and MMA issuer
+// Ten warps leave each elementwise thread enough registers to hold all 64 of
+// its S^T and dP^T columns, so a step pays the TMEM load latency only twice.
+constexpr int kMainThreads = 320;
 
 struct __align__(1024) BwdSmem {
   uint8_t k[kTileBytes];                 // K_j (resident); later dK staging
@@ -151,16 +154,46 @@ __device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) {
   return s.tiles[k];
 }
 
-// Writes 32 consecutive bf16 (four 16-byte chunks) of row `row` into a
-// [128 rows][128 cols] bf16 tile stored as two 128-byte-swizzled halves.
-__device__ __forceinline__ void store_row32(uint8_t (*tile)[kTileBytes], int row, int c4,
-                                            const uint32_t *w) {
-  const uint32_t base = smem_u32(tile[c4 >> 1]) + row * 128;
+// P^T (bf16 pairs into TMEM) and dS^T (bf16 into the swizzled shared tile)
+// for 32 query columns starting at qc, from this thread's S^T / dP^T values:
+//   P^T = 2^(S^T * scale * log2(e) - lse2_q),  dS^T = P^T o (dP^T - D_q).
+// kMask selects the edge-tile body (keys past kv_len, causal diagonal); the
+// common body carries no masking work at all.
+template <bool kMask>
+__device__ __forceinline__ void emit_pds32(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                           int qc, int half, int kr, bool key_ok, bool diag,
+                                           float sl2, uint32_t lse2, uint32_t dsum,
+                                           uint32_t tmem_pt, uint32_t ds_row) {
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t ch = (c4 & 1) * 4 + t;
-    st_shared_v4(base + ((ch ^ (row & 7)) << 4), w[4 * t], w[4 * t + 1], w[4 * t + 2],
-                 w[4 * t + 3]);
+  for (int c = 0; c < 2; ++c) {
+    uint32_t pw[8], dw[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int e0 = c * 16 + 4 * g;
+      const float4 l4 = ld_shared_f4(lse2 + (qc + e0) * 4);
+      const float4 d4 = ld_shared_f4(dsum + (qc + e0) * 4);
+      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+      float p[4], ds[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        p[u] = ex2_approx(fmaf(__uint_as_float(sr[e0 + u]), sl2, -lv[u]));
+        if (kMask) {
+          const bool masked = !key_ok || (diag && kr > qc + e0 + u);
+          p[u] = masked ? 0.f : p[u];
+        }
+        ds[u] = p[u] * (__uint_as_float(dr[e0 + u]) - dv4[u]);
+      }
+      pw[2 * g] = pack_bf16(p[0], p[1]);
+      pw[2 * g + 1] = pack_bf16(p[2], p[3]);
+      dw[2 * g] = pack_bf16(ds[0], ds[1]);
+      dw[2 * g + 1] = pack_bf16(ds[2], ds[3]);
+    }
+    const int q16 = qc + c * 16;  // first of these 16 columns
+    tmem_st8(tmem_pt + (q16 >> 1), pw);
+    const uint32_t ch0 = static_cast<uint32_t>((q16 - half * 64) >> 3);
+    st_shared_v4(ds_row + ((ch0 ^ (kr & 7)) << 4), dw[0], dw[1], dw[2], dw[3]);
+    st_shared_v4(ds_row + (((ch0 + 1) ^ (kr & 7)) << 4), dw[4], dw[5], dw[6], dw[7]);
   }
 }
 
@@ -193,14 +226,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&s.bar_ds_free[0], 1);
     mbar_init(&s.bar_ds_free[1], 1);
     mbar_init(&s.bar_dq_full, 1);
-    mbar_init(&s.bar_dq_free, 128);
+    mbar_init(&s.bar_dq_free, 256);
     mbar_init(&s.bar_done, 1);
     mbar_init(&s.bar_final, 1);
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 13) tmem_alloc(&s.tmem_base, kTmemCols);
-  if (warp == 12 && lane == 0) {
+  if (warp == 9) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -232,7 +265,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 12) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
@@ -251,7 +284,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
       }
     }
-  } else if (warp == 13) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -321,72 +354,102 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_wait_drain(&s.bar_final, 0, pr.wait);
     }
     __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ P^T / dS^T (rows = keys)
+  } else {
+    // ------------------------------------------------------------ elementwise + dQ readout
     const int half = warp >> 2;            // query columns 64*half .. 64*half+63
-    const int kr = (warp & 3) * 32 + lane; // key row == TMEM lane
+    const int kr = (warp & 3) * 32 + lane; // TMEM lane: key row (S^T, dP^T) / query row (dQ)
+    const uint32_t wg_bar = 2 + half;      // named barrier of this warpgroup
     const int key = kt * kTile + kr;
     const bool key_ok = key < kv_bound;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = pr.scale_log2;
+    // Every wait of this warpgroup takes one decision for all four warps, so the
+    // named barriers inside the loop are always reached by all of them.
+    auto wg_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return named_bar_and(wg_bar, 128, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
+    };
+    // dQ partial of step `step`: this warpgroup's 32 columns, all 128 query rows.
+    auto dq_readout = [&](int step) -> bool {
+      if (!wg_wait(&s.bar_dq_full, step & 1)) return false;
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + kColDQ + half * 32, r);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s.bar_dq_free);
+      if (kr == 0) bulk_wait_read_all();  // the previous reduce-add has read the stage
+      named_bar_sync(wg_bar, 128);
+      const uint32_t base = smem_u32(s.dq_stage[half]);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(base + sw128_offset(kr, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
+                     r[4 * ch + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(wg_bar, 128);
+      if (kr == 0) {
+        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[half], half * 32,
+                          bh * a.n_pad + qtile_at(s, step) * kTile);
+        bulk_commit();
+      }
+      return true;
+    };
     bool ok = true;
-    for (int it = 0; it < n && ok; ++it) {
+    for (int it = 0; it < n; ++it) {
       const int st = it % kStages;
       const int buf = it & 1;
       const int i = qtile_at(s, it);
-      if (!mbar_wait_warp(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort) ||
-          !mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort)) {
+      if (!wg_wait(&s.bar_q_full[st], (it / kStages) & 1) || !wg_wait(&s.bar_s_full, it & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const bool diag = pr.causal && (i == kt);
-      const float *lse2 = s.lse2[st];
-      const float *dsum = s.dsum[st];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int q0 = half * 64 + c * 32;  // first query column of this chunk
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + kColST + q0, sr);
-        tmem_ld32(tmem + lane_base + kColDPT + q0, dr);
+      const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+      const uint32_t t_s = tmem + lane_base + kColST + half * 64;
+      const uint32_t t_dp = tmem + lane_base + kColDPT + half * 64;
+      uint32_t sa[32], da[32], sb[32], db[32];
+      tmem_ld32(t_s, sa);
+      tmem_ld32(t_dp, da);
+      tmem_wait_ld_tied32(sa, da);
+      tmem_ld32(t_s + 32, sb);   // second half in flight while the first is computed
+      tmem_ld32(t_dp + 32, db);
+      // P^T columns free once dV(it-1) is done; dS^T buffer once dK/dQ(it-2) are
+      if ((it > 0 && !wg_wait(&s.bar_pt_free, (it - 1) & 1)) ||
+          (it > 1 && !wg_wait(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1))) {
         tmem_wait_ld();
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float p2[2], d2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int ql = q0 + t + u;
-            float p = ex2_approx(fmaf(__uint_as_float(sr[t + u]), sl2, -lse2[ql]));
-            const bool masked = !key_ok || (diag && kr > ql);
-            p = masked ? 0.f : p;
-            p2[u] = p;
-            d2[u] = p * (__uint_as_float(dr[t + u]) - dsum[ql]);
-          }
-          pw[t >> 1] = pack_bf16(p2[0], p2[1]);
-          dw[t >> 1] = pack_bf16(d2[0], d2[1]);
-        }
-        if (c == 0) {
-          // P^T columns free once dV(it-1) is done; dS^T buffer once dK/dQ(it-2) are
-          if ((it > 0 && !mbar_wait_warp(&s.bar_pt_free, (it - 1) & 1, pr.wait, &s.abort)) ||
-              (it > 1 && !mbar_wait_warp(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1, pr.wait,
-                                         &s.abort))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        tmem_st16(tmem + lane_base + kColPT + (q0 >> 1), pw);
-        store_row32(s.dst[buf], kr, half * 2 + c, dw);
+        ok = false;
+        break;
       }
-      if (!ok) break;
+      tc_fence_after();
+      const uint32_t ds_row = smem_u32(s.dst[buf][half]) + kr * 128;
+      const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
+      const uint32_t t_pt = tmem + lane_base + kColPT;
+      if (need_mask) {
+        emit_pds32<true>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt, ds_row);
+        tmem_wait_ld_tied32(sb, db);
+        emit_pds32<true>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
+                         ds_row);
+      } else {
+        emit_pds32<false>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
+                          ds_row);
+        tmem_wait_ld_tied32(sb, db);
+        emit_pds32<false>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
+                          ds_row);
+      }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.bar_pds_full);
+      // while the tensor core computes the next step's S^T and dP^T
+      if (it > 0 && !dq_readout(it - 1)) {
+        ok = false;
+        break;
+      }
     }
-    // ---------------------------------------------------------- epilogue: dV (warps 0-3), dK (4-7)
-    if (ok && n > 0) ok = mbar_wait_warp(&s.bar_done, 0, pr.wait, &s.abort);
+    if (ok && n > 0) ok = dq_readout(n - 1);
+    if (kr == 0) bulk_wait_all();
+    // ---------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
+    if (ok && n > 0) ok = wg_wait(&s.bar_done, 0);
     if (ok) {
       tc_fence_after();
       const uint32_t col = half == 0 ? kColDV : kColDK;
@@ -421,47 +484,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       bulk_commit();
       bulk_wait_all();
     }
-  } else {
-    // ------------------------------------------------------------ dQ partials (rows = queries)
-    const int qr = tid - 256;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int it = 0; it < n; ++it) {
-      const int i = qtile_at(s, it);
-      // one decision for all four warps: the barriers below must see all of them
-      if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort))) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(tmem + lane_base + kColDQ, r);
-      tmem_ld32(tmem + lane_base + kColDQ + 32, r + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s.bar_dq_free);
-      // the previous step's reduce-adds must have finished reading the stage
-      if (qr == 0) bulk_wait_read_all();
-      named_bar_sync(2, 128);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t base = smem_u32(s.dq_stage[h]);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int c0 = h * 32 + ch * 4;
-          st_shared_v4(base + sw128_offset(qr, ch), r[c0], r[c0 + 1], r[c0 + 2], r[c0 + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      if (qr == 0) {
-        const int row0 = bh * a.n_pad + i * kTile;
-        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
-        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
-        bulk_commit();
-      }
-    }
-    if (qr == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
