@@ -100,17 +100,19 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- main kernel
 
-// Warp roles (10 warps):
-//   warps 0-3   warpgroup 0: P^T / dS^T for queries 0-63 of the step (thread =
-//               key row), then columns 0-31 of the previous step's dQ partial
-//               (thread = query row): TMEM -> swizzled shared tile -> TMA
-//               reduce-add into the fp32 accumulators
-//   warps 4-7   warpgroup 1: the same for queries 64-127 and dQ columns 32-63
-//   warp 8      TMA producer
-//   warp 9      TMEM owner and MMA issuer
-// Ten warps leave each elementwise thread enough registers to hold all 64 of
-// its S^T and dP^T columns, so a step pays the TMEM load latency only twice.
-constexpr int kMainThreads = 320;
+// Warp roles (16 warps, four warpgroups):
+//   warpgroup 0 (warps 0-3)   P^T / dS^T for queries 0-63 of the step (thread = key row)
+//   warpgroup 1 (warps 4-7)   the same for queries 64-127
+//   warpgroup 2 (warps 8-11)  dQ partial: TMEM -> swizzled shared tile -> TMA
+//                             reduce-add into the fp32 accumulators (thread = query row)
+//   warpgroup 3: warp 12      TMA producer
+//                warp 13      TMEM owner and MMA issuer
+//                warps 14-15  idle
+// Launched at 128 registers per thread; the elementwise warpgroups then take
+// 168 (room for all 64 S^T and dP^T columns of a thread), the dQ warpgroup
+// keeps 96 and the producer / MMA warpgroup 80: 168 + 168 + 96 + 80 = 4 x 128.
+constexpr int kMainThreads = 512;
+constexpr uint32_t kRegsElementwise = 168, kRegsDq = 96, kRegsControl = 80;
 
 struct __align__(1024) BwdSmem {
   uint8_t k[kTileBytes];                 // K_j (resident); later dK staging
@@ -125,6 +127,7 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_q_full[kStages];
   uint64_t bar_q_empty[kStages];
   uint64_t bar_s_full;
+  uint64_t bar_st_read;    // elementwise warps hold S^T / dP^T in registers
   uint64_t bar_pds_full;
   uint64_t bar_pt_free;
   uint64_t bar_ds_free[2];
@@ -221,19 +224,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_init(&s.bar_q_empty[i], 1);
     }
     mbar_init(&s.bar_s_full, 1);
+    mbar_init(&s.bar_st_read, 256);
     mbar_init(&s.bar_pds_full, 256);
     mbar_init(&s.bar_pt_free, 1);
     mbar_init(&s.bar_ds_free[0], 1);
     mbar_init(&s.bar_ds_free[1], 1);
     mbar_init(&s.bar_dq_full, 1);
-    mbar_init(&s.bar_dq_free, 256);
+    mbar_init(&s.bar_dq_free, 128);
     mbar_init(&s.bar_done, 1);
     mbar_init(&s.bar_final, 1);
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&s.tmem_base, kTmemCols);
-  if (warp == 8 && lane == 0) {
+  if (warp == 13) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -265,100 +269,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
-      tma_load_3d(s.k, &tm_k, &s.bar_kv, 0, kt * kTile, bh);
-      tma_load_3d(s.v, &tm_v, &s.bar_kv, 0, kt * kTile, bh);
-      for (int it = 0; it < n; ++it) {
-        const int st = it % kStages;
-        const uint32_t use = it / kStages;
-        if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
-        const int i = qtile_at(s, it);
-        const size_t stat = static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile;
-        mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
-        tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, bh);
-        tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, bh);
-        bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
-        bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step it.
-      auto issue_s = [&](int it) -> bool {
-        const int st = it % kStages;
-        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
-                      sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
-                      sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
-        mma_commit(&s.bar_s_full);
-        return true;
-      };
-      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort) && issue_s(0);
-      for (int it = 0; ok && it < n; ++it) {
-        const int st = it % kStages;
-        const int buf = it & 1;
-        // P^T(it) is in TMEM, dS^T(it) in shared memory, and S^T / dP^T(it)
-        // have been read: start the next step's S^T, dP^T first so the
-        // elementwise warps can begin while dV, dK, dQ of this step run.
-        if (!mbar_wait(&s.bar_pds_full, it & 1, pr.wait, &s.abort)) break;
-        tc_fence_after();
-        if (it + 1 < n && !issue_s(it + 1)) break;
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
-        // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per step),
-        // B = dO_i (queries x d, d contiguous: MN-major).
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                      sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
-        mma_commit(&s.bar_pt_free);
-        // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[buf][kk >> 2]) + off, 16, 1024),
-                      sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
-        }
-        mma_commit(&s.bar_q_empty[st]);
-        if (it > 0 && !mbar_wait(&s.bar_dq_free, (it - 1) & 1, pr.wait, &s.abort)) break;
-        tc_fence_after();
-        // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major operand
-        // (queries contiguous, two 64-query halves 16 KiB apart); B = K_j,
-        // MN-major (d contiguous).  K dimension = keys, 16 per instruction.
-        const uint32_t ds_addr = smem_u32(s.dst[buf][0]);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
-                      sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
-        mma_commit(&s.bar_dq_full);
-        mma_commit(&s.bar_ds_free[buf]);
-      }
-      mma_commit(&s.bar_done);
-    }
-    if (lane == 0) {
-      mma_commit(&s.bar_final);
-      mbar_wait_drain(&s.bar_final, 0, pr.wait);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ elementwise + dQ readout
+  if (warp < 8) {
+    setmaxnreg_inc<kRegsElementwise>();
+    // ------------------------------------------------------------ elementwise
     const int half = warp >> 2;            // query columns 64*half .. 64*half+63
-    const int kr = (warp & 3) * 32 + lane; // TMEM lane: key row (S^T, dP^T) / query row (dQ)
-    const uint32_t wg_bar = 2 + half;      // named barrier of this warpgroup
+    const int kr = (warp & 3) * 32 + lane; // TMEM lane: key row
+    const uint32_t wg_bar = 3 + half;      // named barrier of this warpgroup
     const int key = kt * kTile + kr;
     const bool key_ok = key < kv_bound;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -367,31 +283,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // named barriers inside the loop are always reached by all of them.
     auto wg_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return named_bar_and(wg_bar, 128, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
-    };
-    // dQ partial of step `step`: this warpgroup's 32 columns, all 128 query rows.
-    auto dq_readout = [&](int step) -> bool {
-      if (!wg_wait(&s.bar_dq_full, step & 1)) return false;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + kColDQ + half * 32, r);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s.bar_dq_free);
-      if (kr == 0) bulk_wait_read_all();  // the previous reduce-add has read the stage
-      named_bar_sync(wg_bar, 128);
-      const uint32_t base = smem_u32(s.dq_stage[half]);
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(base + sw128_offset(kr, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
-                     r[4 * ch + 3]);
-      fence_proxy_async_smem();
-      named_bar_sync(wg_bar, 128);
-      if (kr == 0) {
-        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[half], half * 32,
-                          bh * a.n_pad + qtile_at(s, step) * kTile);
-        bulk_commit();
-      }
-      return true;
     };
     bool ok = true;
     for (int it = 0; it < n; ++it) {
@@ -427,12 +318,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (need_mask) {
         emit_pds32<true>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt, ds_row);
         tmem_wait_ld_tied32(sb, db);
+        tc_fence_before();
+        mbar_arrive(&s.bar_st_read);
         emit_pds32<true>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
                          ds_row);
       } else {
         emit_pds32<false>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
                           ds_row);
         tmem_wait_ld_tied32(sb, db);
+        tc_fence_before();
+        mbar_arrive(&s.bar_st_read);
         emit_pds32<false>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
                           ds_row);
       }
@@ -440,14 +335,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&s.bar_pds_full);
-      // while the tensor core computes the next step's S^T and dP^T
-      if (it > 0 && !dq_readout(it - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && n > 0) ok = dq_readout(n - 1);
-    if (kr == 0) bulk_wait_all();
     // ---------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
     if (ok && n > 0) ok = wg_wait(&s.bar_done, 0);
     if (ok) {
@@ -484,10 +372,143 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       bulk_commit();
       bulk_wait_all();
     }
+  } else if (warp < 12) {
+    setmaxnreg_dec<kRegsDq>();
+    // ------------------------------------------------------------ dQ partials (rows = queries)
+    const int qr = tid - 256;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int it = 0; it < n; ++it) {
+      const int i = qtile_at(s, it);
+      // one decision for all four warps: the barriers below must see all of them
+      if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort))) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + lane_base + kColDQ, r0);
+      tmem_ld32(tmem + lane_base + kColDQ + 32, r1);
+      tmem_wait_ld_tied32(r0, r1);
+      tc_fence_before();
+      mbar_arrive(&s.bar_dq_free);
+      // the previous step's reduce-adds must have finished reading the stage
+      if (qr == 0) bulk_wait_read_all();
+      named_bar_sync(2, 128);
+      const uint32_t b0 = smem_u32(s.dq_stage[0]), b1 = smem_u32(s.dq_stage[1]);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        st_shared_v4(b0 + sw128_offset(qr, ch), r0[4 * ch], r0[4 * ch + 1], r0[4 * ch + 2],
+                     r0[4 * ch + 3]);
+        st_shared_v4(b1 + sw128_offset(qr, ch), r1[4 * ch], r1[4 * ch + 1], r1[4 * ch + 2],
+                     r1[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      if (qr == 0) {
+        const int row0 = bh * a.n_pad + i * kTile;
+        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
+        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
+        bulk_commit();
+      }
+    }
+      if (qr == 0) bulk_wait_all();
+  } else {
+    setmaxnreg_dec<kRegsControl>();
+    if (warp == 12) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
+      tma_load_3d(s.k, &tm_k, &s.bar_kv, 0, kt * kTile, bh);
+      tma_load_3d(s.v, &tm_v, &s.bar_kv, 0, kt * kTile, bh);
+      for (int it = 0; it < n; ++it) {
+        const int st = it % kStages;
+        const uint32_t use = it / kStages;
+        if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
+        const int i = qtile_at(s, it);
+        const size_t stat = static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile;
+        mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
+        tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, bh);
+        tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, bh);
+        bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
+        bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
+      }
+    }
+    } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
+      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
+      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step it.
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % kStages;
+        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
+                      sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
+        mma_commit(&s.bar_s_full);
+        return true;
+      };
+      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort) && issue_s(0);
+      for (int it = 0; ok && it < n; ++it) {
+        const int st = it % kStages;
+        const int buf = it & 1;
+        // S^T / dP^T(it) are in the elementwise warps' registers: the next
+        // step's S^T, dP^T can overwrite them while P^T / dS^T(it) are built.
+        if (it + 1 < n) {
+          if (!mbar_wait(&s.bar_st_read, it & 1, pr.wait, &s.abort)) break;
+          tc_fence_after();
+          if (!issue_s(it + 1)) break;
+        }
+        // P^T(it) is in TMEM and dS^T(it) in shared memory.
+        if (!mbar_wait(&s.bar_pds_full, it & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+        // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per step),
+        // B = dO_i (queries x d, d contiguous: MN-major).
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
+                      sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
+        mma_commit(&s.bar_pt_free);
+        // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[buf][kk >> 2]) + off, 16, 1024),
+                      sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
+        }
+        mma_commit(&s.bar_q_empty[st]);
+        if (it > 0 && !mbar_wait(&s.bar_dq_free, (it - 1) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major operand
+        // (queries contiguous, two 64-query halves 16 KiB apart); B = K_j,
+        // MN-major (d contiguous).  K dimension = keys, 16 per instruction.
+        const uint32_t ds_addr = smem_u32(s.dst[buf][0]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
+                      sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
+        mma_commit(&s.bar_dq_full);
+        mma_commit(&s.bar_ds_free[buf]);
+      }
+      mma_commit(&s.bar_done);
+    }
+    if (lane == 0) {
+      mma_commit(&s.bar_final);
+      mbar_wait_drain(&s.bar_final, 0, pr.wait);
+    }
+    __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -153,6 +153,16 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
+// Warpgroup register reallocation: every warp of the warpgroup executes it.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
