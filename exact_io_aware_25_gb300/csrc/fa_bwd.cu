@@ -128,7 +128,8 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_q_empty[kStages];
   uint64_t bar_s_full;
   uint64_t bar_st_read;    // elementwise warps hold S^T / dP^T in registers
-  uint64_t bar_pds_full;
+  uint64_t bar_p_full;     // P^T of the step is in TMEM
+  uint64_t bar_ds_full;    // dS^T of the step is in shared memory
   uint64_t bar_pt_free;
   uint64_t bar_ds_free[2];
   uint64_t bar_dq_full;
@@ -157,44 +158,62 @@ __device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) {
   return s.tiles[k];
 }
 
-// P^T (bf16 pairs into TMEM) and dS^T (bf16 into the swizzled shared tile)
-// for 32 query columns starting at qc, from this thread's S^T / dP^T values:
-//   P^T = 2^(S^T * scale * log2(e) - lse2_q),  dS^T = P^T o (dP^T - D_q).
+// Elementwise phase 1 for 32 query columns starting at qc: S^T values in
+// `v` are replaced, in place, by P^T = 2^(S^T * scale * log2(e) - lse2_q).
 // kMask selects the edge-tile body (keys past kv_len, causal diagonal); the
 // common body carries no masking work at all.
 template <bool kMask>
-__device__ __forceinline__ void emit_pds32(const uint32_t (&sr)[32], const uint32_t (&dr)[32],
-                                           int qc, int half, int kr, bool key_ok, bool diag,
-                                           float sl2, uint32_t lse2, uint32_t dsum,
-                                           uint32_t tmem_pt, uint32_t ds_row) {
+__device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int kr, bool key_ok,
+                                           bool diag, float sl2, uint32_t lse2) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 l4 = ld_shared_f4(lse2 + (qc + 4 * g) * 4);
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float p = ex2_approx(fmaf(__uint_as_float(v[4 * g + u]), sl2, -lv[u]));
+      if (kMask) {
+        const bool masked = !key_ok || (diag && kr > qc + 4 * g + u);
+        p = masked ? 0.f : p;
+      }
+      v[4 * g + u] = __float_as_uint(p);
+    }
+  }
+}
+
+// P^T of 32 columns as bf16 pairs into the TMEM P^T columns.
+__device__ __forceinline__ void store_p32(const uint32_t (&v)[32], int qc, uint32_t tmem_pt) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    uint32_t pw[8], dw[8];
+    uint32_t pw[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      pw[t] = pack_bf16(__uint_as_float(v[16 * c + 2 * t]), __uint_as_float(v[16 * c + 2 * t + 1]));
+    tmem_st8(tmem_pt + ((qc + 16 * c) >> 1), pw);
+  }
+}
+
+// Elementwise phase 2: dS^T = P^T o (dP^T - D_q) for 32 columns, bf16 into
+// row kr of this warpgroup's 128-byte-swizzled dS^T tile.
+__device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint32_t (&dv)[32],
+                                           int qc, int half, int kr, uint32_t dsum,
+                                           uint32_t ds_row) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t dw[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const int e0 = c * 16 + 4 * g;
-      const float4 l4 = ld_shared_f4(lse2 + (qc + e0) * 4);
+      const int e0 = 16 * c + 4 * g;
       const float4 d4 = ld_shared_f4(dsum + (qc + e0) * 4);
-      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-      const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-      float p[4], ds[4];
+      const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+      float ds[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        p[u] = ex2_approx(fmaf(__uint_as_float(sr[e0 + u]), sl2, -lv[u]));
-        if (kMask) {
-          const bool masked = !key_ok || (diag && kr > qc + e0 + u);
-          p[u] = masked ? 0.f : p[u];
-        }
-        ds[u] = p[u] * (__uint_as_float(dr[e0 + u]) - dv4[u]);
-      }
-      pw[2 * g] = pack_bf16(p[0], p[1]);
-      pw[2 * g + 1] = pack_bf16(p[2], p[3]);
+      for (int u = 0; u < 4; ++u)
+        ds[u] = __uint_as_float(pv[e0 + u]) * (__uint_as_float(dv[e0 + u]) - dl[u]);
       dw[2 * g] = pack_bf16(ds[0], ds[1]);
       dw[2 * g + 1] = pack_bf16(ds[2], ds[3]);
     }
-    const int q16 = qc + c * 16;  // first of these 16 columns
-    tmem_st8(tmem_pt + (q16 >> 1), pw);
-    const uint32_t ch0 = static_cast<uint32_t>((q16 - half * 64) >> 3);
+    const uint32_t ch0 = static_cast<uint32_t>((qc + 16 * c - half * 64) >> 3);
     st_shared_v4(ds_row + ((ch0 ^ (kr & 7)) << 4), dw[0], dw[1], dw[2], dw[3]);
     st_shared_v4(ds_row + (((ch0 + 1) ^ (kr & 7)) << 4), dw[4], dw[5], dw[6], dw[7]);
   }
@@ -225,7 +244,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     mbar_init(&s.bar_s_full, 1);
     mbar_init(&s.bar_st_read, 256);
-    mbar_init(&s.bar_pds_full, 256);
+    mbar_init(&s.bar_p_full, 256);
+    mbar_init(&s.bar_ds_full, 256);
     mbar_init(&s.bar_pt_free, 1);
     mbar_init(&s.bar_ds_free[0], 1);
     mbar_init(&s.bar_ds_free[1], 1);
@@ -304,37 +324,37 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tmem_wait_ld_tied32(sa, da);
       tmem_ld32(t_s + 32, sb);   // second half in flight while the first is computed
       tmem_ld32(t_dp + 32, db);
-      // P^T columns free once dV(it-1) is done; dS^T buffer once dK/dQ(it-2) are
-      if ((it > 0 && !wg_wait(&s.bar_pt_free, (it - 1) & 1)) ||
-          (it > 1 && !wg_wait(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1))) {
-        tmem_wait_ld();
+      const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
+      // phase 1: P^T, in place over the S^T registers
+      if (need_mask) p_from_s32<true>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
+      else p_from_s32<false>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
+      tmem_wait_ld_tied32(sb, db);
+      tc_fence_before();
+      mbar_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
+      if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
+      else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
+      // the P^T columns are free once dV(it-1) has read them
+      if (it > 0 && !wg_wait(&s.bar_pt_free, (it - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t ds_row = smem_u32(s.dst[buf][half]) + kr * 128;
-      const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
       const uint32_t t_pt = tmem + lane_base + kColPT;
-      if (need_mask) {
-        emit_pds32<true>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt, ds_row);
-        tmem_wait_ld_tied32(sb, db);
-        tc_fence_before();
-        mbar_arrive(&s.bar_st_read);
-        emit_pds32<true>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
-                         ds_row);
-      } else {
-        emit_pds32<false>(sa, da, half * 64, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
-                          ds_row);
-        tmem_wait_ld_tied32(sb, db);
-        tc_fence_before();
-        mbar_arrive(&s.bar_st_read);
-        emit_pds32<false>(sb, db, half * 64 + 32, half, kr, key_ok, diag, sl2, lse2_a, dsum_a, t_pt,
-                          ds_row);
-      }
+      store_p32(sa, half * 64, t_pt);
+      store_p32(sb, half * 64 + 32, t_pt);
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&s.bar_pds_full);
+      mbar_arrive(&s.bar_p_full);   // dV(it) may start
+      // phase 2: dS^T; its buffer is free once dK/dQ(it-2) have read it
+      if (it > 1 && !wg_wait(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t ds_row = smem_u32(s.dst[buf][half]) + kr * 128;
+      ds_store32(sa, da, half * 64, half, kr, dsum_a, ds_row);
+      ds_store32(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row);
+      fence_proxy_async_smem();
+      mbar_arrive(&s.bar_ds_full);  // dK(it), dQ(it) may start
     }
     // ---------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
     if (ok && n > 0) ok = wg_wait(&s.bar_done, 0);
@@ -465,8 +485,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           tc_fence_after();
           if (!issue_s(it + 1)) break;
         }
-        // P^T(it) is in TMEM and dS^T(it) in shared memory.
-        if (!mbar_wait(&s.bar_pds_full, it & 1, pr.wait, &s.abort)) break;
+        // P^T(it) is in TMEM.
+        if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
         // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per step),
@@ -476,6 +496,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
                       sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
         mma_commit(&s.bar_pt_free);
+        // dS^T(it) is in shared memory.
+        if (!mbar_wait(&s.bar_ds_full, it & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
         // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
