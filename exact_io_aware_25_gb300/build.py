@@ -51,6 +51,7 @@ def _compile(src: str, verbose: bool) -> str:
            "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
+    cmd[1:1] = os.environ.get("FA_EXTRA_NVCC_FLAGS", "").split()
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -61,7 +62,7 @@ def _compile(src: str, verbose: bool) -> str:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every csrc/*.cu and link libfa.so; returns its path."""
-    if not force and up_to_date():
+    if not force and not os.environ.get("FA_EXTRA_NVCC_FLAGS") and up_to_date():
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = sources()

@@ -11,8 +11,9 @@
 // then only O and the per-row statistic (lse = m + ln l) are written.
 //
 // GB300 mapping (one CTA per (query tile, b*h); 6 warps; two CTAs share an SM:
-// 256 TMEM columns and ~83 KB of shared memory each):
-//   warp 4   TMA producer: Q once, then K_j / V_j into a 2-stage ring.
+// 256 TMEM columns and ~99 KB of shared memory each):
+//   warp 4   TMA producer: Q once, then K_j (3-stage ring, one tile ahead) and
+//            V_j (2-stage ring).
 //   warp 5   TMEM owner and MMA issuer: S = Q K_j^T (M=128, N=128, K=64)
 //            into TMEM, and O += P~ V_j (M=128, N=64, K=128) with P~ read
 //            straight from TMEM (A operand in tensor memory).  S_{j+1} is
@@ -30,18 +31,21 @@
 namespace fa {
 namespace {
 
-constexpr int kStages = 2;
+// K ring 3 deep (a slot frees as soon as S = Q K^T has read it), V ring 2
+// deep (frees after PV); the producer keeps K one tile ahead of V.
+constexpr int kKStages = 3, kVStages = 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
 
 struct __align__(1024) FwdSmem {
   uint8_t q[kTileBytes];              // Q_i; reused to stage O for the TMA store
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
   uint64_t bar_q;
-  uint64_t bar_k_full[kStages];
-  uint64_t bar_v_full[kStages];
-  uint64_t bar_kv_empty[kStages];
+  uint64_t bar_k_full[kKStages];
+  uint64_t bar_k_empty[kKStages];
+  uint64_t bar_v_full[kVStages];
+  uint64_t bar_v_empty[kVStages];
   uint64_t bar_s_full;
   uint64_t bar_s_free;
   uint64_t bar_p_full;
@@ -59,6 +63,54 @@ constexpr uint32_t kColS = 0, kColP = 128, kColO = 192, kTmemCols = 256;
 __device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
   return sparse ? static_cast<int>(s.tiles[it]) : it;
 }
+
+// The running reference max of a row is only moved when the row max exceeds
+// it by more than this (base-2 units), so P~ <= 2^8 and the O rescale is rare.
+// Exact: O / l and lse use the same reference.
+constexpr float kLazyRescale = 8.f;
+
+// 2^x for x in [-126, 9) without the MUFU unit: n = round(x) from the
+// 1.5 * 2^23 rounding trick, f = x - n in [-1/2, 1/2], 2^f by a degree-4
+// polynomial (Chebyshev interpolation of 2^f at 5 nodes, coefficients from
+// gen_exp2_poly.py; relative error below 4e-6), and n added to the exponent
+// field.  Inputs below -126 are clamped (result ~1e-38, never used where an
+// exact 0 is required: edge tiles take the MUFU path).
+__device__ __forceinline__ float exp2_poly(float x) {
+  constexpr float c0 = 1.000000000e+00f, c1 = 6.931210160e-01f, c2 = 2.402234972e-01f,
+                  c3 = 5.592197552e-02f, c4 = 9.666368365e-03f;
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;
+  const float n = t - 12582912.f;
+  const float r = x - n;
+  const float q = fmaf(fmaf(fmaf(fmaf(c4, r, c3), r, c2), r, c1), r, c0);
+  const int ni = __float_as_int(t) - 0x4B400000;
+  return __int_as_float(__float_as_int(q) + (ni << 23));
+}
+
+// Exponentials of one 64-column half of a row: sv[c] <- 2^(sv[c]*sl2 - m),
+// accumulated into the eight partial sums and packed to bf16 pairs.  In every
+// group of eight columns the first kPoly use exp2_poly (FMA pipe), the rest
+// the MUFU unit, to balance the two pipes.
+template <int kPoly>
+__device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
+                                         float (&rs8)[8], uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int c = half * 64; c < half * 64 + 64; c += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float x = fmaf(sv[c + u], sl2, -m);
+      sv[c + u] = (u < kPoly) ? exp2_poly(x) : ex2_approx(x);
+      rs8[u] += sv[c + u];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u += 2) pk[((c - half * 64) + u) >> 1] = pack_bf16(sv[c + u], sv[c + u + 1]);
+  }
+}
+
+#ifndef FA_FWD_POLY_PER8
+#define FA_FWD_POLY_PER8 0
+#endif
+constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -79,10 +131,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (tid == 0) {
     mbar_init(&s.bar_q, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&s.bar_k_full[i], 1);
+      mbar_init(&s.bar_k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&s.bar_v_full[i], 1);
-      mbar_init(&s.bar_kv_empty[i], 1);
+      mbar_init(&s.bar_v_empty[i], 1);
     }
     mbar_init(&s.bar_s_full, 1);
     mbar_init(&s.bar_s_free, 128);
@@ -130,15 +185,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(&s.bar_q, kTileBytes);
       tma_load_3d(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
       if (!args.starve) {
-        for (int it = 0; it < n; ++it) {
-          const int st = it % kStages;
-          const uint32_t use = it / kStages;
-          if (use > 0 && !mbar_wait(&s.bar_kv_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
-          const int j = tile_at(s, sparse, it);
+        auto load_k = [&](int it) -> bool {
+          const int st = it % kKStages;
+          const uint32_t use = it / kKStages;
+          if (use > 0 && !mbar_wait(&s.bar_k_empty[st], (use - 1) & 1, pr.wait, &s.abort))
+            return false;
           mbar_arrive_expect_tx(&s.bar_k_full[st], kTileBytes);
-          tma_load_3d(s.k[st], &tm_k, &s.bar_k_full[st], 0, j * kTile, bh);
+          tma_load_3d(s.k[st], &tm_k, &s.bar_k_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
+          return true;
+        };
+        bool ok = load_k(0);
+        for (int it = 0; ok && it < n; ++it) {
+          if (it + 1 < n && !load_k(it + 1)) break;
+          const int st = it % kVStages;
+          const uint32_t use = it / kVStages;
+          if (use > 0 && !mbar_wait(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
           mbar_arrive_expect_tx(&s.bar_v_full[st], kTileBytes);
-          tma_load_3d(s.v[st], &tm_v, &s.bar_v_full[st], 0, j * kTile, bh);
+          tma_load_3d(s.v[st], &tm_v, &s.bar_v_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
         }
       }
     }
@@ -151,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = mbar_wait(&s.bar_q, 0, pr.wait, &s.abort);
       // S_it = Q K_it^T into the S columns.
       auto issue_s = [&](int it) -> bool {
-        const int st = it % kStages;
-        if (!mbar_wait(&s.bar_k_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
+        const int st = it % kKStages;
+        if (!mbar_wait(&s.bar_k_full[st], (it / kKStages) & 1, pr.wait, &s.abort)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(s.k[st]);
 #pragma unroll
@@ -161,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                       sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0);
         }
         mma_commit(&s.bar_s_full);
+        mma_commit(&s.bar_k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -169,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!mbar_wait(&s.bar_s_free, it & 1, pr.wait, &s.abort)) break;
         if (it + 1 < n && !issue_s(it + 1)) break;
         if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
-        const int st = it % kStages;
-        if (!mbar_wait(&s.bar_v_full[st], (it / kStages) & 1, pr.wait, &s.abort)) break;
+        const int st = it % kVStages;
+        if (!mbar_wait(&s.bar_v_full[st], (it / kVStages) & 1, pr.wait, &s.abort)) break;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(s.v[st]);
 #pragma unroll
@@ -182,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                       sdesc_sw128(v_addr + kk * 2048, 1024, 1024), idesc_o, (it > 0 || kk > 0));
         }
         mma_commit(&s.bar_o_done);
-        mma_commit(&s.bar_kv_empty[st]);
+        mma_commit(&s.bar_v_empty[st]);
       }
     }
     if (lane == 0) {
@@ -240,9 +304,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], sv[c + u]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);  // 0 when m = -inf
+      const float m_cand = fmaxf(m, mx * sl2);
+      const bool bump = (m == -INFINITY) || (m_cand > m + kLazyRescale);
+      const float m_ref = bump ? m_cand : m;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float alpha = bump ? ex2_approx(m - m_use) : 1.f;  // 0 when m = -inf
       float rs8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
@@ -251,16 +317,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
-#pragma unroll
-        for (int c = half * 64; c < half * 64 + 64; c += 8) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            sv[c + u] = ex2_approx(fmaf(sv[c + u], sl2, -m_use));
-            rs8[u] += sv[c + u];
-          }
-#pragma unroll
-          for (int u = 0; u < 8; u += 2) pk[((c - half * 64) + u) >> 1] = pack_bf16(sv[c + u], sv[c + u + 1]);
-        }
+        if (edge) exp_half<0>(sv, half, sl2, m_use, rs8, pk);  // exact zeros where masked
+        else exp_half<kPolyPer8>(sv, half, sl2, m_use, rs8, pk);
         if (half == 0 && it > 0) {
           if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
             ok = false;
@@ -286,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tmem_wait_st();
       l = l * alpha + rs;
-      m = m_new;
+      m = m_ref;
       tc_fence_before();
       mbar_arrive(&s.bar_p_full);
     }
