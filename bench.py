@@ -55,15 +55,36 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = {
+    "fa_bwd_main_kernel": ("fa_bwd.cu", "fa_sm103.cuh", "fa_kernels.cuh"),
+    "fa_fwd_kernel": ("fa_fwd.cu", "fa_sm103.cuh", "fa_kernels.cuh"),
+}
+
+
+def _sources_hash(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if one matches."""
+    """DRAM bytes per launch from the committed ncu summary, or None when no
+    capture matches this kernel and workload or the kernel's sources changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        return t.get(f"{kernel}:{workload}")
+            entry = json.load(f).get(f"{kernel}:{workload}")
     except (OSError, ValueError):
         return None
+    if not entry or kernel not in KERNEL_SOURCES:
+        return None
+    if entry.get("sources") != _sources_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return entry.get("bytes")
 
 
 def counted_flops(spec, kv_len, block_mask=None):
