@@ -31,35 +31,53 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
 
-// 8 threads per row: each reads 8 bf16 of O and dO (16 bytes each) and
-// zeroes 8 fp32 accumulators.
+// Preprocess, one (b, h) per blockIdx.y: 8 threads per row, each reading 8
+// bf16 of O and dO (16 bytes each) and zeroing 8 fp32 accumulators.  Each
+// thread takes kRowsPerThread rows, spaced one block-row apart, and issues all
+// their loads before using any, so enough requests are in flight.  Rows past
+// N (up to the 128-row padding) get D = 0 and lse2 = +inf.
+constexpr int kRowsPerThread = 4;
+constexpr int kRowsPerBlock = 256 / 8;  // rows one pass of a block covers
+
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const Problem &pr = a.pr;
-  const long long rows = static_cast<long long>(pr.B) * pr.H * a.n_pad;
+  const int bh = blockIdx.y;
   const int sub = threadIdx.x & 7;
-  // rows is a multiple of 128 and every warp handles 4 consecutive rows, so
-  // the loop below is warp-uniform and the shuffles see all 32 lanes.
-  for (long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; g < rows;
-       g += (static_cast<long long>(gridDim.x) * blockDim.x) >> 3) {
-    const int bh = static_cast<int>(g / a.n_pad);
-    const int i = static_cast<int>(g % a.n_pad);
-    float dsum = 0.f;
-    if (i < pr.N) {
-      const size_t off = (static_cast<size_t>(bh) * pr.N + i) * kHeadDim + sub * 8;
-      const uint4 ov = __ldg(reinterpret_cast<const uint4 *>(a.o + off));
-      const uint4 dv = __ldg(reinterpret_cast<const uint4 *>(a.dout + off));
-      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+  const int r0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
+  const uint16_t *o_head = a.o + static_cast<size_t>(bh) * pr.N * kHeadDim;
+  const uint16_t *do_head = a.dout + static_cast<size_t>(bh) * pr.N * kHeadDim;
+  const size_t ws_row0 = static_cast<size_t>(bh) * a.n_pad;
+  uint4 ov[kRowsPerThread], dv[kRowsPerThread];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(dw[t] << 16), dsum);
-        dsum = fmaf(__uint_as_float(ow[t] & 0xFFFF0000u), __uint_as_float(dw[t] & 0xFFFF0000u), dsum);
-      }
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const int i = r0 + u * kRowsPerBlock;
+    ov[u] = make_uint4(0u, 0u, 0u, 0u);
+    dv[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < pr.N) {
+      ov[u] = __ldg(reinterpret_cast<const uint4 *>(o_head + i * kHeadDim + sub * 8));
+      dv[u] = __ldg(reinterpret_cast<const uint4 *>(do_head + i * kHeadDim + sub * 8));
+    }
+  }
+  // n_pad is a multiple of 128 and the grid covers it exactly: every row
+  // below is in the padded range, and all 32 lanes reach the shuffles.
+#pragma unroll
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const int i = r0 + u * kRowsPerBlock;
+    const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+    const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+    float dsum = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(dw[t] << 16), dsum);
+      dsum = fmaf(__uint_as_float(ow[t] & 0xFFFF0000u), __uint_as_float(dw[t] & 0xFFFF0000u), dsum);
     }
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
-    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + static_cast<size_t>(g) * kHeadDim + sub * 8);
+    const size_t g = ws_row0 + i;
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + g * kHeadDim + sub * 8);
     acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub == 0) {
@@ -76,25 +94,41 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- dQ convert
 
+// dQ = scale * accumulator -> bf16, one (b, h) per blockIdx.y; a thread
+// converts 8 consecutive values of a row (chunk c: row c / 8, part c % 8) for
+// kRowsPerThread chunks spaced one block apart.
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const Problem &pr = a.pr;
-  const long long chunks = static_cast<long long>(pr.B) * pr.H * pr.N * (kHeadDim / 8);
-  for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
-       c += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = c / (kHeadDim / 8);
-    const int part = static_cast<int>(c % (kHeadDim / 8));
-    const int bh = static_cast<int>(row / pr.N);
-    const int i = static_cast<int>(row % pr.N);
-    const float4 *src = reinterpret_cast<const float4 *>(
-        a.dq_acc + (static_cast<size_t>(bh) * a.n_pad + i) * kHeadDim + part * 8);
-    const float4 x = __ldg(src), y = __ldg(src + 1);
-    const float s = pr.scale;
+  const int bh = blockIdx.y;
+  const int chunks = pr.N * (kHeadDim / 8);
+  const int c0 = blockIdx.x * (256 * kRowsPerThread) + threadIdx.x;
+  const float *acc_head = a.dq_acc + static_cast<size_t>(bh) * a.n_pad * kHeadDim;
+  uint16_t *dq_head = a.dq + static_cast<size_t>(bh) * pr.N * kHeadDim;
+  float4 x[kRowsPerThread], y[kRowsPerThread];
+#pragma unroll
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const int c = c0 + u * 256;
+    if (c < chunks) {
+      // the accumulator rows are padded but contiguous within the head, so
+      // chunk c sits at element 8 c
+      const float4 *src = reinterpret_cast<const float4 *>(acc_head + static_cast<size_t>(c) * 8);
+      x[u] = __ldcs(src);
+      y[u] = __ldcs(src + 1);
+    }
+  }
+  const float s = pr.scale;
+#pragma unroll
+  for (int u = 0; u < kRowsPerThread; ++u) {
+    const int c = c0 + u * 256;
+    if (c >= chunks) break;
     uint4 out;
-    out.x = pack_bf16(x.x * s, x.y * s);
-    out.y = pack_bf16(x.z * s, x.w * s);
-    out.z = pack_bf16(y.x * s, y.y * s);
-    out.w = pack_bf16(y.z * s, y.w * s);
-    *reinterpret_cast<uint4 *>(a.dq + static_cast<size_t>(row) * kHeadDim + part * 8) = out;
+    out.x = pack_bf16(x[u].x * s, x[u].y * s);
+    out.y = pack_bf16(x[u].z * s, x[u].w * s);
+    out.z = pack_bf16(y[u].x * s, y[u].y * s);
+    out.w = pack_bf16(y[u].z * s, y[u].w * s);
+    *reinterpret_cast<uint4 *>(dq_head + static_cast<size_t>(c) * 8) = out;
   }
 }
 
@@ -224,6 +258,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        const __grid_constant__ CUtensorMap tm_dq_acc, const BwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   BwdSmem &s = *reinterpret_cast<BwdSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -559,21 +595,19 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  const long long pre_rows = static_cast<long long>(a.pr.B) * a.pr.H * a.n_pad;
-  const long long pre_blocks = (pre_rows * 8 + 255) / 256;
-  const int pre_grid = static_cast<int>(pre_blocks < num_sms * 16LL ? pre_blocks : num_sms * 16LL);
-  fa_bwd_pre_kernel<<<pre_grid, 256, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // preprocess: n_pad / (32 rows x 4) blocks per head cover the padded rows exactly
+  const dim3 pre_grid(a.n_pad / (kRowsPerBlock * kRowsPerThread), a.pr.B * a.pr.H);
+  if ((e = launch_pdl(fa_bwd_pre_kernel, pre_grid, dim3(256), 0, st, a)) != cudaSuccess)
+    return e;
   dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
-  fa_bwd_main_kernel<<<grid, kMainThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(fa_bwd_main_kernel, grid, dim3(kMainThreads), smem, st, tq, tk, tv, tdo, tdk,
+                      tdv, tdq_acc, a)) != cudaSuccess)
+    return e;
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
-  const long long chunks = static_cast<long long>(a.pr.B) * a.pr.H * a.pr.N * (kHeadDim / 8);
-  const long long dq_blocks = (chunks + 255) / 256;
-  const int dq_grid = static_cast<int>(dq_blocks < num_sms * 16LL ? dq_blocks : num_sms * 16LL);
-  fa_bwd_dq_kernel<<<dq_grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  const int chunks = a.pr.N * (kHeadDim / 8);
+  const dim3 dq_grid((chunks + 256 * kRowsPerThread - 1) / (256 * kRowsPerThread), a.pr.B * a.pr.H);
+  return launch_pdl(fa_bwd_dq_kernel, dq_grid, dim3(256), 0, st, a);
 }
 
 }  // namespace fa

@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdArgs args) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   FwdSmem &s = *reinterpret_cast<FwdSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -417,8 +419,7 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     configured_dev = dev;
   }
   dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
-  fa_fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, a);
-  return cudaGetLastError();
+  return launch_pdl(fa_fwd_kernel, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
 }
 
 }  // namespace fa

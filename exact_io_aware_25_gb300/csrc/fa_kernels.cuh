@@ -50,6 +50,33 @@ __device__ __forceinline__ int key_bound(const Problem &p, int b) {
   return L < 0 ? 0 : (L > p.N ? p.N : L);
 }
 
+// Programmatic dependent launch: a kernel of this library may begin launching
+// while the previous kernel on the stream drains.  Each kernel calls
+// pdl_wait() before it reads anything (so results of the previous kernel
+// are complete and visible) and pdl_trigger() to let its own successor
+// start launching.  A successor starts only once every CTA of this kernel
+// has triggered, so it never takes SMs that this kernel still needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 size_t fwd_smem_bytes();
 size_t bwd_smem_bytes();
 
