@@ -132,17 +132,25 @@ Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t dsum, lse2, dq_acc, total;
+  size_t dsum, lse2, dq_acc, col_cnt, col_idx, sched, total;
 };
 
+// Workspace: D and base-2 lse [B*H, n_pad] fp32, dQ accumulators
+// [B*H, n_pad, 64] fp32, and the block-sparse column lists (key tile ->
+// ascending query tiles): counts int32 [nt] and indices int16 [nt, nt]; one
+// int32 work counter for the persistent main kernel.
 WsLayout ws_layout(int B, int H, int N) {
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t n_pad = align_up(static_cast<size_t>(N), kTile);
+  const size_t nt = n_pad / kTile;
   WsLayout w{};
   w.dsum = 0;
   w.lse2 = align_up(w.dsum + bh * n_pad * sizeof(float), 256);
   w.dq_acc = align_up(w.lse2 + bh * n_pad * sizeof(float), 256);
-  w.total = align_up(w.dq_acc + bh * n_pad * kHeadDim * sizeof(float), 256);
+  w.col_cnt = align_up(w.dq_acc + bh * n_pad * kHeadDim * sizeof(float), 256);
+  w.col_idx = align_up(w.col_cnt + nt * sizeof(int), 256);
+  w.sched = align_up(w.col_idx + nt * nt * sizeof(int16_t), 256);
+  w.total = align_up(w.sched + sizeof(int), 256);
   return w;
 }
 
@@ -218,6 +226,9 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
   a.dsum = reinterpret_cast<float *>(ws + wl.dsum);
   a.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
   a.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
+  a.col_cnt = reinterpret_cast<int *>(ws + wl.col_cnt);
+  a.col_idx = reinterpret_cast<int16_t *>(ws + wl.col_idx);
+  a.sched = reinterpret_cast<int *>(ws + wl.sched);
   a.dq = static_cast<uint16_t *>(dq);
   CUtensorMap tdq_acc;
   if (!encode_dq_acc(&tdq_acc, a.dq_acc, static_cast<size_t>(BH) * a.n_pad)) return FA_ERR_CUDA;

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
   const int bh = blockIdx.y;
   const int sub = threadIdx.x & 7;
   const int r0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.sched = 0;
   const uint16_t *o_head = a.o + static_cast<size_t>(bh) * pr.N * kHeadDim;
   const uint16_t *do_head = a.dout + static_cast<size_t>(bh) * pr.N * kHeadDim;
   const size_t ws_row0 = static_cast<size_t>(bh) * a.n_pad;
@@ -134,9 +135,60 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- main kernel
 
+// ---------------------------------------------------------------- block-sparse column lists
+
+// For key tile kt (one block each): the query tiles i >= i_begin with
+// block_mask[i][kt] != 0, ascending, and their count.  Built once per call;
+// the main kernel reads the list of the key tile it is working on.
+__global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int warp_tot[8];
+  __shared__ int base;
+  const Problem &pr = a.pr;
+  const int kt = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i_begin = pr.causal ? kt : 0;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int chunk = 0; chunk < pr.nt; chunk += 256) {
+    const int i = chunk + tid;
+    const bool keep = i >= i_begin && i < pr.nt &&
+                      __ldg(pr.block_mask + static_cast<size_t>(i) * pr.nt + kt) != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int off = base;
+    for (int w = 0; w < warp; ++w) off += warp_tot[w];
+    if (keep)
+      a.col_idx[static_cast<size_t>(kt) * pr.nt + off + __popc(bal & ((1u << lane) - 1u))] =
+          static_cast<int16_t>(i);
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < 8; ++w) tot += warp_tot[w];
+      base += tot;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) a.col_cnt[kt] = base;
+}
+
+// ---------------------------------------------------------------- main kernel
+
+// Persistent: one CTA per SM walks the work items (key tile kt, head b*h).
+// Its first item is t = blockIdx.x; later ones are claimed from a global
+// counter by the producer warp and handed to the other roles through a small
+// ring in shared memory, so CTAs that drew short items take more of them.
+// Items are numbered key-tile major: under a causal mask the longest items
+// (small kt) are handed out first.
+// K_j and V_j are double-buffered across items and every ring runs on one
+// step counter for the whole CTA, so the next item's loads and first
+// S^T / dP^T overlap the current item's last step and epilogue.
+//
 // Warp roles (16 warps, four warpgroups):
-//   warpgroup 0 (warps 0-3)   P^T / dS^T for queries 0-63 of the step (thread = key row)
-//   warpgroup 1 (warps 4-7)   the same for queries 64-127
+//   warpgroup 0 (warps 0-3)   P^T / dS^T for queries 0-63 of the step (thread = key row),
+//                             then the dV half of the item's epilogue
+//   warpgroup 1 (warps 4-7)   the same for queries 64-127, then the dK half
 //   warpgroup 2 (warps 8-11)  dQ partial: TMEM -> swizzled shared tile -> TMA
 //                             reduce-add into the fp32 accumulators (thread = query row)
 //   warpgroup 3: warp 12      TMA producer
@@ -149,15 +201,15 @@ constexpr int kMainThreads = 512;
 constexpr uint32_t kRegsElementwise = 168, kRegsDq = 96, kRegsControl = 80;
 
 struct __align__(1024) BwdSmem {
-  uint8_t k[kTileBytes];                 // K_j (resident); later dK staging
-  uint8_t v[kTileBytes];                 // V_j (resident); later dV staging
+  uint8_t kv[2][2][kTileBytes];          // [item parity][K_j | V_j]; later dK / dV staging
   uint8_t q[kStages][kTileBytes];
   uint8_t dout[kStages][kTileBytes];
-  uint8_t dst[2][2][kTileBytes];         // dS^T bf16, double-buffered; [buf][query half], rows = keys
+  uint8_t dst[2][kTileBytes];            // dS^T bf16 [query half], rows = keys
   uint8_t dq_stage[2][kTileBytes];       // dQ partial fp32, columns 0-31 | 32-63, rows = queries
   float lse2[kStages][kTile];
   float dsum[kStages][kTile];
-  uint64_t bar_kv;
+  uint64_t bar_kv[2];
+  uint64_t bar_kv_free[2];
   uint64_t bar_q_full[kStages];
   uint64_t bar_q_empty[kStages];
   uint64_t bar_s_full;
@@ -165,17 +217,21 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_p_full;     // P^T of the step is in TMEM
   uint64_t bar_ds_full;    // dS^T of the step is in shared memory
   uint64_t bar_pt_free;
-  uint64_t bar_ds_free[2];
+  uint64_t bar_ds_free;
   uint64_t bar_dq_full;
   uint64_t bar_dq_free;
   uint64_t bar_done;
   uint64_t bar_final;
+  uint64_t bar_item_full[4];
+  uint64_t bar_item_empty[4];
+  int item_ring[4];
   uint32_t tmem_base;
   int abort;
-  int n_tiles;
-  int rot;
-  int16_t tiles[kMaxMaskTiles];
 };
+
+// Consumers of the item ring: the MMA thread, the 256 elementwise threads and
+// the 128 dQ threads each release a slot once they have read it.
+constexpr uint32_t kItemConsumers = 1 + 256 + 128;
 
 // TMEM columns: S^T, dP^T (fp32, lanes = keys), dV, dK (fp32 accumulators,
 // lanes = keys), dQ partial (fp32, lanes = queries), P^T (bf16 pairs).
@@ -183,13 +239,37 @@ constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ
                    kColPT = 448;
 constexpr uint32_t kTmemCols = 512;
 
-// Step it visits query tile tiles[(it + rot) % n]: the key tiles of one head
-// start at different query tiles so their concurrent dQ reduce-adds land on
-// different accumulator rows.
-__device__ __forceinline__ int qtile_at(const BwdSmem &s, int it) {
-  int k = it + s.rot;
-  if (k >= s.n_tiles) k -= s.n_tiles;
-  return s.tiles[k];
+// One work item: key tile kt of head bh and the query tiles that attend to
+// it (i >= kt under causal, the block mask's column kt, none at all when the
+// tile lies past kv_len).
+struct Item {
+  int kt, bh, n, rot, i_begin;
+  int kv_bound;
+};
+
+__device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
+  const Problem &pr = a.pr;
+  const int BH = pr.B * pr.H;
+  Item it;
+  it.kt = t / BH;
+  it.bh = t - it.kt * BH;
+  it.kv_bound = key_bound(pr, it.bh / pr.H);
+  it.i_begin = pr.causal ? it.kt : 0;
+  if (it.kt * kTile >= it.kv_bound) it.n = 0;
+  else if (pr.block_mask) it.n = __ldg(a.col_cnt + it.kt);
+  else it.n = pr.nt - it.i_begin;
+  // the key tiles of one head start at different query tiles, so their
+  // concurrent dQ reduce-adds land on different accumulator rows
+  it.rot = it.n > 0 ? it.kt % it.n : 0;
+  return it;
+}
+
+// Query tile of step k of the item.
+__device__ __forceinline__ int qtile_of(const BwdArgs &a, const Item &it, int k) {
+  int j = k + it.rot;
+  if (j >= it.n) j -= it.n;
+  return a.pr.block_mask ? static_cast<int>(__ldg(a.col_idx + static_cast<size_t>(it.kt) * a.pr.nt + j))
+                         : it.i_begin + j;
 }
 
 // Elementwise phase 1 for 32 query columns starting at qc: S^T values in
@@ -265,15 +345,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kt = blockIdx.x;  // key tile; small kt = most query tiles under causal
-  const int bh = blockIdx.y;
-  const int b = bh / pr.H;
-  const int kv_bound = key_bound(pr, b);
-  const bool kv_live = kt * kTile < kv_bound;
-  const int i_begin = pr.causal ? kt : 0;
+  const int n_items = pr.nt * pr.B * pr.H;
 
   if (tid == 0) {
-    mbar_init(&s.bar_kv, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.bar_kv[i], 1);
+      mbar_init(&s.bar_kv_free[i], 1);
+    }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.bar_q_full[i], 1);
       mbar_init(&s.bar_q_empty[i], 1);
@@ -283,12 +361,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&s.bar_p_full, 256);
     mbar_init(&s.bar_ds_full, 256);
     mbar_init(&s.bar_pt_free, 1);
-    mbar_init(&s.bar_ds_free[0], 1);
-    mbar_init(&s.bar_ds_free[1], 1);
+    mbar_init(&s.bar_ds_free, 1);
     mbar_init(&s.bar_dq_full, 1);
     mbar_init(&s.bar_dq_free, 128);
     mbar_init(&s.bar_done, 1);
     mbar_init(&s.bar_final, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s.bar_item_full[i], 1);
+      mbar_init(&s.bar_item_empty[i], kItemConsumers);
+    }
     s.abort = 0;
     fence_mbar_init();
   }
@@ -299,30 +380,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
   }
-  // Query tiles that attend to this key tile: i >= i_begin (causal), the
-  // block mask's column kt, nothing at all when the tile is past kv_len.
-  if (warp == 0) {
-    int count = 0;
-    if (kv_live) {
-      for (int base = i_begin; base < pr.nt; base += 32) {
-        const int i = base + lane;
-        bool keep = i < pr.nt;
-        if (keep && pr.block_mask)
-          keep = __ldg(pr.block_mask + static_cast<size_t>(i) * pr.nt + kt) != 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-        if (keep) s.tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(i);
-        count += __popc(bal);
-      }
-    }
-    if (lane == 0) {
-      s.n_tiles = count;
-      s.rot = count > 0 ? kt % count : 0;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
   if (warp < 8) {
@@ -330,79 +390,92 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // ------------------------------------------------------------ elementwise
     const int half = warp >> 2;            // query columns 64*half .. 64*half+63
     const int kr = (warp & 3) * 32 + lane; // TMEM lane: key row
-    const uint32_t wg_bar = 3 + half;      // named barrier of this warpgroup
-    const int key = kt * kTile + kr;
-    const bool key_ok = key < kv_bound;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = pr.scale_log2;
-    // Every wait of this warpgroup takes one decision for all four warps, so the
-    // named barriers inside the loop are always reached by all of them.
+    // Every wait of the two elementwise warpgroups takes one decision for all
+    // eight warps, so the barrier of the per-item epilogue is always reached by
+    // all of them, on a timeout as well.
     auto wg_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return named_bar_and(wg_bar, 128, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
+      return named_bar_and(1, 256, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
     };
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int st = it % kStages;
-      const int buf = it & 1;
-      const int i = qtile_at(s, it);
-      if (!wg_wait(&s.bar_q_full[st], (it / kStages) & 1) || !wg_wait(&s.bar_s_full, it & 1)) {
-        ok = false;
-        break;
+    int g = 0;          // step counter of this CTA
+    uint32_t done_par = 0;
+    for (int v = 0; ok; ++v) {
+      if (!wg_wait(&s.bar_item_full[v & 3], (v >> 2) & 1)) break;
+      const int t = s.item_ring[v & 3];
+      mbar_arrive(&s.bar_item_empty[v & 3]);
+      if (t >= n_items) break;
+      const Item itm = item_at(a, t);
+      const bool key_ok = itm.kt * kTile + kr < itm.kv_bound;
+      for (int k = 0; k < itm.n; ++k, ++g) {
+        const int st = g % kStages;
+        const int i = qtile_of(a, itm, k);
+        if (!wg_wait(&s.bar_q_full[st], (g / kStages) & 1) || !wg_wait(&s.bar_s_full, g & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool diag = pr.causal && (i == itm.kt);
+        const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+        const uint32_t t_s = tmem + lane_base + kColST + half * 64;
+        const uint32_t t_dp = tmem + lane_base + kColDPT + half * 64;
+        uint32_t sa[32], da[32], sb[32], db[32];
+        tmem_ld32(t_s, sa);
+        tmem_ld32(t_dp, da);
+        tmem_wait_ld_tied32(sa, da);
+        tmem_ld32(t_s + 32, sb);   // second half in flight while the first is computed
+        tmem_ld32(t_dp + 32, db);
+        const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
+        // phase 1: P^T, in place over the S^T registers
+        if (need_mask) p_from_s32<true>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
+        else p_from_s32<false>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
+        tmem_wait_ld_tied32(sb, db);
+        tc_fence_before();
+        mbar_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
+        if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
+        else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
+        // the P^T columns are free once the previous step's dV has read them
+        if (g > 0 && !wg_wait(&s.bar_pt_free, (g - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_pt = tmem + lane_base + kColPT;
+        store_p32(sa, half * 64, t_pt);
+        store_p32(sb, half * 64 + 32, t_pt);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&s.bar_p_full);   // dV of this step may start
+        // phase 2: dS^T; the tile is free once the previous step's dK / dQ read it
+        if (g > 0 && !wg_wait(&s.bar_ds_free, (g - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ds_row = smem_u32(s.dst[half]) + kr * 128;
+        ds_store32(sa, da, half * 64, half, kr, dsum_a, ds_row);
+        ds_store32(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row);
+        fence_proxy_async_smem();
+        mbar_arrive(&s.bar_ds_full);  // dK, dQ of this step may start
       }
-      tc_fence_after();
-      const bool diag = pr.causal && (i == kt);
-      const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
-      const uint32_t t_s = tmem + lane_base + kColST + half * 64;
-      const uint32_t t_dp = tmem + lane_base + kColDPT + half * 64;
-      uint32_t sa[32], da[32], sb[32], db[32];
-      tmem_ld32(t_s, sa);
-      tmem_ld32(t_dp, da);
-      tmem_wait_ld_tied32(sa, da);
-      tmem_ld32(t_s + 32, sb);   // second half in flight while the first is computed
-      tmem_ld32(t_dp + 32, db);
-      const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
-      // phase 1: P^T, in place over the S^T registers
-      if (need_mask) p_from_s32<true>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
-      else p_from_s32<false>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
-      tmem_wait_ld_tied32(sb, db);
-      tc_fence_before();
-      mbar_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
-      if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
-      else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
-      // the P^T columns are free once dV(it-1) has read them
-      if (it > 0 && !wg_wait(&s.bar_pt_free, (it - 1) & 1)) {
-        ok = false;
-        break;
+      if (!ok) break;
+      // -------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
+      if (itm.n > 0) {
+        if (!wg_wait(&s.bar_done, done_par)) {
+          ok = false;
+          break;
+        }
+        done_par ^= 1u;
+        tc_fence_after();
       }
-      tc_fence_after();
-      const uint32_t t_pt = tmem + lane_base + kColPT;
-      store_p32(sa, half * 64, t_pt);
-      store_p32(sb, half * 64 + 32, t_pt);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&s.bar_p_full);   // dV(it) may start
-      // phase 2: dS^T; its buffer is free once dK/dQ(it-2) have read it
-      if (it > 1 && !wg_wait(&s.bar_ds_free[buf], ((it - 2) >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      const uint32_t ds_row = smem_u32(s.dst[buf][half]) + kr * 128;
-      ds_store32(sa, da, half * 64, half, kr, dsum_a, ds_row);
-      ds_store32(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row);
-      fence_proxy_async_smem();
-      mbar_arrive(&s.bar_ds_full);  // dK(it), dQ(it) may start
-    }
-    // ---------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
-    if (ok && n > 0) ok = wg_wait(&s.bar_done, 0);
-    if (ok) {
-      tc_fence_after();
       const uint32_t col = half == 0 ? kColDV : kColDK;
       const float mul = half == 0 ? 1.f : pr.scale;
-      const uint32_t dst = smem_u32(half == 0 ? s.v : s.k) + kr * 128;
+      const int kb = v & 1;
+      const uint32_t dst = smem_u32(s.kv[kb][half == 0 ? 1 : 0]) + kr * 128;
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t r[32];
-        if (n > 0) {
+        if (itm.n > 0) {
           tmem_ld32(tmem + lane_base + col + h2 * 32, r);
           tmem_wait_ld();
         } else {
@@ -419,150 +492,217 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                        pack_bf16(__uint_as_float(r[c0 + 6]) * mul, __uint_as_float(r[c0 + 7]) * mul));
         }
       }
+      tc_fence_before();
       fence_proxy_async_smem();
+      // both warpgroups (dV and dK halves) agree before the store
+      if (!named_bar_and(1, 256, !s.abort)) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) {
+        tma_store_3d(&tm_dv, s.kv[kb][1], 0, itm.kt * kTile, itm.bh);
+        tma_store_3d(&tm_dk, s.kv[kb][0], 0, itm.kt * kTile, itm.bh);
+        bulk_commit();
+        bulk_wait_read_all();  // the staging buffer may be reloaded now
+        mbar_arrive(&s.bar_kv_free[kb]);
+      }
     }
-    named_bar_sync(1, 256);
-    if (tid == 0 && ok && !s.abort) {
-      tma_store_3d(&tm_dv, s.v, 0, kt * kTile, bh);
-      tma_store_3d(&tm_dk, s.k, 0, kt * kTile, bh);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (tid == 0) bulk_wait_all();
   } else if (warp < 12) {
     setmaxnreg_dec<kRegsDq>();
     // ------------------------------------------------------------ dQ partials (rows = queries)
     const int qr = tid - 256;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int it = 0; it < n; ++it) {
-      const int i = qtile_at(s, it);
-      // one decision for all four warps: the barriers below must see all of them
-      if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_dq_full, it & 1, pr.wait, &s.abort))) break;
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + lane_base + kColDQ, r0);
-      tmem_ld32(tmem + lane_base + kColDQ + 32, r1);
-      tmem_wait_ld_tied32(r0, r1);
-      tc_fence_before();
-      mbar_arrive(&s.bar_dq_free);
-      // the previous step's reduce-adds must have finished reading the stage
-      if (qr == 0) bulk_wait_read_all();
-      named_bar_sync(2, 128);
-      const uint32_t b0 = smem_u32(s.dq_stage[0]), b1 = smem_u32(s.dq_stage[1]);
+    bool ok = true;
+    int g = 0;
+    for (int v = 0; ok; ++v) {
+      if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait,
+                                                &s.abort)))
+        break;
+      const int t = s.item_ring[v & 3];
+      mbar_arrive(&s.bar_item_empty[v & 3]);
+      if (t >= n_items) break;
+      const Item itm = item_at(a, t);
+      for (int k = 0; k < itm.n; ++k, ++g) {
+        // one decision for all four warps: the barriers below must see all of them
+        if (!named_bar_and(2, 128, mbar_wait_warp(&s.bar_dq_full, g & 1, pr.wait, &s.abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + kColDQ, r0);
+        tmem_ld32(tmem + lane_base + kColDQ + 32, r1);
+        tmem_wait_ld_tied32(r0, r1);
+        tc_fence_before();
+        mbar_arrive(&s.bar_dq_free);
+        // the previous step's reduce-adds must have finished reading the stage
+        if (qr == 0) bulk_wait_read_all();
+        named_bar_sync(2, 128);
+        const uint32_t b0 = smem_u32(s.dq_stage[0]), b1 = smem_u32(s.dq_stage[1]);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        st_shared_v4(b0 + sw128_offset(qr, ch), r0[4 * ch], r0[4 * ch + 1], r0[4 * ch + 2],
-                     r0[4 * ch + 3]);
-        st_shared_v4(b1 + sw128_offset(qr, ch), r1[4 * ch], r1[4 * ch + 1], r1[4 * ch + 2],
-                     r1[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      if (qr == 0) {
-        const int row0 = bh * a.n_pad + i * kTile;
-        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
-        tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
-        bulk_commit();
+        for (int ch = 0; ch < 8; ++ch) {
+          st_shared_v4(b0 + sw128_offset(qr, ch), r0[4 * ch], r0[4 * ch + 1], r0[4 * ch + 2],
+                       r0[4 * ch + 3]);
+          st_shared_v4(b1 + sw128_offset(qr, ch), r1[4 * ch], r1[4 * ch + 1], r1[4 * ch + 2],
+                       r1[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (qr == 0) {
+          const int row0 = itm.bh * a.n_pad + qtile_of(a, itm, k) * kTile;
+          tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
+          tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
+          bulk_commit();
+        }
       }
     }
-      if (qr == 0) bulk_wait_all();
+    if (qr == 0) bulk_wait_all();
   } else {
     setmaxnreg_dec<kRegsControl>();
     if (warp == 12) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&s.bar_kv, 2 * kTileBytes);
-      tma_load_3d(s.k, &tm_k, &s.bar_kv, 0, kt * kTile, bh);
-      tma_load_3d(s.v, &tm_v, &s.bar_kv, 0, kt * kTile, bh);
-      for (int it = 0; it < n; ++it) {
-        const int st = it % kStages;
-        const uint32_t use = it / kStages;
-        if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
-        const int i = qtile_at(s, it);
-        const size_t stat = static_cast<size_t>(bh) * a.n_pad + static_cast<size_t>(i) * kTile;
-        mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
-        tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, bh);
-        tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, bh);
-        bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
-        bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        bool ok = true;
+        int g = 0;
+        for (int v = 0; ok; ++v) {
+          // claim the next item and publish it to the other roles
+          const int slot = v & 3;
+          if (v >= 4 && !mbar_wait(&s.bar_item_empty[slot], ((v - 4) >> 2) & 1, pr.wait, &s.abort))
+            break;
+          const int t = v == 0 ? static_cast<int>(blockIdx.x)
+                               : static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+          s.item_ring[slot] = t;
+          mbar_arrive(&s.bar_item_full[slot]);
+          if (t >= n_items) break;
+          const Item itm = item_at(a, t);
+          const int kb = v & 1;
+          // The item two back has stored its dK / dV out of this buffer.  Taken
+          // for items without steps as well (their zero dK / dV are staged in
+          // the buffer too), so that each wait is for the barrier's next phase.
+          if (v >= 2 && !mbar_wait(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort)) break;
+          if (itm.n == 0) continue;
+          mbar_arrive_expect_tx(&s.bar_kv[kb], 2 * kTileBytes);
+          tma_load_3d(s.kv[kb][0], &tm_k, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
+          tma_load_3d(s.kv[kb][1], &tm_v, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
+          for (int k = 0; k < itm.n; ++k, ++g) {
+            const int st = g % kStages;
+            const uint32_t use = g / kStages;
+            if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) {
+              ok = false;
+              break;
+            }
+            const int i = qtile_of(a, itm, k);
+            const size_t stat = static_cast<size_t>(itm.bh) * a.n_pad + static_cast<size_t>(i) * kTile;
+            mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
+            tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, itm.bh);
+            tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, itm.bh);
+            bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
+            bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
+          }
+        }
       }
-    }
     } else if (warp == 13) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
-      const uint32_t k_addr = smem_u32(s.k), v_addr = smem_u32(s.v);
-      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step it.
-      auto issue_s = [&](int it) -> bool {
-        const int st = it % kStages;
-        if (!mbar_wait(&s.bar_q_full[st], (it / kStages) & 1, pr.wait, &s.abort)) return false;
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+        constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
+        constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
+        bool ok = true;
+        int g = 0;
+        uint32_t kv_use[2] = {0u, 0u};
+        for (int v = 0; ok; ++v) {
+          if (!mbar_wait(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
+          const int t = s.item_ring[v & 3];
+          mbar_arrive(&s.bar_item_empty[v & 3]);
+          if (t >= n_items) break;
+          const Item itm = item_at(a, t);
+          if (itm.n == 0) continue;
+          const int kb = v & 1;
+          const uint32_t k_addr = smem_u32(s.kv[kb][0]), v_addr = smem_u32(s.kv[kb][1]);
+          if (!mbar_wait(&s.bar_kv[kb], kv_use[kb] & 1, pr.wait, &s.abort)) break;
+          ++kv_use[kb];
+          // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step gs.
+          auto issue_s = [&](int gs) -> bool {
+            const int st = gs % kStages;
+            if (!mbar_wait(&s.bar_q_full[st], (gs / kStages) & 1, pr.wait, &s.abort)) return false;
+            tc_fence_after();
+            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
-                      sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
+            for (int kk = 0; kk < kHeadDim / 16; ++kk)
+              mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
+                          sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
-                      sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
-        mma_commit(&s.bar_s_full);
-        return true;
-      };
-      bool ok = mbar_wait(&s.bar_kv, 0, pr.wait, &s.abort) && issue_s(0);
-      for (int it = 0; ok && it < n; ++it) {
-        const int st = it % kStages;
-        const int buf = it & 1;
-        // S^T / dP^T(it) are in the elementwise warps' registers: the next
-        // step's S^T, dP^T can overwrite them while P^T / dS^T(it) are built.
-        if (it + 1 < n) {
-          if (!mbar_wait(&s.bar_st_read, it & 1, pr.wait, &s.abort)) break;
+            for (int kk = 0; kk < kHeadDim / 16; ++kk)
+              mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
+                          sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
+            mma_commit(&s.bar_s_full);
+            return true;
+          };
+          // the previous step's S^T / dP^T are in registers before they are overwritten
+          if (g > 0 && !mbar_wait(&s.bar_st_read, (g - 1) & 1, pr.wait, &s.abort)) break;
           tc_fence_after();
-          if (!issue_s(it + 1)) break;
+          if (!issue_s(g)) break;
+          for (int k = 0; k < itm.n; ++k, ++g) {
+            const int st = g % kStages;
+            if (k + 1 < itm.n) {
+              if (!mbar_wait(&s.bar_st_read, g & 1, pr.wait, &s.abort) || (tc_fence_after(), !issue_s(g + 1))) {
+                ok = false;
+                break;
+              }
+            }
+            // P^T of this step is in TMEM.
+            if (!mbar_wait(&s.bar_p_full, g & 1, pr.wait, &s.abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
+            // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per
+            // instruction), B = dO_i (queries x d, d contiguous: MN-major).
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
+                          sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (k > 0 || kk > 0));
+            mma_commit(&s.bar_pt_free);
+            // dS^T of this step is in shared memory.
+            if (!mbar_wait(&s.bar_ds_full, g & 1, pr.wait, &s.abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[kk >> 2]) + off, 16, 1024),
+                          sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (k > 0 || kk > 0));
+            }
+            mma_commit(&s.bar_q_empty[st]);
+            if (g > 0 && !mbar_wait(&s.bar_dq_free, (g - 1) & 1, pr.wait, &s.abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major
+            // operand (queries contiguous, two 64-query halves 16 KiB apart);
+            // B = K_j, MN-major (d contiguous).  K dimension = keys.
+            const uint32_t ds_addr = smem_u32(s.dst[0]);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
+                          sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
+            mma_commit(&s.bar_dq_full);
+            mma_commit(&s.bar_ds_free);
+          }
+          if (ok) mma_commit(&s.bar_done);
         }
-        // P^T(it) is in TMEM.
-        if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
-        tc_fence_after();
-        const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
-        // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per step),
-        // B = dO_i (queries x d, d contiguous: MN-major).
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                      sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
-        mma_commit(&s.bar_pt_free);
-        // dS^T(it) is in shared memory.
-        if (!mbar_wait(&s.bar_ds_full, it & 1, pr.wait, &s.abort)) break;
-        tc_fence_after();
-        // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[buf][kk >> 2]) + off, 16, 1024),
-                      sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (it > 0 || kk > 0));
-        }
-        mma_commit(&s.bar_q_empty[st]);
-        if (it > 0 && !mbar_wait(&s.bar_dq_free, (it - 1) & 1, pr.wait, &s.abort)) break;
-        tc_fence_after();
-        // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major operand
-        // (queries contiguous, two 64-query halves 16 KiB apart); B = K_j,
-        // MN-major (d contiguous).  K dimension = keys, 16 per instruction.
-        const uint32_t ds_addr = smem_u32(s.dst[buf][0]);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
-                      sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
-        mma_commit(&s.bar_dq_full);
-        mma_commit(&s.bar_ds_free[buf]);
       }
-      mma_commit(&s.bar_done);
-    }
-    if (lane == 0) {
-      mma_commit(&s.bar_final);
-      mbar_wait_drain(&s.bar_final, 0, pr.wait);
-    }
-    __syncwarp();
+      if (lane == 0) {
+        mma_commit(&s.bar_final);
+        mbar_wait_drain(&s.bar_final, 0, pr.wait);
+      }
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -595,11 +735,15 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
+  if (a.pr.block_mask &&
+      (e = launch_pdl(fa_bwd_cols_kernel, dim3(a.pr.nt), dim3(256), 0, st, a)) != cudaSuccess)
+    return e;
   // preprocess: n_pad / (32 rows x 4) blocks per head cover the padded rows exactly
   const dim3 pre_grid(a.n_pad / (kRowsPerBlock * kRowsPerThread), a.pr.B * a.pr.H);
   if ((e = launch_pdl(fa_bwd_pre_kernel, pre_grid, dim3(256), 0, st, a)) != cudaSuccess)
     return e;
-  dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
+  const int n_items = a.pr.nt * a.pr.B * a.pr.H;
+  const dim3 grid(n_items < num_sms ? n_items : num_sms);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
   if ((e = launch_pdl(fa_bwd_main_kernel, grid, dim3(kMainThreads), smem, st, tq, tk, tv, tdo, tdk,
                       tdv, tdq_acc, a)) != cudaSuccess)

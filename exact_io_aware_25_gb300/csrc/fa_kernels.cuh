@@ -40,6 +40,9 @@ struct BwdArgs {
   float *dsum;            // workspace D   [B*H, n_pad]
   float *lse2;            // workspace lse * log2(e) [B*H, n_pad] (+inf in padding rows)
   float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, 64]
+  int *col_cnt;           // workspace, block mask only: query tiles per key tile [nt]
+  int16_t *col_idx;       // workspace, block mask only: their indices [nt][nt], ascending
+  int *sched;             // workspace: work counter of the persistent main kernel
   uint16_t *dq;           // [B, H, N, 64] bf16
 };
 

@@ -41,14 +41,20 @@ def test_status_strings(fa_lib):
 
 
 def test_workspace_size_formula(fa_lib):
-    # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + 64 fp32 dQ accumulators
+    # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + 64 fp32 dQ accumulators;
+    # plus the block-sparse column lists: nt int32 counts and nt*nt int16 indices,
+    # and one int32 work counter
+    up = lambda x: -(-x // 256) * 256
     for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536)]:
         n_pad = -(-N // 128) * 128
+        nt = n_pad // 128
         bh = B * H
-        want = 0
-        want = -(-(bh * n_pad * 4) // 256) * 256
-        want = -(-(want + bh * n_pad * 4) // 256) * 256
-        want = -(-(want + bh * n_pad * 64 * 4) // 256) * 256
+        want = up(bh * n_pad * 4)
+        want = up(want + bh * n_pad * 4)
+        want = up(want + bh * n_pad * 64 * 4)
+        want = up(want + nt * 4)
+        want = up(want + nt * nt * 2)
+        want = up(want + 4)
         assert fa_lib.fa_bwd_workspace_size(B, H, N, 64) == want
     assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 128) == 0
     assert fa_lib.fa_bwd_workspace_size(0, 1, 128, 64) == 0

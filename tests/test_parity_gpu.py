@@ -106,6 +106,35 @@ def test_key_padding_edges(H, oracle_mod, kv):
     _full_check(H, oracle_mod, H.Inputs(w, kv_len=np.array(kv, np.int32)))
 
 
+def test_many_key_tiles_without_work(H, oracle_mod):
+    """More (key tile, head) items than SMs, most of them with no query tile
+    to visit (keys past kv_len): their dK / dV are zero and the items around
+    them are unaffected."""
+    import workloads as W
+    w = W.make("tiny", seed=11, B=4, H=4, N=4096)
+    x = H.Inputs(w, kv_len=np.array([130, 4096, 1, 300], np.int32))
+    _sampled_check(H, oracle_mod, x, rows_per_head=64, key_tiles_per_head=3, seed=5)
+    _, dk, dv = H.run_bwd(x, *H.run_fwd(x))
+    assert torch.all(dk[0, :, 256:].float() == 0) and torch.all(dv[2, :, 128:].float() == 0)
+
+
+def test_block_mask_with_empty_key_columns(H, oracle_mod):
+    """A block mask whose key-tile columns are mostly empty, over more items
+    than SMs, with causal on top."""
+    import workloads as W
+    w = W.make("tiny", seed=12, B=2, H=8, N=4096)
+    rng = np.random.default_rng(12)
+    mask = np.zeros((32, 32), np.uint8)
+    cols = rng.choice(32, size=6, replace=False)
+    mask[:, cols] = rng.integers(0, 2, size=(32, 6)).astype(np.uint8)
+    x = H.Inputs(w, causal=True, block_mask=mask)
+    _sampled_check(H, oracle_mod, x, rows_per_head=64, key_tiles_per_head=3, seed=6)
+    _, dk, _ = H.run_bwd(x, *H.run_fwd(x))
+    empty = [c for c in range(32) if c not in set(cols.tolist())]
+    for c in empty[:4]:
+        assert torch.all(dk[:, :, c * 128:(c + 1) * 128].float() == 0)
+
+
 def test_mask_with_empty_rows_and_causal(H, oracle_mod):
     import workloads as W
     w = W.make("tiny", seed=8, B=1, H=2, N=500)
