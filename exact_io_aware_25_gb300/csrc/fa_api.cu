@@ -107,6 +107,7 @@ fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t
   if (rows >= (1LL << 31) || static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
   if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
   const int nt = (N + kTile - 1) / kTile;
+  if (nt > kMaxGridTiles) return FA_ERR_UNSUPPORTED;
   if (block_mask && nt > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -147,9 +148,11 @@ WsLayout ws_layout(int B, int H, int N) {
   w.dsum = 0;
   w.lse2 = align_up(w.dsum + bh * n_pad * sizeof(float), 256);
   w.dq_acc = align_up(w.lse2 + bh * n_pad * sizeof(float), 256);
+  // column lists exist only with a block mask, which limits nt to kMaxMaskTiles
+  const size_t nl = nt < static_cast<size_t>(kMaxMaskTiles) ? nt : kMaxMaskTiles;
   w.col_cnt = align_up(w.dq_acc + bh * n_pad * kHeadDim * sizeof(float), 256);
-  w.col_idx = align_up(w.col_cnt + nt * sizeof(int), 256);
-  w.sched = align_up(w.col_idx + nt * nt * sizeof(int16_t), 256);
+  w.col_idx = align_up(w.col_cnt + nl * sizeof(int), 256);
+  w.sched = align_up(w.col_idx + nl * nl * sizeof(int16_t), 256);
   w.total = align_up(w.sched + sizeof(int), 256);
   return w;
 }
@@ -191,7 +194,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || d != kHeadDim) return 0;
+  if (validate_common(B, H, N, d, 1.f, nullptr) != FA_OK) return 0;
   return ws_layout(B, H, N).total;
 }
 

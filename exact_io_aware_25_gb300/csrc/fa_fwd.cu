@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = args.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.x);  // heavy causal tiles first
-  const int bh = blockIdx.y;
+  // blockIdx.x (the head) varies fastest in launch order, so every head's last
+  // query tile, the heaviest under a causal mask, is dispatched first.
+  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.y);
+  const int bh = blockIdx.x;
   const int b = bh / pr.H;
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
@@ -418,7 +420,7 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  dim3 grid(a.pr.nt, a.pr.B * a.pr.H);
+  dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
   return launch_pdl(fa_fwd_kernel, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
 }
 

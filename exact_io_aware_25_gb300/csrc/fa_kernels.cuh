@@ -13,6 +13,8 @@ namespace fa {
 constexpr int kTile = 128;      // B_r = B_c = 128 query / key rows per tile
 constexpr int kHeadDim = 64;    // d
 constexpr int kMaxMaskTiles = 1024;  // block-sparse: at most 1024 tiles per row (N <= 131072)
+// Query tiles per head are a grid dimension of the forward launch (y, at most 65535).
+constexpr int kMaxGridTiles = 65535;
 
 struct Problem {
   int B, H, N;

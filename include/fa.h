@@ -51,7 +51,8 @@ extern "C" {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, non-finite or non-positive scale */
-    FA_ERR_UNSUPPORTED = -2,  /* d != 64, or no sm_103 device */
+    FA_ERR_UNSUPPORTED = -2,  /* d != 64, N > 65535 * 128, N > 1024 * 128 with a block
+                                 mask, or no sm_103 device */
     FA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     FA_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed */
     FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait ran out (reported by fa_check) */
@@ -79,8 +80,10 @@ FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, fl
  * Bytes of device workspace fa_bwd needs for this shape: per (b, h) and
  * query row (padded to a multiple of 128) one fp32 D_i = <dO_i, O_i>, one
  * fp32 base-2 log-sum-exp, and d fp32 dQ accumulators; O(N) per head
- * ([EXPL] "Complexity analysis": O(N) extra memory).  Returns 0 for
- * invalid sizes.
+ * ([EXPL] "Complexity analysis": O(N) extra memory).  Plus, for the
+ * block-sparse schedule, one int32 count and up to nt int16 query-tile indices
+ * per key tile (nt = ceil(N / 128), capped at 1024), and one int32 work
+ * counter.  Returns 0 for invalid sizes.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

@@ -42,22 +42,24 @@ def test_status_strings(fa_lib):
 
 def test_workspace_size_formula(fa_lib):
     # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + 64 fp32 dQ accumulators;
-    # plus the block-sparse column lists: nt int32 counts and nt*nt int16 indices,
-    # and one int32 work counter
+    # plus the block-sparse column lists: nl int32 counts and nl*nl int16 indices
+    # (nl = min(nt, 1024), the most tiles a block mask may have), and one int32
+    # work counter
     up = lambda x: -(-x // 256) * 256
-    for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536)]:
+    for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536), (1, 1, 1 << 20)]:
         n_pad = -(-N // 128) * 128
-        nt = n_pad // 128
+        nl = min(n_pad // 128, 1024)
         bh = B * H
         want = up(bh * n_pad * 4)
         want = up(want + bh * n_pad * 4)
         want = up(want + bh * n_pad * 64 * 4)
-        want = up(want + nt * 4)
-        want = up(want + nt * nt * 2)
+        want = up(want + nl * 4)
+        want = up(want + nl * nl * 2)
         want = up(want + 4)
         assert fa_lib.fa_bwd_workspace_size(B, H, N, 64) == want
     assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 128) == 0
     assert fa_lib.fa_bwd_workspace_size(0, 1, 128, 64) == 0
+    assert fa_lib.fa_bwd_workspace_size(1, 1, 65536 * 128, 64) == 0  # too many tiles
 
 
 def _fwd_status(fa, **kw):
@@ -75,7 +77,7 @@ def _fwd_status(fa, **kw):
     (dict(scale=float("inf")), -1), (dict(scale=float("nan")), -1),
     (dict(d=128), -2), (dict(d=32), -2), (dict(N=1 << 20, block_mask=FAKE), -2),
     (dict(k=FAKE + 8), -3), (dict(lse=FAKE + 4), -3),
-    (dict(B=1 << 16, H=1 << 16, N=1), -1),
+    (dict(B=1 << 16, H=1 << 16, N=1), -1), (dict(N=65535 * 128 + 1), -2),
 ])
 def test_forward_validation_without_gpu(fa_lib, kw, status):
     assert _fwd_status(fa_lib, **kw) == status
