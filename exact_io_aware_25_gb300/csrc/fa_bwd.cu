@@ -25,7 +25,7 @@
 namespace fa {
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -205,7 +205,7 @@ struct __align__(1024) BwdSmem {
   uint8_t q[kStages][kTileBytes];
   uint8_t dout[kStages][kTileBytes];
   uint8_t dst[2][kTileBytes];            // dS^T bf16 [query half], rows = keys
-  uint8_t dq_stage[2][kTileBytes];       // dQ partial fp32, columns 0-31 | 32-63, rows = queries
+  uint8_t dq_stage[kTileBytes];          // dQ partial fp32, 32 columns at a time, rows = queries
   float lse2[kStages][kTile];
   float dsum[kStages][kTile];
   uint64_t bar_kv[2];
@@ -536,24 +536,25 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_wait_ld_tied32(r0, r1);
         tc_fence_before();
         mbar_arrive(&s.bar_dq_free);
-        // the previous step's reduce-adds must have finished reading the stage
-        if (qr == 0) bulk_wait_read_all();
-        named_bar_sync(2, 128);
-        const uint32_t b0 = smem_u32(s.dq_stage[0]), b1 = smem_u32(s.dq_stage[1]);
+        // Columns 0-31, then 32-63, go through the one staging tile: each time
+        // the previous reduce-add must have finished reading it.
+        const uint32_t stage = smem_u32(s.dq_stage);
+        const int row0 = itm.bh * a.n_pad + qtile_of(a, itm, k) * kTile;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          st_shared_v4(b0 + sw128_offset(qr, ch), r0[4 * ch], r0[4 * ch + 1], r0[4 * ch + 2],
-                       r0[4 * ch + 3]);
-          st_shared_v4(b1 + sw128_offset(qr, ch), r1[4 * ch], r1[4 * ch + 1], r1[4 * ch + 2],
-                       r1[4 * ch + 3]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (qr == 0) {
-          const int row0 = itm.bh * a.n_pad + qtile_of(a, itm, k) * kTile;
-          tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[0], 0, row0);
-          tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[1], 32, row0);
-          bulk_commit();
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (qr == 0) bulk_wait_read_all();
+          named_bar_sync(2, 128);
+          const uint32_t *r = h2 == 0 ? r0 : r1;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(stage + sw128_offset(qr, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2],
+                         r[4 * ch + 3]);
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (qr == 0) {
+            tma_reduce_add_2d(&tm_dq_acc, s.dq_stage, h2 * 32, row0);
+            bulk_commit();
+          }
         }
       }
     }
