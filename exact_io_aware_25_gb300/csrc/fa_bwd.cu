@@ -195,10 +195,10 @@ __global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
 //                warp 13      TMEM owner and MMA issuer
 //                warps 14-15  idle
 // Launched at 128 registers per thread; the elementwise warpgroups then take
-// 168 (room for all 64 S^T and dP^T columns of a thread), the dQ warpgroup
-// keeps 96 and the producer / MMA warpgroup 80: 168 + 168 + 96 + 80 = 4 x 128.
+// 160 (room for all 64 S^T and dP^T columns of a thread), the dQ warpgroup and
+// the producer / MMA warpgroup 96 each: 160 + 160 + 96 + 96 = 4 x 128.
 constexpr int kMainThreads = 512;
-constexpr uint32_t kRegsElementwise = 168, kRegsDq = 96, kRegsControl = 80;
+constexpr uint32_t kRegsElementwise = 160, kRegsDq = 96, kRegsControl = 96;
 
 struct __align__(1024) BwdSmem {
   uint8_t kv[2][2][kTileBytes];          // [item parity][K_j | V_j]; later dK / dV staging
@@ -229,9 +229,18 @@ struct __align__(1024) BwdSmem {
   int abort;
 };
 
-// Consumers of the item ring: the MMA thread, the 256 elementwise threads and
-// the 128 dQ threads each release a slot once they have read it.
-constexpr uint32_t kItemConsumers = 1 + 256 + 128;
+// Barriers between roles count warps, not threads: each warp arrives once,
+// from lane 0 after a __syncwarp, so that 256 arrivals do not queue on one
+// shared-memory word every step.
+constexpr uint32_t kEwWarps = 8, kDqWarps = 4;
+// Consumers of the item ring: the MMA warp, the elementwise warps and the dQ
+// warps each release a slot once they have read it.
+constexpr uint32_t kItemConsumers = 1 + kEwWarps + kDqWarps;
+
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 
 // TMEM columns: S^T, dP^T (fp32, lanes = keys), dV, dK (fp32 accumulators,
 // lanes = keys), dQ partial (fp32, lanes = queries), P^T (bf16 pairs).
@@ -357,13 +366,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_init(&s.bar_q_empty[i], 1);
     }
     mbar_init(&s.bar_s_full, 1);
-    mbar_init(&s.bar_st_read, 256);
-    mbar_init(&s.bar_p_full, 256);
-    mbar_init(&s.bar_ds_full, 256);
+    mbar_init(&s.bar_st_read, kEwWarps);
+    mbar_init(&s.bar_p_full, kEwWarps);
+    mbar_init(&s.bar_ds_full, kEwWarps);
     mbar_init(&s.bar_pt_free, 1);
     mbar_init(&s.bar_ds_free, 1);
     mbar_init(&s.bar_dq_full, 1);
-    mbar_init(&s.bar_dq_free, 128);
+    mbar_init(&s.bar_dq_free, kDqWarps);
     mbar_init(&s.bar_done, 1);
     mbar_init(&s.bar_final, 1);
     for (int i = 0; i < 4; ++i) {
@@ -392,11 +401,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const int kr = (warp & 3) * 32 + lane; // TMEM lane: key row
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = pr.scale_log2;
-    // Every wait of the two elementwise warpgroups takes one decision for all
-    // eight warps, so the barrier of the per-item epilogue is always reached by
-    // all of them, on a timeout as well.
+    // Per-item waits take one decision for all eight warps (a named-barrier
+    // reduction), so the barriers of the per-item epilogue are reached by all
+    // of them, on a timeout as well.  Inside an item each warp waits on its own
+    // (a reduction per wait cost about 200 cycles); the outcome is reduced
+    // once after the item's last step.
     auto wg_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return named_bar_and(1, 256, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
+    };
+    auto w_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return mbar_wait_warp(bar, parity, pr.wait, &s.abort);
     };
     bool ok = true;
     int g = 0;          // step counter of this CTA
@@ -404,14 +418,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int v = 0; ok; ++v) {
       if (!wg_wait(&s.bar_item_full[v & 3], (v >> 2) & 1)) break;
       const int t = s.item_ring[v & 3];
-      mbar_arrive(&s.bar_item_empty[v & 3]);
+      warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
       const Item itm = item_at(a, t);
       const bool key_ok = itm.kt * kTile + kr < itm.kv_bound;
       for (int k = 0; k < itm.n; ++k, ++g) {
         const int st = g % kStages;
         const int i = qtile_of(a, itm, k);
-        if (!wg_wait(&s.bar_q_full[st], (g / kStages) & 1) || !wg_wait(&s.bar_s_full, g & 1)) {
+        if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1) || !w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
         }
@@ -432,11 +446,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         else p_from_s32<false>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
         tmem_wait_ld_tied32(sb, db);
         tc_fence_before();
-        mbar_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
+        warp_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
         if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
         // the P^T columns are free once the previous step's dV has read them
-        if (g > 0 && !wg_wait(&s.bar_pt_free, (g - 1) & 1)) {
+        if (g > 0 && !w_wait(&s.bar_pt_free, (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -446,9 +460,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         store_p32(sb, half * 64 + 32, t_pt);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&s.bar_p_full);   // dV of this step may start
+        warp_arrive(&s.bar_p_full);   // dV of this step may start
         // phase 2: dS^T; the tile is free once the previous step's dK / dQ read it
-        if (g > 0 && !wg_wait(&s.bar_ds_free, (g - 1) & 1)) {
+        if (g > 0 && !w_wait(&s.bar_ds_free, (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -456,8 +470,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         ds_store32(sa, da, half * 64, half, kr, dsum_a, ds_row);
         ds_store32(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row);
         fence_proxy_async_smem();
-        mbar_arrive(&s.bar_ds_full);  // dK, dQ of this step may start
+        warp_arrive(&s.bar_ds_full);  // dK, dQ of this step may start
       }
+      // every warp gets here, from the last step or from a failed wait
+      ok = named_bar_and(1, 256, ok);
       if (!ok) break;
       // -------------------------------------------------------- epilogue: dV (warpgroup 0), dK (1)
       if (itm.n > 0) {
@@ -520,7 +536,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                                                 &s.abort)))
         break;
       const int t = s.item_ring[v & 3];
-      mbar_arrive(&s.bar_item_empty[v & 3]);
+      warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
       const Item itm = item_at(a, t);
       for (int k = 0; k < itm.n; ++k, ++g) {
@@ -535,7 +551,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_ld32(tmem + lane_base + kColDQ + 32, r1);
         tmem_wait_ld_tied32(r0, r1);
         tc_fence_before();
-        mbar_arrive(&s.bar_dq_free);
+        warp_arrive(&s.bar_dq_free);
         // Columns 0-31, then 32-63, go through the one staging tile: each time
         // the previous reduce-add must have finished reading it.
         const uint32_t stage = smem_u32(s.dq_stage);
@@ -561,148 +577,161 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     if (qr == 0) bulk_wait_all();
   } else {
     setmaxnreg_dec<kRegsControl>();
+    // The producer and MMA warps run converged, whole-warp: every wait is
+    // one decision for the warp and an elected lane issues each operation.
     if (warp == 12) {
       // ---------------------------------------------------------- producer
-      if (lane == 0) {
-        bool ok = true;
-        int g = 0;
-        for (int v = 0; ok; ++v) {
-          // claim the next item and publish it to the other roles
-          const int slot = v & 3;
-          if (v >= 4 && !mbar_wait(&s.bar_item_empty[slot], ((v - 4) >> 2) & 1, pr.wait, &s.abort))
-            break;
-          const int t = v == 0 ? static_cast<int>(blockIdx.x)
-                               : static_cast<int>(gridDim.x) + atomicAdd(a.sched, 1);
+      bool ok = true;
+      int g = 0;
+      for (int v = 0; ok; ++v) {
+        // claim the next item and publish it to the other roles
+        const int slot = v & 3;
+        if (v >= 4 &&
+            !mbar_wait_warp(&s.bar_item_empty[slot], ((v - 4) >> 2) & 1, pr.wait, &s.abort))
+          break;
+        int t = static_cast<int>(blockIdx.x);
+        if (v > 0) {
+          int c = 0;
+          if (lane == 0) c = atomicAdd(a.sched, 1);
+          t = static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, c, 0);
+        }
+        if (lane == 0) {
           s.item_ring[slot] = t;
           mbar_arrive(&s.bar_item_full[slot]);
-          if (t >= n_items) break;
-          const Item itm = item_at(a, t);
-          const int kb = v & 1;
-          // The item two back has stored its dK / dV out of this buffer.  Taken
-          // for items without steps as well (their zero dK / dV are staged in
-          // the buffer too), so that each wait is for the barrier's next phase.
-          if (v >= 2 && !mbar_wait(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort)) break;
-          if (itm.n == 0) continue;
-          mbar_arrive_expect_tx(&s.bar_kv[kb], 2 * kTileBytes);
-          tma_load_3d(s.kv[kb][0], &tm_k, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
-          tma_load_3d(s.kv[kb][1], &tm_v, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
-          for (int k = 0; k < itm.n; ++k, ++g) {
-            const int st = g % kStages;
-            const uint32_t use = g / kStages;
-            if (use > 0 && !mbar_wait(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) {
-              ok = false;
-              break;
-            }
-            const int i = qtile_of(a, itm, k);
-            const size_t stat = static_cast<size_t>(itm.bh) * a.n_pad + static_cast<size_t>(i) * kTile;
-            mbar_arrive_expect_tx(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
-            tma_load_3d(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, itm.bh);
-            tma_load_3d(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, itm.bh);
-            bulk_load(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
-            bulk_load(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
+        }
+        __syncwarp();
+        if (t >= n_items) break;
+        const Item itm = item_at(a, t);
+        const int kb = v & 1;
+        // The item two back has stored its dK / dV out of this buffer.  Taken
+        // for items without steps as well (their zero dK / dV are staged in
+        // the buffer too), so that each wait is for the barrier's next phase.
+        if (v >= 2 && !mbar_wait_warp(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort))
+          break;
+        if (itm.n == 0) continue;
+        mbar_arrive_expect_tx_w(&s.bar_kv[kb], 2 * kTileBytes);
+        tma_load_3d_w(s.kv[kb][0], &tm_k, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
+        tma_load_3d_w(s.kv[kb][1], &tm_v, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
+        for (int k = 0; k < itm.n; ++k, ++g) {
+          const int st = g % kStages;
+          const uint32_t use = g / kStages;
+          if (use > 0 && !mbar_wait_warp(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) {
+            ok = false;
+            break;
           }
+          const int i = qtile_of(a, itm, k);
+          const size_t stat = static_cast<size_t>(itm.bh) * a.n_pad + static_cast<size_t>(i) * kTile;
+          mbar_arrive_expect_tx_w(&s.bar_q_full[st], 2 * kTileBytes + 2 * kTile * 4);
+          tma_load_3d_w(s.q[st], &tm_q, &s.bar_q_full[st], 0, i * kTile, itm.bh);
+          tma_load_3d_w(s.dout[st], &tm_do, &s.bar_q_full[st], 0, i * kTile, itm.bh);
+          bulk_load_w(s.lse2[st], a.lse2 + stat, kTile * 4, &s.bar_q_full[st]);
+          bulk_load_w(s.dsum[st], a.dsum + stat, kTile * 4, &s.bar_q_full[st]);
         }
       }
     } else if (warp == 13) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
-        constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
-        bool ok = true;
-        int g = 0;
-        uint32_t kv_use[2] = {0u, 0u};
-        for (int v = 0; ok; ++v) {
-          if (!mbar_wait(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
-          const int t = s.item_ring[v & 3];
-          mbar_arrive(&s.bar_item_empty[v & 3]);
-          if (t >= n_items) break;
-          const Item itm = item_at(a, t);
-          if (itm.n == 0) continue;
-          const int kb = v & 1;
-          const uint32_t k_addr = smem_u32(s.kv[kb][0]), v_addr = smem_u32(s.kv[kb][1]);
-          if (!mbar_wait(&s.bar_kv[kb], kv_use[kb] & 1, pr.wait, &s.abort)) break;
-          ++kv_use[kb];
-          // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step gs.
-          auto issue_s = [&](int gs) -> bool {
-            const int st = gs % kStages;
-            if (!mbar_wait(&s.bar_q_full[st], (gs / kStages) & 1, pr.wait, &s.abort)) return false;
-            tc_fence_after();
-            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
-#pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk)
-              mma_bf16_ss(tmem + kColST, sdesc_sw128(k_addr + kk * 32, 16, 1024),
-                          sdesc_sw128(q_addr + kk * 32, 16, 1024), id_s, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk)
-              mma_bf16_ss(tmem + kColDPT, sdesc_sw128(v_addr + kk * 32, 16, 1024),
-                          sdesc_sw128(do_addr + kk * 32, 16, 1024), id_s, kk > 0);
-            mma_commit(&s.bar_s_full);
-            return true;
-          };
-          // the previous step's S^T / dP^T are in registers before they are overwritten
-          if (g > 0 && !mbar_wait(&s.bar_st_read, (g - 1) & 1, pr.wait, &s.abort)) break;
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(128, 64, true, true);    // dQ (A = dS, MN-major)
+      // shared-memory descriptors of the fixed buffers (start address in 16-byte
+      // units in the low bits: an offset of o bytes adds o / 16)
+      const uint64_t d_dst_k = sdesc_sw128(smem_u32(s.dst[0]), 16, 1024);         // dS^T, K-major
+      const uint64_t d_dst_mn = sdesc_sw128(smem_u32(s.dst[0]), kTileBytes, 1024);  // dS, MN-major
+      bool ok = true;
+      int g = 0;
+      uint32_t kv_use[2] = {0u, 0u};
+      for (int v = 0; ok; ++v) {
+        if (!mbar_wait_warp(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
+        const int t = s.item_ring[v & 3];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.bar_item_empty[v & 3]);
+        __syncwarp();
+        if (t >= n_items) break;
+        const Item itm = item_at(a, t);
+        if (itm.n == 0) continue;
+        const int kb = v & 1;
+        const uint32_t k_addr = smem_u32(s.kv[kb][0]), v_addr = smem_u32(s.kv[kb][1]);
+        const uint64_t d_k = sdesc_sw128(k_addr, 16, 1024), d_v = sdesc_sw128(v_addr, 16, 1024);
+        const uint64_t d_k_mn = sdesc_sw128(k_addr, 1024, 1024);
+        if (!mbar_wait_warp(&s.bar_kv[kb], kv_use[kb] & 1, pr.wait, &s.abort)) break;
+        ++kv_use[kb];
+        // S^T = K_j Q_i^T and dP^T = V_j dO_i^T for step gs.
+        auto issue_s = [&](int gs) -> bool {
+          const int st = gs % kStages;
+          if (!mbar_wait_warp(&s.bar_q_full[st], (gs / kStages) & 1, pr.wait, &s.abort))
+            return false;
           tc_fence_after();
-          if (!issue_s(g)) break;
-          for (int k = 0; k < itm.n; ++k, ++g) {
-            const int st = g % kStages;
-            if (k + 1 < itm.n) {
-              if (!mbar_wait(&s.bar_st_read, g & 1, pr.wait, &s.abort) || (tc_fence_after(), !issue_s(g + 1))) {
-                ok = false;
-                break;
-              }
-            }
-            // P^T of this step is in TMEM.
-            if (!mbar_wait(&s.bar_p_full, g & 1, pr.wait, &s.abort)) {
+          const uint64_t d_q = sdesc_sw128(smem_u32(s.q[st]), 16, 1024);
+          const uint64_t d_do = sdesc_sw128(smem_u32(s.dout[st]), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            mma_bf16_ss_w(tmem + kColST, d_k + kk * 2, d_q + kk * 2, id_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            mma_bf16_ss_w(tmem + kColDPT, d_v + kk * 2, d_do + kk * 2, id_s, kk > 0);
+          mma_commit_w(&s.bar_s_full);
+          return true;
+        };
+        // the previous step's S^T / dP^T are in registers before they are overwritten
+        if (g > 0 && !mbar_wait_warp(&s.bar_st_read, (g - 1) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        if (!issue_s(g)) break;
+        for (int k = 0; k < itm.n; ++k, ++g) {
+          const int st = g % kStages;
+          if (k + 1 < itm.n) {
+            if (!mbar_wait_warp(&s.bar_st_read, g & 1, pr.wait, &s.abort) ||
+                (tc_fence_after(), !issue_s(g + 1))) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint32_t q_addr = smem_u32(s.q[st]), do_addr = smem_u32(s.dout[st]);
-            // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per
-            // instruction), B = dO_i (queries x d, d contiguous: MN-major).
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                          sdesc_sw128(do_addr + kk * 2048, 1024, 1024), id_acc, (k > 0 || kk > 0));
-            mma_commit(&s.bar_pt_free);
-            // dS^T of this step is in shared memory.
-            if (!mbar_wait(&s.bar_ds_full, g & 1, pr.wait, &s.abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // dK += dS^T Q_i: A = dS^T (K-major over queries), B = Q_i (MN-major).
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t off = (kk & 3) * 32;
-              mma_bf16_ss(tmem + kColDK, sdesc_sw128(smem_u32(s.dst[kk >> 2]) + off, 16, 1024),
-                          sdesc_sw128(q_addr + kk * 2048, 1024, 1024), id_acc, (k > 0 || kk > 0));
-            }
-            mma_commit(&s.bar_q_empty[st]);
-            if (g > 0 && !mbar_wait(&s.bar_dq_free, (g - 1) & 1, pr.wait, &s.abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major
-            // operand (queries contiguous, two 64-query halves 16 KiB apart);
-            // B = K_j, MN-major (d contiguous).  K dimension = keys.
-            const uint32_t ds_addr = smem_u32(s.dst[0]);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_bf16_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, kTileBytes, 1024),
-                          sdesc_sw128(k_addr + kk * 2048, 1024, 1024), id_dq, kk > 0);
-            mma_commit(&s.bar_dq_full);
-            mma_commit(&s.bar_ds_free);
           }
-          if (ok) mma_commit(&s.bar_done);
+          // P^T of this step is in TMEM.
+          if (!mbar_wait_warp(&s.bar_p_full, g & 1, pr.wait, &s.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t d_q_mn = sdesc_sw128(smem_u32(s.q[st]), 1024, 1024);
+          const uint64_t d_do_mn = sdesc_sw128(smem_u32(s.dout[st]), 1024, 1024);
+          const uint32_t acc0 = k > 0 ? 1u : 0u;
+          // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 columns per
+          // instruction), B = dO_i (queries x d, d contiguous: MN-major).
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ts_w(tmem + kColDV, tmem + kColPT + kk * 8, d_do_mn + kk * 128, id_acc,
+                          kk > 0 ? 1u : acc0);
+          mma_commit_w(&s.bar_pt_free);
+          // dS^T of this step is in shared memory.
+          if (!mbar_wait_warp(&s.bar_ds_full, g & 1, pr.wait, &s.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dK += dS^T Q_i: A = dS^T (K-major over queries, two 64-query
+          // halves 16 KiB apart), B = Q_i (MN-major).
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss_w(tmem + kColDK, d_dst_k + (kk >> 2) * (kTileBytes >> 4) + (kk & 3) * 2,
+                          d_q_mn + kk * 128, id_acc, kk > 0 ? 1u : acc0);
+          mma_commit_w(&s.bar_q_empty[st]);
+          if (g > 0 && !mbar_wait_warp(&s.bar_dq_free, (g - 1) & 1, pr.wait, &s.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dQ_i = dS K_j: A = dS read from the dS^T tile as an MN-major
+          // operand (queries contiguous, two 64-query halves 16 KiB apart);
+          // B = K_j, MN-major (d contiguous).  K dimension = keys.
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss_w(tmem + kColDQ, d_dst_mn + kk * 128, d_k_mn + kk * 128, id_dq, kk > 0);
+          mma_commit_w(&s.bar_dq_full);
+          mma_commit_w(&s.bar_ds_free);
         }
+        if (ok) mma_commit_w(&s.bar_done);
       }
-      if (lane == 0) {
-        mma_commit(&s.bar_final);
-        mbar_wait_drain(&s.bar_final, 0, pr.wait);
-      }
+      mma_commit_w(&s.bar_final);
+      mbar_wait_drain(&s.bar_final, 0, pr.wait);
       __syncwarp();
     }
   }
