@@ -112,6 +112,8 @@ __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2
 #endif
 constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
+constexpr uint32_t kSoftmaxWarps = 4;
+
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&s.bar_v_empty[i], 1);
     }
     mbar_init(&s.bar_s_full, 1);
-    mbar_init(&s.bar_s_free, 128);
-    mbar_init(&s.bar_p_full, 128);
+    mbar_init(&s.bar_s_free, kSoftmaxWarps);   // one arrival per softmax warp
+    mbar_init(&s.bar_p_full, kSoftmaxWarps);
     mbar_init(&s.bar_o_done, 1);
     mbar_init(&s.bar_final, 1);
     s.abort = 0;
@@ -183,19 +185,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
+  // The producer and MMA warps run converged, whole-warp: waits are one
+  // decision per warp and an elected lane issues each copy and MMA.
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
-      mbar_arrive_expect_tx(&s.bar_q, kTileBytes);
-      tma_load_3d(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+    if (n > 0) {
+      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
       if (!args.starve) {
         auto load_k = [&](int it) -> bool {
           const int st = it % kKStages;
           const uint32_t use = it / kKStages;
-          if (use > 0 && !mbar_wait(&s.bar_k_empty[st], (use - 1) & 1, pr.wait, &s.abort))
+          if (use > 0 && !mbar_wait_warp(&s.bar_k_empty[st], (use - 1) & 1, pr.wait, &s.abort))
             return false;
-          mbar_arrive_expect_tx(&s.bar_k_full[st], kTileBytes);
-          tma_load_3d(s.k[st], &tm_k, &s.bar_k_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
+          mbar_arrive_expect_tx_w(&s.bar_k_full[st], kTileBytes);
+          tma_load_3d_w(s.k[st], &tm_k, &s.bar_k_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
           return true;
         };
         bool ok = load_k(0);
@@ -203,61 +207,59 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (it + 1 < n && !load_k(it + 1)) break;
           const int st = it % kVStages;
           const uint32_t use = it / kVStages;
-          if (use > 0 && !mbar_wait(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort)) break;
-          mbar_arrive_expect_tx(&s.bar_v_full[st], kTileBytes);
-          tma_load_3d(s.v[st], &tm_v, &s.bar_v_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
+          if (use > 0 && !mbar_wait_warp(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort))
+            break;
+          mbar_arrive_expect_tx_w(&s.bar_v_full[st], kTileBytes);
+          tma_load_3d_w(s.v[st], &tm_v, &s.bar_v_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
         }
       }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    if (n > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, 64, false, true);
-      const uint32_t q_addr = smem_u32(s.q);
-      bool ok = mbar_wait(&s.bar_q, 0, pr.wait, &s.abort);
+      const uint64_t d_q = sdesc_sw128(smem_u32(s.q), 16, 1024);
+      bool ok = mbar_wait_warp(&s.bar_q, 0, pr.wait, &s.abort);
       // S_it = Q K_it^T into the S columns.
       auto issue_s = [&](int it) -> bool {
         const int st = it % kKStages;
-        if (!mbar_wait(&s.bar_k_full[st], (it / kKStages) & 1, pr.wait, &s.abort)) return false;
+        if (!mbar_wait_warp(&s.bar_k_full[st], (it / kKStages) & 1, pr.wait, &s.abort))
+          return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(s.k[st]);
+        const uint64_t d_k = sdesc_sw128(smem_u32(s.k[st]), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          mma_bf16_ss(tmem + kColS, sdesc_sw128(q_addr + kk * 32, 16, 1024),
-                      sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&s.bar_s_full);
-        mma_commit(&s.bar_k_empty[st]);
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          mma_bf16_ss_w(tmem + kColS, d_q + kk * 2, d_k + kk * 2, idesc_s, kk > 0);
+        mma_commit_w(&s.bar_s_full);
+        mma_commit_w(&s.bar_k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int it = 0; ok && it < n; ++it) {
         // the softmax has copied S_it into registers: the S columns are free
-        if (!mbar_wait(&s.bar_s_free, it & 1, pr.wait, &s.abort)) break;
+        if (!mbar_wait_warp(&s.bar_s_free, it & 1, pr.wait, &s.abort)) break;
         if (it + 1 < n && !issue_s(it + 1)) break;
-        if (!mbar_wait(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
+        if (!mbar_wait_warp(&s.bar_p_full, it & 1, pr.wait, &s.abort)) break;
         const int st = it % kVStages;
-        if (!mbar_wait(&s.bar_v_full[st], (it / kVStages) & 1, pr.wait, &s.abort)) break;
+        if (!mbar_wait_warp(&s.bar_v_full[st], (it / kVStages) & 1, pr.wait, &s.abort)) break;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(s.v[st]);
+        // A = P~ from TMEM (16 keys = 8 packed columns per step); V_j is
+        // [keys][d] with d contiguous: an MN-major B operand, one 64-wide
+        // swizzle atom along N, 8-key groups 1024 bytes apart.
+        const uint64_t d_v = sdesc_sw128(smem_u32(s.v[st]), 1024, 1024);
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // A = P~ from TMEM (16 keys = 8 packed columns per step); V_j is
-          // [keys][d] with d contiguous: an MN-major B operand, one 64-wide
-          // swizzle atom along N, 8-key groups 1024 bytes apart.
-          mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8,
-                      sdesc_sw128(v_addr + kk * 2048, 1024, 1024), idesc_o, (it > 0 || kk > 0));
-        }
-        mma_commit(&s.bar_o_done);
-        mma_commit(&s.bar_v_empty[st]);
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts_w(tmem + kColO, tmem + kColP + kk * 8, d_v + kk * 128, idesc_o,
+                        kk > 0 ? 1u : acc0);
+        mma_commit_w(&s.bar_o_done);
+        mma_commit_w(&s.bar_v_empty[st]);
       }
     }
-    if (lane == 0) {
-      // make sure no MMA is in flight before TMEM is released
-      mma_commit(&s.bar_final);
-      mbar_wait_drain(&s.bar_final, 0, pr.wait);
-    }
+    // make sure no MMA is in flight before TMEM is released
+    mma_commit_w(&s.bar_final);
+    mbar_wait_drain(&s.bar_final, 0, pr.wait);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (rows)
@@ -288,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
       }
       tc_fence_before();
-      mbar_arrive(&s.bar_s_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar_s_free);
       const int key0 = j * kTile;
       const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
       if (edge) {
@@ -350,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       l = l * alpha + rs;
       m = m_ref;
       tc_fence_before();
-      mbar_arrive(&s.bar_p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar_p_full);
     }
     // ---------------------------------------------------------- epilogue
     if (ok) {
