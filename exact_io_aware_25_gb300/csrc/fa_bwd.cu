@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
 //                             reduce-add into the fp32 accumulators (thread = query row)
 //   warpgroup 3: warp 12      TMA producer
 //                warp 13      TMEM owner and MMA issuer
-//                warps 14-15  idle
+//                warp 14      dK / dV stores (TMA) from the staging buffer
+//                warp 15      idle
 // Launched at 128 registers per thread; the elementwise warpgroups then take
 // 160 (room for all 64 S^T and dP^T columns of a thread), the dQ warpgroup and
 // the producer / MMA warpgroup 96 each: 160 + 160 + 96 + 96 = 4 x 128.
@@ -222,6 +223,8 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_dq_free;
   uint64_t bar_done;
   uint64_t bar_final;
+  uint64_t bar_epi_full[2];   // dK / dV of the item staged in kv[parity]
+  int epi_item[2];            // its item id, -1 = no more items
   uint64_t bar_item_full[4];
   uint64_t bar_item_empty[4];
   int item_ring[4];
@@ -375,6 +378,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&s.bar_dq_free, kDqWarps);
     mbar_init(&s.bar_done, 1);
     mbar_init(&s.bar_final, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&s.bar_epi_full[i], kEwWarps);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s.bar_item_full[i], 1);
       mbar_init(&s.bar_item_empty[i], kItemConsumers);
@@ -415,6 +419,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bool ok = true;
     int g = 0;          // step counter of this CTA
     uint32_t done_par = 0;
+    int last_v = 0;     // items handed to the store warp
     for (int v = 0; ok; ++v) {
       if (!wg_wait(&s.bar_item_full[v & 3], (v >> 2) & 1)) break;
       const int t = s.item_ring[v & 3];
@@ -487,17 +492,25 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const uint32_t col = half == 0 ? kColDV : kColDK;
       const float mul = half == 0 ? 1.f : pr.scale;
       const int kb = v & 1;
+      // the store of the item two back has read this staging buffer (implied
+      // by done for items with steps; waited here for the others too)
+      if (v >= 2 && !w_wait(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
       const uint32_t dst = smem_u32(s.kv[kb][half == 0 ? 1 : 0]) + kr * 128;
+      uint32_t r0[32], r1[32];
+      if (itm.n > 0) {
+        tmem_ld32(tmem + lane_base + col, r0);
+        tmem_ld32(tmem + lane_base + col + 32, r1);
+        tmem_wait_ld_tied32(r0, r1);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) r0[c] = r1[c] = 0u;
+      }
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t r[32];
-        if (itm.n > 0) {
-          tmem_ld32(tmem + lane_base + col + h2 * 32, r);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = 0u;
-        }
+        const uint32_t *r = h2 == 0 ? r0 : r1;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           const int c0 = ch * 8;
@@ -510,20 +523,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      // both warpgroups (dV and dK halves) agree before the store
-      if (!named_bar_and(1, 256, !s.abort)) {
-        ok = false;
-        break;
-      }
-      if (tid == 0) {
-        tma_store_3d(&tm_dv, s.kv[kb][1], 0, itm.kt * kTile, itm.bh);
-        tma_store_3d(&tm_dk, s.kv[kb][0], 0, itm.kt * kTile, itm.bh);
-        bulk_commit();
-        bulk_wait_read_all();  // the staging buffer may be reloaded now
-        mbar_arrive(&s.bar_kv_free[kb]);
+      // the store warp takes it from here
+      if (tid == 0) s.epi_item[kb] = t;
+      warp_arrive(&s.bar_epi_full[kb]);
+      last_v = v + 1;
+    }
+    // tell the store warp there is nothing more (after it is done with the
+    // staging buffer's previous use, whose item id shares the slot)
+    if (ok) {
+      const int kb = last_v & 1;
+      if (last_v < 2 || w_wait(&s.bar_kv_free[kb], ((last_v - 2) >> 1) & 1)) {
+        if (tid == 0) s.epi_item[kb] = -1;
+        warp_arrive(&s.bar_epi_full[kb]);
       }
     }
-    if (tid == 0) bulk_wait_all();
   } else if (warp < 12) {
     setmaxnreg_dec<kRegsDq>();
     // ------------------------------------------------------------ dQ partials (rows = queries)
@@ -732,6 +745,26 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       mma_commit_w(&s.bar_final);
       mbar_wait_drain(&s.bar_final, 0, pr.wait);
+      __syncwarp();
+    } else if (warp == 14) {
+      // ---------------------------------------------------------- dK / dV store
+      for (int u = 0;; ++u) {
+        const int kb = u & 1;
+        if (!mbar_wait_warp(&s.bar_epi_full[kb], (u >> 1) & 1, pr.wait, &s.abort)) break;
+        const int t = s.epi_item[kb];
+        if (t < 0) break;
+        const int BH = pr.B * pr.H;
+        const int kt = t / BH, bh = t - (t / BH) * BH;
+        if (lane == 0) {
+          tma_store_3d(&tm_dv, s.kv[kb][1], 0, kt * kTile, bh);
+          tma_store_3d(&tm_dk, s.kv[kb][0], 0, kt * kTile, bh);
+          bulk_commit();
+          bulk_wait_read_all();  // the staging buffer may be reloaded now
+          mbar_arrive(&s.bar_kv_free[kb]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) bulk_wait_all();
       __syncwarp();
     }
   }
