@@ -83,6 +83,16 @@ def _load():
             lib.fa_oracle_bwd.argtypes = [dp, dp, dp, dp, ci, ci, ci, ci, cd, ci, i32p, u8p, ci,
                                           i64p, cl, i64p, cl, dp, dp, dp, ci]
             lib.fa_oracle_bwd.restype = ci
+            u64 = ctypes.c_uint64
+            lib.fa_oracle_fwd_dropout.argtypes = [dp, dp, dp, ci, ci, ci, ci, cd, ci, i32p, u8p,
+                                                  ci, ci, u64, i64p, cl, dp, dp, ci]
+            lib.fa_oracle_fwd_dropout.restype = ci
+            lib.fa_oracle_bwd_dropout.argtypes = [dp, dp, dp, dp, ci, ci, ci, ci, cd, ci, i32p,
+                                                  u8p, ci, ci, u64, i64p, cl, i64p, cl, dp, dp,
+                                                  dp, ci]
+            lib.fa_oracle_bwd_dropout.restype = ci
+            lib.fa_oracle_keep.argtypes = [u64, ci, ci, ci, ci]
+            lib.fa_oracle_keep.restype = ci
             _lib = lib
     return _lib
 
@@ -123,13 +133,25 @@ def _shape(q):
     return q.shape
 
 
+def drop_p8(p):
+    """Dropout threshold in 1/256 units for drop probability p in [0, 1):
+    p * 256 rounded to nearest, ties to even, at most 255."""
+    return min(int(np.rint(np.float32(p) * np.float32(256.0))), 255)
+
+
+def keep(seed, p8, bh, i, j):
+    """Dropout keep mask Z_ij (1 kept, 0 dropped) of head bh."""
+    return int(_load().fa_oracle_keep(int(seed), int(p8), int(bh), int(i), int(j)))
+
+
 def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=None,
-            nthreads=None, block=BLOCK):
+            nthreads=None, block=BLOCK, p8=0, seed=0):
     """Exact forward.  q, k, v: float64 [B, H, N, d].
 
     rows: optional int64 array of global row ids (bh * N + i).  Returns
     (o, lse): o [B, H, N, d] and lse [B, H, N] for rows=None, else o [nrows, d]
-    and lse [nrows].
+    and lse [nrows].  p8 > 0 applies dropout with keep mask keep(seed, p8, ...)
+    and keep scale 256 / (256 - p8) to P before the product with V.
     """
     lib = _load()
     B, H, N, d = _shape(q)
@@ -142,8 +164,9 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=Non
     nrows = B * H * N if rows is None else len(ra)
     o = np.zeros((nrows, d), np.float64)
     lse = np.zeros((nrows,), np.float64)
-    rc = lib.fa_oracle_fwd(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), klp, bmp,
-                           int(block), rp, nrows, _f64(o)[1], _f64(lse)[1], _threads(nthreads))
+    rc = lib.fa_oracle_fwd_dropout(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), klp,
+                                   bmp, int(block), int(p8), int(seed), rp, nrows, _f64(o)[1],
+                                   _f64(lse)[1], _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"fa_oracle_fwd failed ({rc})")
     if rows is None:
@@ -187,8 +210,8 @@ def forward_tiled(q, k, v, scale, Br, Bc, causal=False, kv_len=None, block_mask=
 
 
 def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, q_rows=None,
-             k_rows=None, nthreads=None, block=BLOCK):
-    """Textbook backward.  Returns (dq, dk, dv).
+             k_rows=None, nthreads=None, block=BLOCK, p8=0, seed=0):
+    """Textbook backward (of the dropped-out forward when p8 > 0).  Returns (dq, dk, dv).
 
     With q_rows/k_rows None the results are full [B, H, N, d] arrays;
     otherwise dq is [len(q_rows), d] and dk, dv are [len(k_rows), d].  Pass an
@@ -209,9 +232,9 @@ def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, q
     dq = np.zeros((max(nq, 1), d), np.float64)
     dk = np.zeros((max(nk, 1), d), np.float64)
     dv = np.zeros((max(nk, 1), d), np.float64)
-    rc = lib.fa_oracle_bwd(qp, kp, vp, dp, B, H, N, d, float(scale), int(bool(causal)), klp,
-                           bmp, int(block), qrp, nq, krp, nk, _f64(dq)[1], _f64(dk)[1],
-                           _f64(dv)[1], _threads(nthreads))
+    rc = lib.fa_oracle_bwd_dropout(qp, kp, vp, dp, B, H, N, d, float(scale), int(bool(causal)),
+                                   klp, bmp, int(block), int(p8), int(seed), qrp, nq, krp, nk,
+                                   _f64(dq)[1], _f64(dk)[1], _f64(dv)[1], _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"fa_oracle_bwd failed ({rc})")
     dq, dk, dv = dq[:nq], dk[:nk], dv[:nk]

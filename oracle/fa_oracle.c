@@ -31,6 +31,16 @@
  *     dV = P^T dO,  dP = dO V^T,  D_i = <dO_i, o_i>,  dS = P o (dP - D),
  *     dQ = scale * dS K,  dK = scale * dS^T Q.
  *
+ * Dropout (fused into the kernels per [EXPL] "Key ideas", kernel fusion; the
+ * pages give no formula, so the standard one is used): with a keep mask Z and
+ * keep scale c = 1 / (1 - p8/256),
+ *     o_i = sum_j P_ij Z_ij c v_j  (lse from P, before dropout),
+ *     dV_j = sum_i P_ij Z_ij c dO_i,  dS_ij = P_ij (Z_ij c dP_ij - D_i),
+ * with D_i = <dO_i, o_i> of the dropped-out o.  Z is drawn from a
+ * counter-based generator, the 32-bit PCG hash of Jarzynski and Olano
+ * ("Hash Functions for GPU Rendering", JCGT 9(3), 2020), keyed by the seed
+ * and the head and counted by the 2x2 block (i/2, j/2); see keep() below.
+ *
  * Everything is in double precision, with plain loops and no blocking,
  * fusion or reordering beyond the definitions above.  Threads (pthreads)
  * split independent rows only; each row's arithmetic is sequential.
@@ -54,6 +64,9 @@ typedef struct {
     const int32_t *kv_len;
     const uint8_t *block_mask;
     int blk, nb;
+    int p8;             /* dropout threshold in 1/256 units; 0 = no dropout */
+    uint64_t seed;
+    double keep_scale;  /* 256 / (256 - p8) */
 } problem;
 
 static void problem_init(problem *p, const double *q, const double *k, const double *v,
@@ -66,6 +79,43 @@ static void problem_init(problem *p, const double *q, const double *k, const dou
     p->kv_len = kv_len; p->block_mask = block_mask;
     p->blk = blk > 0 ? blk : 128;
     p->nb = (N + p->blk - 1) / p->blk;
+    p->p8 = 0;
+    p->seed = 0;
+    p->keep_scale = 1.0;
+}
+
+static void problem_dropout(problem *p, int p8, uint64_t seed) {
+    p->p8 = p8;
+    p->seed = seed;
+    p->keep_scale = 256.0 / (256.0 - (double)p8);
+}
+
+/* The PCG hash: one LCG step of the 32-bit PCG generator followed by its
+ * RXS-M-XS output permutation (Jarzynski and Olano, JCGT 2020, "pcg"). */
+static uint32_t pcg_hash(uint32_t x) {
+    const uint32_t state = x * 747796405u + 2891336453u;
+    const uint32_t word = ((state >> ((state >> 28) + 4u)) ^ state) * 277803737u;
+    return (word >> 22) ^ word;
+}
+
+/* Dropout keep mask Z for (head bh, query i, key j): one 32-bit hash per 2x2
+ * block of the head, keyed by the seed and the head; the block's four
+ * elements take its four bytes.  Kept when the byte is >= p8. */
+static int keep(uint64_t seed, int p8, int bh, int i, int j) {
+    const uint32_t k0 = pcg_hash((uint32_t)(seed & 0xffffffffu));
+    const uint32_t k1 = pcg_hash(k0 ^ (uint32_t)(seed >> 32));
+    const uint32_t kb = pcg_hash(k1 ^ (uint32_t)bh);
+    const uint32_t ctr = ((uint32_t)(i >> 1) << 16) | (uint32_t)(j >> 1);
+    const uint32_t r = pcg_hash(kb ^ ctr);
+    const int byte = ((i & 1) << 1) | (j & 1);
+    const int u = (int)((r >> (8 * byte)) & 0xffu);
+    return u >= p8;
+}
+
+/* Z_ij * keep_scale (1 when there is no dropout). */
+static double drop_factor(const problem *p, int bh, int i, int j) {
+    if (p->p8 == 0) return 1.0;
+    return keep(p->seed, p->p8, bh, i, j) ? p->keep_scale : 0.0;
 }
 
 /* Key bound of batch b: kv_len[b] clamped to [0, N]. */
@@ -123,10 +173,10 @@ static int forward_row(const problem *p, int bh, int i, double *s, double *m_out
     double l = 0.0;
     for (int j = 0; j < p->N; ++j)
         if (allowed(p, b, i, j)) l += exp(s[j] - m);
-    /* 4.-5. normalised probabilities times V */
+    /* 4.-5. normalised probabilities (dropped out and rescaled) times V */
     for (int j = 0; j < p->N; ++j) {
         if (!allowed(p, b, i, j)) continue;
-        const double pij = exp(s[j] - m) / l;
+        const double pij = exp(s[j] - m) / l * drop_factor(p, bh, i, j);
         const double *vj = row_of(p->v, p, bh, j);
         for (int c = 0; c < d; ++c) o[c] += pij * vj[c];
     }
@@ -216,19 +266,35 @@ static void fwd_item(void *vctx, int64_t item, double *s) {
  * head bh (NULL selects every row, in order).  o is [nrows, d], lse [nrows].
  * Returns 0 on success, a negative value on bad arguments / no memory.
  */
-int fa_oracle_fwd(const double *q, const double *k, const double *v, int B, int H, int N,
-                  int d, double scale, int causal, const int32_t *kv_len,
-                  const uint8_t *block_mask, int blk, const int64_t *rows, int64_t nrows,
-                  double *o, double *lse, int nthreads) {
+int fa_oracle_fwd_dropout(const double *q, const double *k, const double *v, int B, int H,
+                          int N, int d, double scale, int causal, const int32_t *kv_len,
+                          const uint8_t *block_mask, int blk, int p8, uint64_t seed,
+                          const int64_t *rows, int64_t nrows, double *o, double *lse,
+                          int nthreads) {
     if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    if (p8 < 0 || p8 > 255) return -1;
     problem p;
     problem_init(&p, q, k, v, NULL, B, H, N, d, scale, causal, kv_len, block_mask, blk);
+    problem_dropout(&p, p8, seed);
     const int64_t total = (int64_t)B * H * N;
     if (!rows) nrows = total;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= total) return -1;
     fwd_ctx c = {&p, rows, o, lse};
     return parallel_for(nrows, nthreads, (size_t)N, fwd_item, &c);
+}
+
+int fa_oracle_fwd(const double *q, const double *k, const double *v, int B, int H, int N,
+                  int d, double scale, int causal, const int32_t *kv_len,
+                  const uint8_t *block_mask, int blk, const int64_t *rows, int64_t nrows,
+                  double *o, double *lse, int nthreads) {
+    return fa_oracle_fwd_dropout(q, k, v, B, H, N, d, scale, causal, kv_len, block_mask, blk, 0,
+                                 0, rows, nrows, o, lse, nthreads);
+}
+
+/* The dropout keep mask Z_ij (1 kept, 0 dropped) of head bh. */
+int fa_oracle_keep(uint64_t seed, int p8, int bh, int i, int j) {
+    return keep(seed, p8, bh, i, j);
 }
 
 /*
@@ -401,7 +467,7 @@ static void dq_item(void *vctx, int64_t item, double *s) {
         const double sij = p->scale * dot(qi, row_of(p->k, p, bh, j), d);
         const double pij = exp(sij - m) / l;
         const double dpij = dot(doi, row_of(p->v, p, bh, j), d);
-        const double dsij = pij * (dpij - D);
+        const double dsij = pij * (drop_factor(p, bh, i, j) * dpij - D);
         const double *kj = row_of(p->k, p, bh, j);
         for (int cc = 0; cc < d; ++cc) dq[cc] += p->scale * dsij * kj[cc];
     }
@@ -425,9 +491,10 @@ static void dkdv_item(void *vctx, int64_t item, double *s) {
         const double sij = p->scale * dot(qi, kj, d);
         const double pij = exp(sij - m) / l;
         const double dpij = dot(doi, vj, d);
-        const double dsij = pij * (dpij - D);
+        const double zc = drop_factor(p, bh, i, j);
+        const double dsij = pij * (zc * dpij - D);
         for (int cc = 0; cc < d; ++cc) {
-            dv[cc] += pij * doi[cc];
+            dv[cc] += pij * zc * doi[cc];
             dk[cc] += p->scale * dsij * qi[cc];
         }
     }
@@ -441,16 +508,19 @@ static void dkdv_item(void *vctx, int64_t item, double *s) {
  * rows that are needed (the dQ rows, plus every row that attends to one of
  * the selected keys).
  */
-int fa_oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
-                  int B, int H, int N, int d, double scale, int causal,
-                  const int32_t *kv_len, const uint8_t *block_mask, int blk,
-                  const int64_t *q_rows, int64_t nq, const int64_t *k_rows, int64_t nk,
-                  double *dq, double *dk, double *dv, int nthreads) {
+int fa_oracle_bwd_dropout(const double *q, const double *k, const double *v,
+                          const double *dout, int B, int H, int N, int d, double scale,
+                          int causal, const int32_t *kv_len, const uint8_t *block_mask, int blk,
+                          int p8, uint64_t seed, const int64_t *q_rows, int64_t nq,
+                          const int64_t *k_rows, int64_t nk, double *dq, double *dk,
+                          double *dv, int nthreads) {
     if (!q || !k || !v || !dout || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    if (p8 < 0 || p8 > 255) return -1;
     if ((nq != 0 || !q_rows) && !dq) return -1;
     if ((nk != 0 || !k_rows) && (!dk || !dv)) return -1;
     problem p;
     problem_init(&p, q, k, v, dout, B, H, N, d, scale, causal, kv_len, block_mask, blk);
+    problem_dropout(&p, p8, seed);
     const int64_t total = (int64_t)B * H * N;
     if (!q_rows) nq = total;
     if (!k_rows) nk = total;
@@ -512,4 +582,13 @@ int fa_oracle_bwd(const double *q, const double *k, const double *v, const doubl
 done:
     free(need); free(row_index); free(fwd_rows); free(fm); free(fl); free(fD); free(fo);
     return rc;
+}
+
+int fa_oracle_bwd(const double *q, const double *k, const double *v, const double *dout,
+                  int B, int H, int N, int d, double scale, int causal,
+                  const int32_t *kv_len, const uint8_t *block_mask, int blk,
+                  const int64_t *q_rows, int64_t nq, const int64_t *k_rows, int64_t nk,
+                  double *dq, double *dk, double *dv, int nthreads) {
+    return fa_oracle_bwd_dropout(q, k, v, dout, B, H, N, d, scale, causal, kv_len, block_mask,
+                                 blk, 0, 0, q_rows, nq, k_rows, nk, dq, dk, dv, nthreads);
 }

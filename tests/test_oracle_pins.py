@@ -337,3 +337,137 @@ def test_cross_check_with_numpy_definition(oracle_mod):
             np.testing.assert_allclose(dv[b, h], dV, rtol=0, atol=1e-12)
             np.testing.assert_allclose(dq[b, h], scale * dS @ k[b, h], rtol=0, atol=1e-12)
             np.testing.assert_allclose(dk[b, h], scale * dS.T @ q[b, h], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- dropout
+#
+# Dropout is fused into the kernels ([EXPL] "Key ideas", kernel fusion); the
+# keep mask comes from a counter-based hash both sides implement from its
+# published definition.  These pins tie the oracle's dropout to the
+# definition O = (P o Z) V / (1 - p') through paths that do not use it.
+
+
+def test_dropout_with_zero_threshold_is_the_plain_definition(oracle_mod):
+    rng = np.random.default_rng(30)
+    B, H, N, d = 2, 2, 19, 4
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    o1, l1 = oracle_mod.forward(q, k, vv, 0.7, causal=True)
+    o2, l2 = oracle_mod.forward(q, k, vv, 0.7, causal=True, p8=0, seed=1234)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    g1 = oracle_mod.backward(q, k, vv, do, 0.7, causal=True)
+    g2 = oracle_mod.backward(q, k, vv, do, 0.7, causal=True, p8=0, seed=99)
+    for a, b in zip(g1, g2):
+        assert np.array_equal(a, b)
+
+
+def _keep_grid(oracle_mod, seed, p8, bh, n):
+    return np.array([[oracle_mod.keep(seed, p8, bh, i, j) for j in range(n)] for i in range(n)])
+
+
+@pytest.mark.parametrize("p8", [26, 128, 230])
+def test_dropout_keep_rate_and_nested_thresholds(oracle_mod, p8):
+    """The kept fraction is 1 - p8/256 within 5 binomial sigmas, and a higher
+    threshold keeps a subset of what a lower one keeps (keep iff byte >= p8)."""
+    n = 96
+    z = np.concatenate([_keep_grid(oracle_mod, 7, p8, bh, n).ravel() for bh in (0, 5)])
+    p_keep = 1 - p8 / 256
+    sigma = math.sqrt(p_keep * (1 - p_keep) / z.size)
+    assert abs(z.mean() - p_keep) < 5 * sigma
+    z_hi = _keep_grid(oracle_mod, 7, min(p8 + 20, 255), 0, n)
+    assert np.all(z_hi <= _keep_grid(oracle_mod, 7, p8, 0, n))
+
+
+def test_dropout_bytes_are_uniform_and_depend_on_seed_and_head(oracle_mod):
+    """Recover each element's byte (the largest threshold that still keeps it)
+    and check it is uniform over 0..255 (chi-square, 255 degrees of freedom);
+    other seeds and heads give different masks."""
+    n = 48
+
+    def byte(seed, bh, i, j):
+        lo, hi = 0, 255                      # keep(0) always holds
+        while lo < hi:
+            mid = (lo + hi + 1) // 2
+            if oracle_mod.keep(seed, mid, bh, i, j):
+                lo = mid
+            else:
+                hi = mid - 1
+        return lo
+
+    u = np.array([byte(3, bh, i, j) for bh in (0, 1) for i in range(n) for j in range(n)])
+    counts = np.bincount(u, minlength=256)
+    expected = u.size / 256
+    chi2 = float(((counts - expected) ** 2 / expected).sum())
+    assert chi2 < 255 + 6 * math.sqrt(2 * 255)
+    a = _keep_grid(oracle_mod, 3, 128, 0, n)
+    assert (a != _keep_grid(oracle_mod, 4, 128, 0, n)).mean() > 0.3
+    assert (a != _keep_grid(oracle_mod, 3, 128, 1, n)).mean() > 0.3
+    assert (a != _keep_grid(oracle_mod, 3 + (1 << 32), 128, 0, n)).mean() > 0.3
+
+
+def test_dropout_forward_equals_masked_probabilities_times_values(oracle_mod):
+    """o_i = sum_j P_ij Z_ij v_j * 256/(256-p8) with P from the plain
+    probabilities and Z from the keep mask, for every mask variant."""
+    rng = np.random.default_rng(31)
+    B, H, N, d, blk, scale, p8, seed = 2, 2, 21, 5, 4, 0.9, 77, 2024
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    kw = _variant_args(rng, B, N, blk, dict(causal=True, kv_len=True, mask=True))
+    o, lse = oracle_mod.forward(q, k, vv, scale, p8=p8, seed=seed, **kw)
+    _, lse0 = oracle_mod.forward(q, k, vv, scale, **kw)
+    np.testing.assert_array_equal(lse, lse0)          # lse is taken before dropout
+    for b in range(B):
+        for h in range(H):
+            bh = b * H + h
+            P = oracle_mod.probs(q, k, scale, bh=bh, **kw)
+            Z = _keep_grid(oracle_mod, seed, p8, bh, N)
+            want = (P * Z) @ vv[b, h] * (256.0 / (256 - p8))
+            np.testing.assert_allclose(o[b, h], want, rtol=0, atol=1e-12)
+
+
+def test_dropout_backward_matches_central_finite_differences(oracle_mod):
+    """With the keep mask fixed, the dropout forward is smooth in q, k, v:
+    its dQ, dK, dV against central differences of sum(dO o O)."""
+    rng = np.random.default_rng(32)
+    B, H, N, d, blk, scale, h, p8, seed = 1, 2, 10, 3, 4, 0.8, 1e-6, 90, 5
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    kw = _variant_args(rng, B, N, blk, dict(causal=True, kv_len=True))
+
+    def loss(q_, k_, v_):
+        o, _ = oracle_mod.forward(q_, k_, v_, scale, p8=p8, seed=seed, **kw)
+        return float(np.sum(do * o))
+
+    dq, dk, dv = oracle_mod.backward(q, k, vv, do, scale, p8=p8, seed=seed, **kw)
+    for which, grad in (("q", dq), ("k", dk), ("v", dv)):
+        num = np.zeros_like(grad)
+        base = {"q": q, "k": k, "v": vv}
+        for idx in np.ndindex(*grad.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (loss(plus["q"], plus["k"], plus["v"])
+                        - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.linalg.norm(num - grad) / max(np.linalg.norm(grad), 1e-30)
+        assert err < 1e-6, (which, err)
+
+
+def test_dropout_output_is_unbiased_over_seeds(oracle_mod):
+    """The keep scale makes the dropped-out output an unbiased estimate of the
+    plain one: the mean over 400 seeds is within a few standard errors."""
+    rng = np.random.default_rng(33)
+    B, H, N, d, scale, p8 = 1, 1, 12, 4, 0.5, 64
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    o0, _ = oracle_mod.forward(q, k, vv, scale)
+    runs = np.stack([oracle_mod.forward(q, k, vv, scale, p8=p8, seed=s)[0] for s in range(400)])
+    se = runs.std(axis=0) / math.sqrt(runs.shape[0])
+    z = np.abs(runs.mean(axis=0) - o0) / np.maximum(se, 1e-12)
+    assert np.mean(z < 4) > 0.98 and np.max(z) < 6
+
+
+def test_dropout_threshold_rounding(oracle_mod):
+    assert oracle_mod.drop_p8(0.0) == 0
+    assert oracle_mod.drop_p8(0.1) == 26          # 25.6 -> 26
+    assert oracle_mod.drop_p8(0.5) == 128
+    assert oracle_mod.drop_p8(0.998) == 255       # 255.49 -> 255
+    assert oracle_mod.drop_p8(0.9999) == 255      # 255.97 rounds to 256, capped
+    assert oracle_mod.drop_p8(1.5 / 256) == 2     # tie 1.5 -> even
+    assert oracle_mod.drop_p8(2.5 / 256) == 2     # tie 2.5 -> even
