@@ -64,6 +64,13 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp,
                                  vp, vp, sz, vp]
             L.fa_bwd.restype = ci
+            u64 = ctypes.c_ulonglong
+            L.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp, vp, cf,
+                                         u64, vp]
+            L.fa_fwd_dropout.restype = ci
+            L.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
+                                         ci, vp, vp, cf, u64, vp, sz, vp]
+            L.fa_bwd_dropout.restype = ci
             L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                          ci, vp, vp, vp]
             L.fa_bwd_noalloc.restype = ci
@@ -129,6 +136,29 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0, kv_le
                         _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
                         int(bool(causal)), _ptr(kv_len), _ptr(block_mask), _ptr(workspace),
                         int(workspace_bytes), _stream(stream)), "fa_bwd")
+
+
+def fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal=0, kv_len=None, block_mask=None,
+                   p=0.0, seed=0, stream=None) -> None:
+    """fa_fwd with dropout of probability p on P (keep mask from ``seed``; see
+    include/fa.h for its definition)."""
+    _check(lib().fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                int(N), int(d), float(scale), int(bool(causal)), _ptr(kv_len),
+                                _ptr(block_mask), float(p), int(seed) & (2**64 - 1),
+                                _stream(stream)), "fa_fwd_dropout")
+
+
+def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0, kv_len=None,
+                   block_mask=None, p=0.0, seed=0, workspace=None, workspace_bytes=0,
+                   stream=None) -> None:
+    """fa_bwd of the dropped-out forward (same p and seed as fa_fwd_dropout)."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d),
+                                float(scale), int(bool(causal)), _ptr(kv_len), _ptr(block_mask),
+                                float(p), int(seed) & (2**64 - 1), _ptr(workspace),
+                                int(workspace_bytes), _stream(stream)), "fa_bwd_dropout")
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0,

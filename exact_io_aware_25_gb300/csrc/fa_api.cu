@@ -112,8 +112,21 @@ fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t
   return FA_OK;
 }
 
+// Dropout threshold for drop probability p: p * 256 rounded to nearest (ties
+// to even, the default rounding mode), at most 255; -1 for p outside [0, 1).
+int drop_threshold(float p) {
+  if (!std::isfinite(p) || p < 0.f || p >= 1.f) return -1;
+  const long r = std::lrintf(p * 256.f);
+  return r > 255 ? 255 : static_cast<int>(r);
+}
+
+// Largest N whose query / key pair indices (i >> 1, j >> 1) fit the 16-bit
+// halves of the dropout hash counter.
+constexpr int kMaxDropN = 131072;
+
 Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t *kv_len,
-                     const uint8_t *block_mask, int *err) {
+                     const uint8_t *block_mask, int *err, int p8 = 0,
+                     unsigned long long seed = 0) {
   Problem p{};
   p.B = B;
   p.H = H;
@@ -127,6 +140,10 @@ Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t
   std::lock_guard<std::mutex> lk(g_mu);
   p.wait.err = err;
   p.wait.timeout_ns = static_cast<uint64_t>(g_timeout_ns);
+  p.drop_p8 = static_cast<uint32_t>(p8);
+  p.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.keep_scale = 256.f / static_cast<float>(256 - p8);
   return p;
 }
 
@@ -164,12 +181,16 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                 int N, int d, float scale, int causal, const int32_t *kv_len,
-                 const uint8_t *block_mask, void *stream) {
+fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t *kv_len, const uint8_t *block_mask, float p,
+                         unsigned long long seed, void *stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status st = validate_common(B, H, N, d, scale, block_mask);
   if (st != FA_OK) return st;
+  const int p8 = drop_threshold(p);
+  if (p8 < 0) return FA_ERR_INVALID_ARG;
+  if (p8 > 0 && N > kMaxDropN) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
   int dev = 0;
@@ -181,7 +202,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
       !encode_bhnd(&to, o, BH, N))
     return FA_ERR_CUDA;
   FwdArgs a{};
-  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err);
+  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
   a.lse = lse;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -193,18 +214,29 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
              : FA_ERR_CUDA;
 }
 
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int N, int d, float scale, int causal, const int32_t *kv_len,
+                 const uint8_t *block_mask, void *stream) {
+  return fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, block_mask, 0.f, 0ull,
+                        stream);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (validate_common(B, H, N, d, 1.f, nullptr) != FA_OK) return 0;
   return ws_layout(B, H, N).total;
 }
 
-fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
-                 float scale, int causal, const int32_t *kv_len, const uint8_t *block_mask,
-                 void *workspace, size_t workspace_bytes, void *stream) {
+fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t *kv_len,
+                         const uint8_t *block_mask, float p, unsigned long long seed,
+                         void *workspace, size_t workspace_bytes, void *stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   fa_status st = validate_common(B, H, N, d, scale, block_mask);
   if (st != FA_OK) return st;
+  const int p8 = drop_threshold(p);
+  if (p8 < 0) return FA_ERR_INVALID_ARG;
+  if (p8 > 0 && N > kMaxDropN) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
@@ -220,7 +252,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
       !encode_bhnd(&tdv, dv, BH, N))
     return FA_ERR_CUDA;
   BwdArgs a{};
-  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err);
+  a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
   a.n_pad = static_cast<int>(align_up(static_cast<size_t>(N), kTile));
   a.o = static_cast<const uint16_t *>(o);
   a.dout = static_cast<const uint16_t *>(dout);
@@ -246,6 +278,14 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                 float scale, int causal, const int32_t *kv_len, const uint8_t *block_mask,
+                 void *workspace, size_t workspace_bytes, void *stream) {
+  return fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, kv_len,
+                        block_mask, 0.f, 0ull, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_check(void *stream) {

@@ -307,23 +307,50 @@ __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int kr, bo
   }
 }
 
-// P^T of 32 columns as bf16 pairs into the TMEM P^T columns.
-__device__ __forceinline__ void store_p32(const uint32_t (&v)[32], int qc, uint32_t tmem_pt) {
+// Dropout keep bits of 32 query columns of this thread's key row: bit e is
+// Z(q0 + e, key).  kk = head key ^ (key >> 1); sh = 8 * (key & 1) selects the
+// key's byte among each 2x2 block word (even queries: bytes 0-1, odd: 2-3).
+__device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32_t p8, int q0) {
+  uint32_t bits = 0u;
+#pragma unroll 4
+  for (int e = 0; e < 32; e += 2) {
+    const uint32_t qp = static_cast<uint32_t>((q0 + e) >> 1);
+    const uint32_t r = pcg_hash(kk ^ (qp << 16)) >> sh;
+    bits |= static_cast<uint32_t>((r & 0xffu) >= p8) << e;
+    bits |= static_cast<uint32_t>(((r >> 16) & 0xffu) >= p8) << (e + 1);
+  }
+  return bits;
+}
+
+// P^T of 32 columns as bf16 pairs into the TMEM P^T columns; with dropout,
+// the dropped columns as 0 (the keep scale is applied to dV at the end).
+template <bool kDrop>
+__device__ __forceinline__ void store_p32(const uint32_t (&v)[32], int qc, uint32_t tmem_pt,
+                                          uint32_t keep) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t pw[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
-      pw[t] = pack_bf16(__uint_as_float(v[16 * c + 2 * t]), __uint_as_float(v[16 * c + 2 * t + 1]));
+    for (int t = 0; t < 8; ++t) {
+      const int e = 16 * c + 2 * t;
+      float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+      if (kDrop) {
+        x0 = (keep >> e) & 1u ? x0 : 0.f;
+        x1 = (keep >> (e + 1)) & 1u ? x1 : 0.f;
+      }
+      pw[t] = pack_bf16(x0, x1);
+    }
     tmem_st8(tmem_pt + ((qc + 16 * c) >> 1), pw);
   }
 }
 
 // Elementwise phase 2: dS^T = P^T o (dP^T - D_q) for 32 columns, bf16 into
-// row kr of this warpgroup's 128-byte-swizzled dS^T tile.
+// row kr of this warpgroup's 128-byte-swizzled dS^T tile.  With dropout,
+// dP^T is first multiplied by Z * keep_scale.
+template <bool kDrop>
 __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint32_t (&dv)[32],
                                            int qc, int half, int kr, uint32_t dsum,
-                                           uint32_t ds_row) {
+                                           uint32_t ds_row, uint32_t keep, float keep_scale) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t dw[8];
@@ -334,8 +361,11 @@ __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint3
       const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
       float ds[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        ds[u] = __uint_as_float(pv[e0 + u]) * (__uint_as_float(dv[e0 + u]) - dl[u]);
+      for (int u = 0; u < 4; ++u) {
+        float dp = __uint_as_float(dv[e0 + u]);
+        if (kDrop) dp = (keep >> (e0 + u)) & 1u ? dp * keep_scale : 0.f;
+        ds[u] = __uint_as_float(pv[e0 + u]) * (dp - dl[u]);
+      }
       dw[2 * g] = pack_bf16(ds[0], ds[1]);
       dw[2 * g + 1] = pack_bf16(ds[2], ds[3]);
     }
@@ -345,6 +375,7 @@ __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint3
   }
 }
 
+template <bool kDrop>
 __global__ void __launch_bounds__(kMainThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -427,9 +458,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (t >= n_items) break;
       const Item itm = item_at(a, t);
       const bool key_ok = itm.kt * kTile + kr < itm.kv_bound;
+      uint32_t drop_kk = 0u, drop_sh = 0u;
+      if (kDrop) {
+        const uint32_t key = static_cast<uint32_t>(itm.kt * kTile + kr);
+        drop_kk = drop_head_key(pr, itm.bh) ^ (key >> 1);
+        drop_sh = 8u * (key & 1u);
+      }
       for (int k = 0; k < itm.n; ++k, ++g) {
         const int st = g % kStages;
         const int i = qtile_of(a, itm, k);
+        // dropout keep bits of this step's 64 query columns, before S^T arrives
+        uint32_t keep_a = 0u, keep_b = 0u;
+        if (kDrop) {
+          keep_a = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i * kTile + half * 64);
+          keep_b = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i * kTile + half * 64 + 32);
+        }
         if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1) || !w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
@@ -461,8 +504,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
         tc_fence_after();
         const uint32_t t_pt = tmem + lane_base + kColPT;
-        store_p32(sa, half * 64, t_pt);
-        store_p32(sb, half * 64 + 32, t_pt);
+        store_p32<kDrop>(sa, half * 64, t_pt, keep_a);
+        store_p32<kDrop>(sb, half * 64 + 32, t_pt, keep_b);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&s.bar_p_full);   // dV of this step may start
@@ -472,8 +515,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           break;
         }
         const uint32_t ds_row = smem_u32(s.dst[half]) + kr * 128;
-        ds_store32(sa, da, half * 64, half, kr, dsum_a, ds_row);
-        ds_store32(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row);
+        ds_store32<kDrop>(sa, da, half * 64, half, kr, dsum_a, ds_row, keep_a, pr.keep_scale);
+        ds_store32<kDrop>(sb, db, half * 64 + 32, half, kr, dsum_a, ds_row, keep_b, pr.keep_scale);
         fence_proxy_async_smem();
         warp_arrive(&s.bar_ds_full);  // dK, dQ of this step may start
       }
@@ -490,7 +533,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_after();
       }
       const uint32_t col = half == 0 ? kColDV : kColDK;
-      const float mul = half == 0 ? 1.f : pr.scale;
+      const float mul = half == 0 ? (kDrop ? pr.keep_scale : 1.f) : pr.scale;
       const int kb = v & 1;
       // the store of the item two back has read this staging buffer (implied
       // by done for items with steps; waited here for the others too)
@@ -791,8 +834,11 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (e != cudaSuccess) return e;
   const size_t smem = bwd_smem_bytes();
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(fa_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaFuncSetAttribute(fa_bwd_main_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_bwd_main_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -808,9 +854,12 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   const int n_items = a.pr.nt * a.pr.B * a.pr.H;
   const dim3 grid(n_items < num_sms ? n_items : num_sms);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
-  if ((e = launch_pdl(fa_bwd_main_kernel, grid, dim3(kMainThreads), smem, st, tq, tk, tv, tdo, tdk,
-                      tdv, tdq_acc, a)) != cudaSuccess)
-    return e;
+  e = a.pr.drop_p8 > 0
+          ? launch_pdl(fa_bwd_main_kernel<true>, grid, dim3(kMainThreads), smem, st, tq, tk, tv,
+                       tdo, tdk, tdv, tdq_acc, a)
+          : launch_pdl(fa_bwd_main_kernel<false>, grid, dim3(kMainThreads), smem, st, tq, tk, tv,
+                       tdo, tdk, tdv, tdq_acc, a);
+  if (e != cudaSuccess) return e;
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
   const int chunks = a.pr.N * (kHeadDim / 8);
   const dim3 dq_grid((chunks + 256 * kRowsPerThread - 1) / (256 * kRowsPerThread), a.pr.B * a.pr.H);

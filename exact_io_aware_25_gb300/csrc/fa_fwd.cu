@@ -87,13 +87,23 @@ __device__ __forceinline__ float exp2_poly(float x) {
   return __int_as_float(__float_as_int(q) + (ni << 23));
 }
 
+// Dropout state of one query row: hash key with the row pair folded in, the
+// bit offset of the row's two bytes in each block word, the threshold.
+struct RowDrop {
+  uint32_t key;    // head key ^ ((i >> 1) << 16)
+  uint32_t shift;  // 16 * (i & 1)
+  uint32_t p8;
+};
+
 // Exponentials of one 64-column half of a row: sv[c] <- 2^(sv[c]*sl2 - m),
-// accumulated into the eight partial sums and packed to bf16 pairs.  In every
-// group of eight columns the first kPoly use exp2_poly (FMA pipe), the rest
-// the MUFU unit, to balance the two pipes.
-template <int kPoly>
+// accumulated into the eight partial sums (before dropout) and packed to
+// bf16 pairs, with dropped elements packed as 0 when kDrop (jp0 = index of
+// the tile's first key pair).  In every group of eight columns the first
+// kPoly use exp2_poly (FMA pipe), the rest the MUFU unit.
+template <int kPoly, bool kDrop>
 __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
-                                         float (&rs8)[8], uint32_t (&pk)[32]) {
+                                         float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
+                                         uint32_t jp0) {
 #pragma unroll
   for (int c = half * 64; c < half * 64 + 64; c += 8) {
 #pragma unroll
@@ -103,7 +113,16 @@ __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2
       rs8[u] += sv[c + u];
     }
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) pk[((c - half * 64) + u) >> 1] = pack_bf16(sv[c + u], sv[c + u + 1]);
+    for (int u = 0; u < 8; u += 2) {
+      float a = sv[c + u], b = sv[c + u + 1];
+      if (kDrop) {
+        // keys c + u (even) and c + u + 1 share one block word
+        const uint32_t r = pcg_hash(rd.key ^ (jp0 + static_cast<uint32_t>((c + u) >> 1))) >> rd.shift;
+        a = (r & 0xffu) >= rd.p8 ? a : 0.f;
+        b = ((r >> 8) & 0xffu) >= rd.p8 ? b : 0.f;
+      }
+      pk[((c - half * 64) + u) >> 1] = pack_bf16(a, b);
+    }
   }
 }
 
@@ -114,6 +133,7 @@ constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 constexpr uint32_t kSoftmaxWarps = 4;
 
+template <bool kDrop>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -269,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float sl2 = pr.scale_log2;
     float m = -INFINITY;  // running max of S*scale*log2e
     float l = 0.f;        // running sum of 2^(S*scale*log2e - m)
+    RowDrop rd{0u, 0u, 0u};
+    if (kDrop) {
+      rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
+      rd.shift = 16u * static_cast<uint32_t>(qrow & 1);
+      rd.p8 = pr.drop_p8;
+    }
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int j = tile_at(s, sparse, it);
@@ -324,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
-        if (edge) exp_half<0>(sv, half, sl2, m_use, rs8, pk);  // exact zeros where masked
-        else exp_half<kPolyPer8>(sv, half, sl2, m_use, rs8, pk);
+        const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
+        if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);  // exact zeros where masked
+        else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
         if (half == 0 && it > 0) {
           if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
             ok = false;
@@ -376,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < kHeadDim; ++c) ov[c] = 0.f;
         }
-        const float inv = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const float inv = (n > 0 && l > 0.f) ? (kDrop ? pr.keep_scale : 1.f) / l : 0.f;
         const uint32_t q_base = smem_u32(s.q) + row * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
@@ -419,13 +446,18 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (e != cudaSuccess) return e;
   const size_t smem = fwd_smem_bytes();
   if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fa_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
-  return launch_pdl(fa_fwd_kernel, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
+  if (a.pr.drop_p8 > 0)
+    return launch_pdl(fa_fwd_kernel<true>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
+  return launch_pdl(fa_fwd_kernel<false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
 }
 
 }  // namespace fa

@@ -25,7 +25,27 @@ struct Problem {
   const int32_t *kv_len;  // device [B] or nullptr
   const uint8_t *block_mask;  // device [nt * nt] or nullptr
   WaitCtl wait;
+  // Dropout: element (i, j) of head bh is kept iff its hash byte >= drop_p8
+  // (0 = no dropout); kept values are scaled by keep_scale = 256 / (256 - drop_p8).
+  uint32_t drop_p8;
+  uint32_t seed_lo, seed_hi;
+  float keep_scale;
 };
+
+// The 32-bit PCG hash (Jarzynski and Olano, "Hash Functions for GPU
+// Rendering", JCGT 9(3), 2020): an LCG step followed by the RXS-M-XS output
+// permutation of the PCG generator.
+__device__ __forceinline__ uint32_t pcg_hash(uint32_t x) {
+  const uint32_t st = x * 747796405u + 2891336453u;
+  const uint32_t w = ((st >> ((st >> 28) + 4u)) ^ st) * 277803737u;
+  return (w >> 22) ^ w;
+}
+
+// Dropout key of head bh; the keep byte of element (i, j) is byte
+// 2 * (i & 1) + (j & 1) of pcg_hash(key ^ ((i >> 1) << 16 | (j >> 1))).
+__device__ __forceinline__ uint32_t drop_head_key(const Problem &pr, int bh) {
+  return pcg_hash(pcg_hash(pcg_hash(pr.seed_lo) ^ pr.seed_hi) ^ static_cast<uint32_t>(bh));
+}
 
 struct FwdArgs {
   Problem pr;

@@ -52,7 +52,7 @@ typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, non-finite or non-positive scale */
     FA_ERR_UNSUPPORTED = -2,  /* d != 64, N > 65535 * 128, N > 1024 * 128 with a block
-                                 mask, or no sm_103 device */
+                                 mask, N > 131072 with dropout, or no sm_103 device */
     FA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     FA_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed */
     FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait ran out (reported by fa_check) */
@@ -108,6 +108,43 @@ FA_API fa_status fa_bwd(const void *q, const void *k, const void *v, const void 
                  int B, int H, int N, int d, float scale, int causal,
                  const int32_t *kv_len, const uint8_t *block_mask,
                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Attention dropout fused into both passes ([EXPL] "Key ideas", kernel fusion:
+ * matmul, masking, softmax and dropout in one kernel).  With P the masked
+ * softmax of fa_fwd and Z a keep mask,
+ *     O = (P o Z / (1 - p')) V,      lse as in fa_fwd (from P, before dropout),
+ * and the backward is the gradient of that O for the same Z:
+ *     dV = (P o Z)^T dO / (1 - p'),  dP~ = dO V^T,  D = rowsum(dO o O),
+ *     dS = P o (Z o dP~ / (1 - p') - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ * Z is regenerated from (seed, b*H + h, i, j) in both passes, never stored:
+ *     pcg(x):  s = x * 747796405 + 2891336453;
+ *              w = ((s >> ((s >> 28) + 4)) ^ s) * 277803737;  return (w >> 22) ^ w
+ *              (the 32-bit "PCG hash", Jarzynski and Olano, "Hash Functions for
+ *              GPU Rendering", JCGT 9(3), 2020; all arithmetic mod 2^32)
+ *     kb    = pcg(pcg(pcg(seed_lo) ^ seed_hi) ^ (b*H + h))
+ *     r     = pcg(kb ^ ((i >> 1) << 16 | (j >> 1)))     (one word per 2x2 block)
+ *     u     = byte ((i & 1) * 2 + (j & 1)) of r (byte 0 = least significant)
+ *     Z_ij  = (u >= p8),  p8 = p * 256 rounded to nearest (ties to even), at most
+ *             255,  p' = p8 / 256.
+ *   p       in : drop probability in [0, 1); p8 = 0 gives exactly fa_fwd / fa_bwd.
+ *   seed    in : 64-bit seed (seed_lo = low 32 bits, seed_hi = high 32 bits).
+ * Other arguments, layouts and errors as fa_fwd / fa_bwd; FA_ERR_INVALID_ARG for
+ * p outside [0, 1) or non-finite, FA_ERR_UNSUPPORTED for p8 > 0 with
+ * N > 131072 (i >> 1 and j >> 1 must fit 16 bits).  fa_bwd_dropout must get the
+ * p, seed, masks and scale given to fa_fwd_dropout and its outputs.
+ */
+FA_API fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int H, int N, int d, float scale, int causal,
+                                const int32_t *kv_len, const uint8_t *block_mask, float p,
+                                unsigned long long seed, void *stream);
+
+FA_API fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                                const float *lse, const void *dout, void *dq, void *dk,
+                                void *dv, int B, int H, int N, int d, float scale, int causal,
+                                const int32_t *kv_len, const uint8_t *block_mask, float p,
+                                unsigned long long seed, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * fa_bwd without a workspace argument, for callers that cannot allocate

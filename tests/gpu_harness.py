@@ -107,3 +107,26 @@ def assert_grad(got, want, what):
     rf = rel_fro(got, want)
     assert rf <= TOL_GRAD_RELFRO, f"{what}: rel-fro {rf:.3e}"
     return rf
+
+
+def run_fwd_dropout(x: Inputs, p, seed):
+    shape = (x.B, x.H, x.N, x.d)
+    o = nan_like_bf16(shape)
+    lse = torch.full((x.B, x.H, x.N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    fa.fa_fwd_dropout(x.q, x.k, x.v, o, lse, x.B, x.H, x.N, x.d, x.scale, x.causal, x.kv_len,
+                      x.mask, p, seed, st)
+    fa.fa_check(st)
+    return o, lse
+
+
+def run_bwd_dropout(x: Inputs, o, lse, p, seed):
+    shape = (x.B, x.H, x.N, x.d)
+    dq, dk, dv = nan_like_bf16(shape), nan_like_bf16(shape), nan_like_bf16(shape)
+    nbytes = fa.fa_bwd_workspace_size(x.B, x.H, x.N, x.d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")  # garbage on entry
+    st = torch.cuda.current_stream()
+    fa.fa_bwd_dropout(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, x.B, x.H, x.N, x.d, x.scale,
+                      x.causal, x.kv_len, x.mask, p, seed, ws, nbytes, st)
+    fa.fa_check(st)
+    return dq, dk, dv

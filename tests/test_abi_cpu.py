@@ -110,3 +110,29 @@ def test_product_path_never_touches_the_oracle():
                     if re.search(r"\boracle\b|fa_oracle", text):
                         bad.append(os.path.join(dirpath, f))
     assert not bad, bad
+
+
+def _fwd_drop_status(fa, p, N=128, seed=1):
+    L = fa.lib()
+    return L.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, N, 64, 0.125, 0, None, None,
+                            p, seed, None)
+
+
+@pytest.mark.parametrize("p,N,status", [
+    (-0.1, 128, -1), (1.0, 128, -1), (1.5, 128, -1), (float("nan"), 128, -1),
+    (float("inf"), 128, -1), (0.1, 131072 + 1, -2), (0.0, 131072 + 1, -4),
+])
+def test_dropout_validation_without_gpu(fa_lib, p, N, status):
+    """Bad drop probabilities are rejected before anything else happens; a
+    positive one needs N <= 131072; p = 0 is plain attention at any N (here it
+    gets as far as the missing device)."""
+    got = _fwd_drop_status(fa_lib, p, N)
+    if status == -4:
+        assert got in (-2, -4)   # no GPU here: device setup fails
+    else:
+        assert got == status
+    L = fa_lib.lib()
+    need = fa_lib.fa_bwd_workspace_size(1, 1, 128, 64)
+    if status in (-1,):
+        assert L.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64,
+                                0.125, 0, None, None, p, 1, FAKE, need, None) == -1
