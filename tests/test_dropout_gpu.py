@@ -51,7 +51,10 @@ def test_dropout_tiny_full(H, oracle_mod, p, seed):
     _check(H, oracle_mod, H.Inputs(W.make("tiny", B=2, H=2)), p, seed)
 
 
-@pytest.mark.parametrize("N", [1, 127, 300])
+# N = 1 is left to the plain ragged test: with one key the exact dQ and dK are
+# 0 (dS = P (Z dP / (1-p') - D) with D = Z dP / (1-p')), so a relative norm
+# only measures the bf16 rounding of the stored O that D is computed from.
+@pytest.mark.parametrize("N", [2, 127, 300])
 @pytest.mark.parametrize("causal", [False, True])
 def test_dropout_ragged(H, oracle_mod, N, causal):
     import workloads as W
