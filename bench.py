@@ -232,7 +232,7 @@ def barrier(world: int, device=None):
 # ---------------------------------------------------------------- oracle timing
 
 
-def time_oracle(w, budget_s: float, max_units=None):
+def time_oracle(w, budget_s: float, max_units=None, dropout=0.0, seed=0):
     """Times the fp64 oracle (forward + backward) on whole (b, h) heads of the
     workload until budget_s has elapsed; returns (flops counted, seconds,
     heads, threads)."""
@@ -241,6 +241,7 @@ def time_oracle(w, budget_s: float, max_units=None):
     import workloads as W
     spec = w.spec
     threads = os.cpu_count() or 1
+    p8 = oracle.drop_p8(dropout) if dropout > 0 else 0
     q, k, v, do = (w.f64(n) for n in ("q", "k", "v", "do"))
     done_flops, elapsed, heads = 0.0, 0.0, 0
     order = [(b, h) for b in range(spec.B) for h in range(spec.H)]
@@ -251,10 +252,11 @@ def time_oracle(w, budget_s: float, max_units=None):
         kv = None if w.kv_len is None else w.kv_len[b:b + 1]
         qs, ks, vs, ds = (x[sl] for x in (q, k, v, do))
         t0 = time.perf_counter()
+        # (the single head keeps its own index 0 for the keep mask: timing only)
         oracle.forward(qs, ks, vs, spec.scale, causal=spec.causal, kv_len=kv,
-                       block_mask=w.block_mask, nthreads=threads)
+                       block_mask=w.block_mask, nthreads=threads, p8=p8, seed=seed)
         oracle.backward(qs, ks, vs, ds, spec.scale, causal=spec.causal, kv_len=kv,
-                        block_mask=w.block_mask, nthreads=threads)
+                        block_mask=w.block_mask, nthreads=threads, p8=p8, seed=seed)
         elapsed += time.perf_counter() - t0
         one = W.Spec(**{**spec.__dict__, "B": 1, "H": 1})
         done_flops += counted_flops(one, kv, w.block_mask)["step"]
@@ -273,14 +275,15 @@ def run_reference(args, rank, world):
     import workloads as W
     w = W.make(args.workload)
     # calibrate one head, then size each step to keep the whole run to ~2 minutes
-    f1, t1, _, threads = time_oracle(w, 0.0, max_units=1)
+    f1, t1, _, threads = time_oracle(w, 0.0, max_units=1, dropout=args.dropout, seed=args.seed)
     per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
     heads_per_step = max(1, min(w.spec.B * w.spec.H, int(per_step_budget / max(t1, 1e-6))))
     for _ in range(args.warmup):
-        time_oracle(w, 0.0, max_units=heads_per_step)
+        time_oracle(w, 0.0, max_units=heads_per_step, dropout=args.dropout, seed=args.seed)
     tot_f, tot_t = 0.0, 0.0
     for _ in range(args.steps):
-        f, t, _, _ = time_oracle(w, float("inf"), max_units=heads_per_step)
+        f, t, _, _ = time_oracle(w, float("inf"), max_units=heads_per_step,
+                                 dropout=args.dropout, seed=args.seed)
         tot_f += f
         tot_t += t
     value = tot_f / tot_t / 1e12
@@ -291,7 +294,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.dropout, args.seed),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -309,7 +312,7 @@ WORKLOAD_NAMES = {
 }
 
 
-def workload_config(w):
+def workload_config(w, dropout=0.0, seed=0):
     s = w.spec
     cfg = {"workload": WORKLOAD_NAMES.get(s.name, s.name),
            "B": s.B, "H": s.H, "N": s.N, "d": s.d, "causal": s.causal, "scale": s.scale,
@@ -323,6 +326,9 @@ def workload_config(w):
     if w.block_mask is not None:
         cfg["block_mask"] = (f"{w.block_mask.shape[0]}x{w.block_mask.shape[1]} of 128x128 blocks, "
                              f"{int(w.block_mask.sum())} nonzero")
+    if dropout > 0:
+        cfg["dropout"] = {"p": dropout, "seed": seed,
+                          "mask": "counter-based hash per 2x2 block, regenerated in both passes"}
     return cfg
 
 
@@ -355,10 +361,26 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
+    p_drop, seed = args.dropout, args.seed
+
+    def fwd_call():
+        if p_drop > 0:
+            fa.fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask,
+                              p_drop, seed, stream)
+        else:
+            fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
+
+    def bwd_call():
+        if p_drop > 0:
+            fa.fa_bwd_dropout(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal,
+                              kv_len, mask, p_drop, seed, ws, ws_bytes, stream)
+        else:
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len,
+                      mask, ws, ws_bytes, stream)
+
     def step():
-        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, mask,
-                  ws, ws_bytes, stream)
+        fwd_call()
+        bwd_call()
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -380,11 +402,10 @@ def run_ours(args, rank, world, local):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev_step0[i].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
+        fwd_call()
         ev_fwd1[i].record(stream)
         fa.fa_set_bwd_main_events(bm0[i], bm1[i])
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, s.scale, s.causal, kv_len, mask,
-                  ws, ws_bytes, stream)
+        bwd_call()
         ev_step1[i].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - wall0
@@ -409,7 +430,8 @@ def run_ours(args, rank, world, local):
     dom_t = bwd_avg if dominant == "fa_bwd_main_kernel" else fwd_avg
     achieved = dom_flops / dom_t / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic(dominant, args.workload),
+                "frac": achieved / peak,
+                "traffic": load_traffic(dominant, args.workload) if p_drop == 0 else None,
                 "kernel": dominant, "peak_source": f"bf16_tflops (burst) of {peak_src}",
                 "algorithmic_flops_per_launch": dom_flops,
                 "avg_launch_ms": dom_t * 1e3}
@@ -461,7 +483,7 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, t, heads, threads = time_oracle(w, args.cpu_budget)
+        f, t, heads, threads = time_oracle(w, args.cpu_budget, dropout=p_drop, seed=seed)
         cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{heads} of {B * H} (b, h) heads, forward + backward, full rows; "
                          f"{t:.1f} s of fp64 C oracle work",
@@ -472,7 +494,7 @@ def run_ours(args, rank, world, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_job / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, p_drop, seed),
             "pct_of_peak": value / peak,
             "fwd": {"tflops": fl["fwd"] / fwd_avg / 1e12, "ms": fwd_avg * 1e3},
             "bwd_main": {"tflops": fl["bwd"] / bwd_avg / 1e12, "ms": bwd_avg * 1e3},
@@ -499,6 +521,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="drop probability of the fused dropout (0 = plain attention)")
+    ap.add_argument("--seed", type=int, default=1234, help="dropout seed")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if world > 1:
