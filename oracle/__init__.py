@@ -91,6 +91,9 @@ def _load():
                                                   u8p, ci, ci, u64, i64p, cl, i64p, cl, dp, dp,
                                                   dp, ci]
             lib.fa_oracle_bwd_dropout.restype = ci
+            lib.fa_oracle_fwd_qk.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, i32p, i64p, cl,
+                                             dp, dp, ci]
+            lib.fa_oracle_fwd_qk.restype = ci
             lib.fa_oracle_keep.argtypes = [u64, ci, ci, ci, ci]
             lib.fa_oracle_keep.restype = ci
             _lib = lib
@@ -171,6 +174,30 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=Non
         raise RuntimeError(f"fa_oracle_fwd failed ({rc})")
     if rows is None:
         return o.reshape(B, H, N, d), lse.reshape(B, H, N)
+    return o, lse
+
+
+def forward_qk(q, k, v, scale, kv_len=None, rows=None, nthreads=None):
+    """Forward with Nq query rows and Nk key rows (q [B, H, Nq, d]; k, v
+    [B, H, Nk, d]; no causal, no block mask).  Returns (o, lse) like forward,
+    row ids bh * Nq + i."""
+    lib = _load()
+    B, H, Nq, d = _shape(q)
+    Nk = _shape(k)[2]
+    qa, qp = _f64(q)
+    ka, kp = _f64(k)
+    va, vp = _f64(v)
+    kl, klp = _opt_i32(kv_len)
+    ra, rp = _opt_i64(rows)
+    nrows = B * H * Nq if rows is None else len(ra)
+    o = np.zeros((nrows, d), np.float64)
+    lse = np.zeros((nrows,), np.float64)
+    rc = lib.fa_oracle_fwd_qk(qp, kp, vp, B, H, Nq, Nk, d, float(scale), klp, rp, nrows,
+                              _f64(o)[1], _f64(lse)[1], _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"fa_oracle_fwd_qk failed ({rc})")
+    if rows is None:
+        return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
     return o, lse
 
 

@@ -46,7 +46,9 @@
  * split independent rows only; each row's arithmetic is sequential.
  *
  * Layout: Q, K, V, dO, O, dQ, dK, dV are [B, H, N, d] row-major doubles;
- * lse is [B, H, N].  kv_len is int32[B] (NULL = N; values clamped to
+ * lse is [B, H, N].  fa_oracle_fwd_qk allows a query length Nq different
+ * from the key length Nk (Q, O [B, H, Nq, d]; K, V [B, H, Nk, d]; no causal
+ * or block mask there): the same definition, row by row.  kv_len is int32[B] (NULL = N; values clamped to
  * [0, N]); block_mask is uint8[nb * nb], nb = ceil(N / blk), one mask shared
  * by every (b, h) (NULL = all ones).
  */
@@ -59,6 +61,7 @@
 typedef struct {
     const double *q, *k, *v, *dout;
     int B, H, N, d;
+    int Nk;             /* key rows (= N except in fa_oracle_fwd_qk) */
     double scale;
     int causal;
     const int32_t *kv_len;
@@ -75,6 +78,7 @@ static void problem_init(problem *p, const double *q, const double *k, const dou
                          int blk) {
     p->q = q; p->k = k; p->v = v; p->dout = dout;
     p->B = B; p->H = H; p->N = N; p->d = d;
+    p->Nk = N;
     p->scale = scale; p->causal = causal;
     p->kv_len = kv_len; p->block_mask = block_mask;
     p->blk = blk > 0 ? blk : 128;
@@ -118,12 +122,12 @@ static double drop_factor(const problem *p, int bh, int i, int j) {
     return keep(p->seed, p->p8, bh, i, j) ? p->keep_scale : 0.0;
 }
 
-/* Key bound of batch b: kv_len[b] clamped to [0, N]. */
+/* Key bound of batch b: kv_len[b] clamped to [0, Nk]. */
 static int key_bound(const problem *p, int b) {
-    if (!p->kv_len) return p->N;
+    if (!p->kv_len) return p->Nk;
     int L = p->kv_len[b];
     if (L < 0) L = 0;
-    if (L > p->N) L = p->N;
+    if (L > p->Nk) L = p->Nk;
     return L;
 }
 
@@ -138,6 +142,11 @@ static int allowed(const problem *p, int b, int i, int j) {
 
 static const double *row_of(const double *t, const problem *p, int bh, int i) {
     return t + ((size_t)bh * p->N + (size_t)i) * p->d;
+}
+
+/* Row j of K or V (Nk rows per head). */
+static const double *key_row(const double *t, const problem *p, int bh, int j) {
+    return t + ((size_t)bh * p->Nk + (size_t)j) * p->d;
 }
 
 static double dot(const double *a, const double *b, int d) {
@@ -158,9 +167,9 @@ static int forward_row(const problem *p, int bh, int i, double *s, double *m_out
     int count = 0;
     double m = -INFINITY;
     /* 1. scores on the allowed set */
-    for (int j = 0; j < p->N; ++j) {
+    for (int j = 0; j < p->Nk; ++j) {
         if (!allowed(p, b, i, j)) continue;
-        s[j] = p->scale * dot(qi, row_of(p->k, p, bh, j), d);
+        s[j] = p->scale * dot(qi, key_row(p->k, p, bh, j), d);
         if (s[j] > m) m = s[j];
         ++count;
     }
@@ -171,13 +180,13 @@ static int forward_row(const problem *p, int bh, int i, double *s, double *m_out
     }
     /* 2.-3. max-shifted exponential sum */
     double l = 0.0;
-    for (int j = 0; j < p->N; ++j)
+    for (int j = 0; j < p->Nk; ++j)
         if (allowed(p, b, i, j)) l += exp(s[j] - m);
     /* 4.-5. normalised probabilities (dropped out and rescaled) times V */
-    for (int j = 0; j < p->N; ++j) {
+    for (int j = 0; j < p->Nk; ++j) {
         if (!allowed(p, b, i, j)) continue;
         const double pij = exp(s[j] - m) / l * drop_factor(p, bh, i, j);
-        const double *vj = row_of(p->v, p, bh, j);
+        const double *vj = key_row(p->v, p, bh, j);
         for (int c = 0; c < d; ++c) o[c] += pij * vj[c];
     }
     *m_out = m; *l_out = l;
@@ -290,6 +299,26 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v, int B, int 
                   double *o, double *lse, int nthreads) {
     return fa_oracle_fwd_dropout(q, k, v, B, H, N, d, scale, causal, kv_len, block_mask, blk, 0,
                                  0, rows, nrows, o, lse, nthreads);
+}
+
+/*
+ * Forward with a query length Nq and a key length Nk (no causal, no block
+ * mask; kv_len clamped to [0, Nk]): q [B, H, Nq, d], k and v [B, H, Nk, d];
+ * rows as in fa_oracle_fwd with ids bh * Nq + i; o [nrows, d], lse [nrows].
+ */
+int fa_oracle_fwd_qk(const double *q, const double *k, const double *v, int B, int H, int Nq,
+                     int Nk, int d, double scale, const int32_t *kv_len, const int64_t *rows,
+                     int64_t nrows, double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+    problem p;
+    problem_init(&p, q, k, v, NULL, B, H, Nq, d, scale, 0, kv_len, NULL, 128);
+    p.Nk = Nk;
+    const int64_t total = (int64_t)B * H * Nq;
+    if (!rows) nrows = total;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= total) return -1;
+    fwd_ctx cx = {&p, rows, o, lse};
+    return parallel_for(nrows, nthreads, (size_t)Nk, fwd_item, &cx);
 }
 
 /* The dropout keep mask Z_ij (1 kept, 0 dropped) of head bh. */

@@ -471,3 +471,42 @@ def test_dropout_threshold_rounding(oracle_mod):
     assert oracle_mod.drop_p8(0.9999) == 255      # 255.97 rounds to 256, capped
     assert oracle_mod.drop_p8(1.5 / 256) == 2     # tie 1.5 -> even
     assert oracle_mod.drop_p8(2.5 / 256) == 2     # tie 2.5 -> even
+
+
+# ---------------------------------------------------------------- Nq != Nk (split-KV forward)
+
+
+def test_short_queries_equal_the_same_rows_of_a_square_problem(oracle_mod):
+    """Query rows are independent: the rows of a short Q against Nk keys equal
+    the same rows of the square problem whose Q is extended to Nk rows."""
+    rng = np.random.default_rng(40)
+    B, H, Nq, Nk, d, scale = 2, 3, 5, 37, 6, 0.6
+    q = _rand(rng, B, H, Nq, d)
+    k, vv = _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d)
+    kv_len = np.array([37, 11], np.int32)
+    o, lse = oracle_mod.forward_qk(q, k, vv, scale, kv_len=kv_len)
+    q_sq = np.concatenate([q, _rand(rng, B, H, Nk - Nq, d)], axis=2)
+    o_sq, lse_sq = oracle_mod.forward(q_sq, k, vv, scale, kv_len=kv_len)
+    np.testing.assert_array_equal(o, o_sq[:, :, :Nq])
+    np.testing.assert_array_equal(lse, lse_sq[:, :, :Nq])
+
+
+def test_short_queries_special_cases(oracle_mod):
+    rng = np.random.default_rng(41)
+    B, H, Nq, Nk, d = 1, 2, 3, 50, 4
+    q = _rand(rng, B, H, Nq, d)
+    k = _rand(rng, B, H, Nk, d)
+    c = np.array([0.5, -1.0, 2.0, 0.25])
+    o, lse = oracle_mod.forward_qk(q, k, np.broadcast_to(c, (B, H, Nk, d)), 0.3)
+    np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=0, atol=1e-14)
+    # one key: the output is its value and lse its score
+    vv = _rand(rng, B, H, Nk, d)
+    o1, l1 = oracle_mod.forward_qk(q, k, vv, 0.3, kv_len=np.array([1], np.int32))
+    np.testing.assert_allclose(o1, np.broadcast_to(vv[:, :, :1], o1.shape), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(l1, 0.3 * np.einsum("bhic,bhc->bhi", q, k[:, :, 0]), rtol=0,
+                               atol=1e-13)
+    # zero queries: the mean of the values and lse = ln Nk
+    o0, l0 = oracle_mod.forward_qk(np.zeros_like(q), k, vv, 0.3)
+    np.testing.assert_allclose(o0, np.broadcast_to(vv.mean(axis=2, keepdims=True), o0.shape),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l0, np.log(Nk), rtol=0, atol=1e-13)
