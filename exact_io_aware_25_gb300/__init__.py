@@ -71,6 +71,11 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                          ci, vp, vp, cf, u64, vp, sz, vp]
             L.fa_bwd_dropout.restype = ci
+            L.fa_fwd_splitkv_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+            L.fa_fwd_splitkv_workspace_size.restype = sz
+            L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ci, vp,
+                                         sz, vp]
+            L.fa_fwd_splitkv.restype = ci
             L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                          ci, vp, vp, vp]
             L.fa_bwd_noalloc.restype = ci
@@ -159,6 +164,23 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=
                                 float(scale), int(bool(causal)), _ptr(kv_len), _ptr(block_mask),
                                 float(p), int(seed) & (2**64 - 1), _ptr(workspace),
                                 int(workspace_bytes), _stream(stream)), "fa_bwd_dropout")
+
+
+def fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_size(int(B), int(H), int(Nq), int(Nk), int(d),
+                                                    int(num_splits)))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, kv_len=None, num_splits=0,
+                   workspace=None, workspace_bytes=0, stream=None) -> None:
+    """Forward of Nq query rows against Nk key rows with the key range split
+    across CTAs and merged (see include/fa.h)."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                int(Nq), int(Nk), int(d), float(scale), _ptr(kv_len),
+                                int(num_splits), _ptr(workspace), int(workspace_bytes),
+                                _stream(stream)), "fa_fwd_splitkv")
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0,

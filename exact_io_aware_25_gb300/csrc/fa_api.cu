@@ -131,6 +131,7 @@ Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t
   p.B = B;
   p.H = H;
   p.N = N;
+  p.Nk = N;
   p.nt = (N + kTile - 1) / kTile;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -172,6 +173,47 @@ WsLayout ws_layout(int B, int H, int N) {
   w.sched = align_up(w.col_idx + nl * nl * sizeof(int16_t), 256);
   w.total = align_up(w.sched + sizeof(int), 256);
   return w;
+}
+
+// Split-KV forward: the number of key-range splits (0 = choose) and the
+// scratch it needs.
+int splitkv_splits(int B, int H, int Nq, int Nk, int num_splits) {
+  const int nq_tiles = (Nq + kTile - 1) / kTile, nk_tiles = (Nk + kTile - 1) / kTile;
+  int s = num_splits;
+  if (s <= 0) {
+    // about two CTAs per SM of a 152-SM GB300, at most one split per key tile
+    const long long units = static_cast<long long>(B) * H * nq_tiles;
+    s = static_cast<int>((2LL * 152 + units - 1) / units);
+    if (s > 256) s = 256;
+  }
+  if (s > nk_tiles) s = nk_tiles;
+  return s < 1 ? 1 : s;
+}
+
+struct SplitWs {
+  size_t part_o, part_lse, total;
+  int nq_pad;
+};
+
+SplitWs splitkv_ws(int B, int H, int Nq, int S) {
+  SplitWs w{};
+  w.nq_pad = static_cast<int>(align_up(static_cast<size_t>(Nq), kTile));
+  const size_t rows = static_cast<size_t>(S) * B * H * w.nq_pad;
+  w.part_o = 0;
+  w.part_lse = align_up(rows * kHeadDim * sizeof(float), 256);
+  w.total = align_up(w.part_lse + rows * sizeof(float), 256);
+  return w;
+}
+
+fa_status validate_splitkv(int B, int H, int Nq, int Nk, int d, float scale, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh >= 65536 || bh * Nq >= (1LL << 31) || bh * Nk >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  if ((Nq + kTile - 1) / kTile > kMaxGridTiles) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
 }
 
 }  // namespace
@@ -276,6 +318,44 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
   return launch_bwd(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a, static_cast<cudaStream_t>(stream), ev0,
                     ev1) ==
                  cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (validate_splitkv(B, H, Nq, Nk, d, 1.f, num_splits) != FA_OK) return 0;
+  return splitkv_ws(B, H, Nq, splitkv_splits(B, H, Nq, Nk, num_splits)).total;
+}
+
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int H, int Nq, int Nk, int d, float scale, const int32_t *kv_len,
+                         int num_splits, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = validate_splitkv(B, H, Nq, Nk, d, scale, num_splits);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  const int S = splitkv_splits(B, H, Nq, Nk, num_splits);
+  const SplitWs wl = splitkv_ws(B, H, Nq, S);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
+  int dev = 0;
+  int *err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bhnd(&tq, q, BH, Nq) || !encode_bhnd(&tk, k, BH, Nk) || !encode_bhnd(&tv, v, BH, Nk))
+    return FA_ERR_CUDA;
+  FwdArgs a{};
+  a.pr = make_problem(B, H, Nq, scale, 0, kv_len, nullptr, err);
+  a.pr.Nk = Nk;
+  a.lse = lse;
+  a.n_split = S;
+  a.nq_pad = wl.nq_pad;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.part_o = reinterpret_cast<float *>(ws + wl.part_o);
+  a.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
+  a.o = static_cast<uint16_t *>(o);
+  return launch_fwd_splitkv(tq, tk, tv, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;
 }

@@ -54,6 +54,7 @@ struct __align__(1024) FwdSmem {
   uint32_t tmem_base;
   int abort;
   int n_tiles;
+  int tile0;              // first key tile (the split's range start; 0 otherwise)
   int16_t tiles[kMaxMaskTiles];
 };
 
@@ -61,7 +62,7 @@ struct __align__(1024) FwdSmem {
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192, kTmemCols = 256;
 
 __device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
-  return sparse ? static_cast<int>(s.tiles[it]) : it;
+  return sparse ? static_cast<int>(s.tiles[it]) : s.tile0 + it;
 }
 
 // The running reference max of a row is only moved when the row max exceeds
@@ -152,7 +153,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = bh / pr.H;
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
-  const int j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
+  int j_begin = 0, j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
+  if (args.n_split > 0) {
+    // split-KV (no causal, no block mask): this CTA's contiguous range of key tiles
+    const int per = (n_kv + args.n_split - 1) / args.n_split;
+    j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
+    j_end = min(n_kv, j_begin + per);
+  }
   const bool sparse = pr.block_mask != nullptr;
 
   if (tid == 0) {
@@ -195,9 +202,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         count += __popc(bal);
       }
     } else {
-      count = j_end;
+      count = j_end - j_begin;
     }
-    if (lane == 0) s.n_tiles = count;
+    if (lane == 0) {
+      s.n_tiles = count;
+      s.tile0 = j_begin;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -404,23 +414,35 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int c = 0; c < kHeadDim; ++c) ov[c] = 0.f;
         }
         const float inv = (n > 0 && l > 0.f) ? (kDrop ? pr.keep_scale : 1.f) / l : 0.f;
-        const uint32_t q_base = smem_u32(s.q) + row * 128;
+        const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (args.n_split > 0) {
+          // split-KV partial: O_s = O / l_s (fp32) and lse_s of this row, for the merge
+          if (qrow < pr.N) {
+            const size_t prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
+                                    static_cast<size_t>(args.nq_pad) + qrow;
+            float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kHeadDim);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const float *x = ov + ch * 8;
-          st_shared_v4(q_base + ((ch ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
-                       pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
-                       pack_bf16(x[6] * inv, x[7] * inv));
+            for (int c4 = 0; c4 < kHeadDim / 4; ++c4)
+              dst[c4] = make_float4(ov[4 * c4] * inv, ov[4 * c4 + 1] * inv, ov[4 * c4 + 2] * inv,
+                                    ov[4 * c4 + 3] * inv);
+            args.part_lse[prow] = lse;
+          }
+        } else {
+          const uint32_t q_base = smem_u32(s.q) + row * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const float *x = ov + ch * 8;
+            st_shared_v4(q_base + ((ch ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                         pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                         pack_bf16(x[6] * inv, x[7] * inv));
+          }
+          if (qrow < pr.N) args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
+          fence_proxy_async_smem();
         }
-        if (qrow < pr.N) {
-          const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-          args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
-        }
-        fence_proxy_async_smem();
       }
     }
     named_bar_sync(1, 128);
-    if (tid == 0 && ok && !s.abort) {
+    if (tid == 0 && ok && !s.abort && args.n_split == 0) {
       tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
       bulk_commit();
       bulk_wait_all();
@@ -434,30 +456,100 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// Split-KV merge ([MATH] §4: the softmax-weighted sum over the keys splits
+// into independent ranges whose (max, sum, output) states combine by
+// rescaling).  Each split s left O_s = (sum over its keys of P~ V) / l_s and
+// lse_s = m_s + ln l_s; then lse = ln sum_s e^{lse_s} and
+// O = sum_s e^{lse_s - lse} O_s.  8 threads per query row, 8 columns each.
+__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const FwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int bh = blockIdx.y;
+  const int row = blockIdx.x * 32 + static_cast<int>(threadIdx.x >> 3);
+  const int sub = threadIdx.x & 7;
+  if (row >= a.pr.N) return;
+  const int S = a.n_split, BH = a.pr.B * a.pr.H;
+  const size_t stride = static_cast<size_t>(BH) * a.nq_pad;   // between splits
+  const size_t base = static_cast<size_t>(bh) * a.nq_pad + row;
+  float mx = -INFINITY;
+  for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, a.part_lse[base + sp * stride]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float den = 0.f;
+  if (mx != -INFINITY) {
+    for (int sp = 0; sp < S; ++sp) {
+      const float ls = a.part_lse[base + sp * stride];
+      if (ls == -INFINITY) continue;
+      const float w = __expf(ls - mx);
+      den += w;
+      const float4 *src =
+          reinterpret_cast<const float4 *>(a.part_o + (base + sp * stride) * kHeadDim + sub * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      acc[0] = fmaf(w, x0.x, acc[0]);
+      acc[1] = fmaf(w, x0.y, acc[1]);
+      acc[2] = fmaf(w, x0.z, acc[2]);
+      acc[3] = fmaf(w, x0.w, acc[3]);
+      acc[4] = fmaf(w, x1.x, acc[4]);
+      acc[5] = fmaf(w, x1.y, acc[5]);
+      acc[6] = fmaf(w, x1.z, acc[6]);
+      acc[7] = fmaf(w, x1.w, acc[7]);
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint4 out;
+  out.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  out.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  out.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  out.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  const size_t orow = static_cast<size_t>(bh) * a.pr.N + row;
+  *reinterpret_cast<uint4 *>(a.o + orow * kHeadDim + sub * 8) = out;
+  if (sub == 0) a.lse[orow] = den > 0.f ? mx + __logf(den) : -INFINITY;
+}
+
 }  // namespace
 
 size_t fwd_smem_bytes() { return sizeof(FwdSmem) + 1024; }
 
-cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st) {
+// Opts both forward instantiations into their dynamic shared memory (once per device).
+cudaError_t launch_fwd_config() {
   static int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const size_t smem = fwd_smem_bytes();
   if (configured_dev != dev) {
+    const int smem = static_cast<int>(fwd_smem_bytes());
     e = cudaFuncSetAttribute(fa_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+                             smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fa_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+                               smem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st) {
+  cudaError_t e = launch_fwd_config();
+  if (e != cudaSuccess) return e;
+  const size_t smem = fwd_smem_bytes();
   dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
   if (a.pr.drop_p8 > 0)
     return launch_pdl(fa_fwd_kernel<true>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
   return launch_pdl(fa_fwd_kernel<false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
+}
+
+cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st) {
+  cudaError_t e = launch_fwd_config();
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt, a.n_split);
+  // the O tensor map is not used in split mode (the merge kernel writes O)
+  e = launch_pdl(fa_fwd_kernel<false>, grid, dim3(kThreads), fwd_smem_bytes(), st, tq, tk, tv, tq,
+                 a);
+  if (e != cudaSuccess) return e;
+  const dim3 mgrid((a.pr.N + 31) / 32, a.pr.B * a.pr.H);
+  return launch_pdl(fa_fwd_merge_kernel, mgrid, dim3(256), 0, st, a);
 }
 
 }  // namespace fa

@@ -17,8 +17,9 @@ constexpr int kMaxMaskTiles = 1024;  // block-sparse: at most 1024 tiles per row
 constexpr int kMaxGridTiles = 65535;
 
 struct Problem {
-  int B, H, N;
-  int nt;                 // ceil(N / 128) tiles per head
+  int B, H, N;            // N: query rows (and key rows, except in the split-KV forward)
+  int Nk;                 // key rows
+  int nt;                 // ceil(N / 128) query tiles per head
   float scale;            // S = scale * Q K^T
   float scale_log2;       // scale * log2(e)
   int causal;
@@ -51,6 +52,14 @@ struct FwdArgs {
   Problem pr;
   float *lse;             // [B, H, N]
   int starve;             // test hook: producer issues no K/V loads
+  // Split-KV: n_split > 0 splits each row's key tiles into n_split contiguous
+  // ranges (blockIdx.z); each CTA writes its normalised partial O and its lse
+  // to the workspace instead of O and lse, and a merge kernel combines them.
+  int n_split;
+  int nq_pad;             // query rows per head in the partial arrays (N rounded up to 128)
+  float *part_o;          // [n_split, B*H, nq_pad, 64] fp32
+  float *part_lse;        // [n_split, B*H, nq_pad] fp32, natural log
+  uint16_t *o;            // [B, H, N, 64] bf16, written by the merge kernel
 };
 
 struct BwdArgs {
@@ -68,11 +77,11 @@ struct BwdArgs {
   uint16_t *dq;           // [B, H, N, 64] bf16
 };
 
-// Key bound of batch b: kv_len[b] clamped to [0, N].
+// Key bound of batch b: kv_len[b] clamped to [0, Nk].
 __device__ __forceinline__ int key_bound(const Problem &p, int b) {
-  if (!p.kv_len) return p.N;
+  if (!p.kv_len) return p.Nk;
   int L = __ldg(p.kv_len + b);
-  return L < 0 ? 0 : (L > p.N ? p.N : L);
+  return L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
 }
 
 // Programmatic dependent launch: a kernel of this library may begin launching
@@ -107,6 +116,8 @@ size_t bwd_smem_bytes();
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
+cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st);
 
 // ev_start / ev_stop (may be null) are recorded around the main kernel.
 // tdq_acc: the fp32 dQ accumulators [B*H*n_pad, 64] as a 2-D map with 128 x 32

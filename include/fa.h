@@ -147,6 +147,35 @@ FA_API fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, con
                                 size_t workspace_bytes, void *stream);
 
 /*
+ * Split-KV forward for a short query block against a long key/value cache
+ * (decoding).  The key tiles of every row are cut into num_splits contiguous
+ * ranges processed by separate CTAs; each range leaves its own normalised
+ * partial output O_s and lse_s (the online-softmax state of [EXPL] "Method",
+ * steps 2-4, over that range), and a merge kernel combines them exactly:
+ *     lse = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s
+ * ([MATH] section 4: the softmax-weighted sum splits into independent key
+ * ranges whose states combine by rescaling).  The result is the fa_fwd
+ * result with Nq query rows and Nk key rows, no causal mask and no block
+ * mask (kv_len as in fa_fwd, clamped to [0, Nk]).
+ *   q              in : bf16 [B, H, Nq, d]
+ *   k, v           in : bf16 [B, H, Nk, d]
+ *   o              out: bf16 [B, H, Nq, d]
+ *   lse            out: fp32 [B, H, Nq]
+ *   num_splits     in : 0 = about two CTAs per SM of a 152-SM GB300, else the
+ *                       count (at most 1024); capped at ceil(Nk / 128)
+ *   workspace      in : device scratch of >= fa_fwd_splitkv_workspace_size()
+ *                       bytes (same num_splits), 16-byte aligned, caller-owned:
+ *                       fp32 partial outputs and lse, S * B * H * ceil(Nq/128)
+ *                       * 128 * 260 bytes.
+ */
+FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+FA_API fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int H, int Nq, int Nk, int d, float scale,
+                                const int32_t *kv_len, int num_splits, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory when they run the backward pass (for instance a plugin whose
  * host application owns every device allocation, or a latency-critical loop

@@ -136,3 +136,39 @@ def test_dropout_validation_without_gpu(fa_lib, p, N, status):
     if status in (-1,):
         assert L.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64,
                                 0.125, 0, None, None, p, 1, FAKE, need, None) == -1
+
+
+def test_splitkv_workspace_and_validation_without_gpu(fa_lib):
+    """Workspace: S * B * H * Nq_pad rows of 64 fp32 partial outputs plus one
+    fp32 lse each (each part 256-byte aligned), S chosen as documented."""
+    up = lambda x: -(-x // 256) * 256
+    for B, H, Nq, Nk, S in [(1, 1, 1, 1000, 3), (2, 8, 16, 32768, 0), (4, 2, 300, 129, 5)]:
+        nq_pad = -(-Nq // 128) * 128
+        nk_t = -(-Nk // 128)
+        if S == 0:
+            units = B * H * (nq_pad // 128)
+            S_eff = min(-(-304 // units), 256)
+        else:
+            S_eff = S
+        S_eff = max(1, min(S_eff, nk_t))
+        rows = S_eff * B * H * nq_pad
+        want = up(up(rows * 64 * 4) + rows * 4)
+        assert fa_lib.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, 64, S) == want, (B, H, Nq, Nk, S)
+    assert fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 128, 0) == 0
+    assert fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 64, 2000) == 0
+    L = fa_lib.lib()
+    need = fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 256, 64, 0)
+
+    def call(**kw):
+        a = dict(q=FAKE, o=FAKE, Nq=1, Nk=256, d=64, scale=0.125, S=0, ws=FAKE, nbytes=need)
+        a.update(kw)
+        return L.fa_fwd_splitkv(a["q"], FAKE, FAKE, a["o"], FAKE, 1, 1, a["Nq"], a["Nk"], a["d"],
+                                a["scale"], None, a["S"], a["ws"], a["nbytes"], None)
+
+    assert call(q=None) == -1
+    assert call(Nq=0) == -1 and call(Nk=0) == -1
+    assert call(scale=-1.0) == -1
+    assert call(S=-1) == -1 and call(S=1025) == -1
+    assert call(d=128) == -2
+    assert call(o=FAKE + 8) == -3
+    assert call(ws=None) == -6 and call(nbytes=need - 1) == -6
