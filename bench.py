@@ -510,6 +510,152 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+# ---------------------------------------------------------------- split-KV decode
+
+DECODE = {"B": 16, "H": 16, "Nq": 1, "Nk": 32768, "d": 64, "scale": 0.125, "seed": 6}
+
+
+def decode_inputs():
+    """Decode-shaped inputs: one query per (b, h) against a 32K-key cache;
+    Q, K, V iid N(0, 1) in fp32 (numpy PCG64, draw order Q, K, V), rounded
+    to bf16 (RNE)."""
+    import numpy as np
+    import workloads as W
+    c = DECODE
+    rng = np.random.default_rng(c["seed"])
+    q = W.f32_to_bf16_bits(rng.standard_normal((c["B"], c["H"], c["Nq"], c["d"]), dtype=np.float32))
+    k = W.f32_to_bf16_bits(rng.standard_normal((c["B"], c["H"], c["Nk"], c["d"]), dtype=np.float32))
+    v = W.f32_to_bf16_bits(rng.standard_normal((c["B"], c["H"], c["Nk"], c["d"]), dtype=np.float32))
+    return q, k, v
+
+
+def run_decode(args, rank, world, local):
+    """Split-KV forward on the decode workload: TFLOP/s of 4*Nq*Nk*d per head
+    and the K/V read bandwidth against the measured HBM copy peak."""
+    import numpy as np
+    import torch
+
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+
+    fa.lib()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    c = DECODE
+    B, H, Nq, Nk, d, scale = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["scale"]
+    hq, hk, hv = decode_inputs()
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+
+    q, k, v = dev(hq), dev(hk), dev(hv)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+    nbytes = fa.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, None, 0, ws, nbytes, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    fa.fa_check(stream)
+    K = args.steps
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        step()
+        e1[i].record(stream)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    fa.fa_check(stream)
+    t_rank = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / 1e3
+    t_job = max_over_ranks(t_rank, world, device)
+    flops = 4.0 * Nq * Nk * d * B * H
+    kv_bytes = 2.0 * B * H * Nk * d * 2
+    value = flops * K * world / t_job / 1e12
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = kv_bytes * K / t_rank / 1e9
+
+    # end to end: pinned host Q, K, V in, O and lse out, every step
+    e2e_steps = max(3, min(args.e2e_steps, 5))
+    pq, pk, pv = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (hq, hk, hv))
+    po = torch.empty(q.shape, dtype=torch.int16).pin_memory()
+    pl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    qi, ki, vi, oi = (t.view(torch.int16) for t in (q, k, v, o))
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        a0[i].record(stream)
+        qi.copy_(pq, non_blocking=True)
+        ki.copy_(pk, non_blocking=True)
+        vi.copy_(pv, non_blocking=True)
+        step()
+        po.copy_(oi, non_blocking=True)
+        pl.copy_(lse, non_blocking=True)
+        a1[i].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_t = max_over_ranks(sum(a0[i].elapsed_time(a1[i]) for i in range(e2e_steps)) / 1e3,
+                           world, device)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = os.cpu_count() or 1
+        heads, t_cpu = 0, 0.0
+        for b in range(B):
+            for h in range(H):
+                if t_cpu >= args.cpu_budget:
+                    break
+                t0 = time.perf_counter()
+                oracle.forward_qk(W.bf16_bits_to_f64(hq[b:b + 1, h:h + 1]),
+                                  W.bf16_bits_to_f64(hk[b:b + 1, h:h + 1]),
+                                  W.bf16_bits_to_f64(hv[b:b + 1, h:h + 1]), scale,
+                                  nthreads=threads)
+                t_cpu += time.perf_counter() - t0
+                heads += 1
+        cpu = {"value": 4.0 * Nq * Nk * d * heads / t_cpu / 1e12, "unit": UNIT, "cores": threads,
+               "kind": "oracle", "sample": f"{heads} of {B * H} (b, h) heads, forward",
+               "seconds": t_cpu}
+
+    if rank == 0:
+        line = {
+            "metric": "split-KV decode forward TFLOP/s (bf16, 1\u00d7GB300)",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_job / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode: one query per head against a 32K-key cache",
+                       "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "scale": scale,
+                       "splits": "auto (about two CTAs per SM)",
+                       "l2": "flushed between timed steps; K and V (2.1 GB) exceed L2 anyway",
+                       "parallelism": "replicas"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "traffic": None,
+                         "kernel": "fa_fwd_kernel (split mode) + fa_fwd_merge_kernel",
+                         "peak_source": f"hbm_gbs of {peak_src}",
+                         "algorithmic_bytes_per_launch": kv_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": flops * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": (pq.numel() + pk.numel() + pv.numel()) * 2,
+                    "d2h_bytes_per_step": po.numel() * 2 + pl.numel() * 4,
+                    "steps": e2e_steps, "ms_per_step": 1e3 * e2e_t / e2e_steps},
+            "gpu_launches": 2 * K,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -517,7 +663,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="workload name from workloads.py (the reported line uses bert)")
+                    help="workload name from workloads.py (the reported line uses bert), or "
+                         "'decode' for the split-KV forward on a decode-shaped problem")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -536,6 +683,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, rank, world)
+        if args.workload == "decode":
+            return run_decode(args, rank, world, local)
         return run_ours(args, rank, world, local)
     finally:
         if world > 1:

@@ -134,7 +134,9 @@ constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 constexpr uint32_t kSoftmaxWarps = 4;
 
-template <bool kDrop>
+// kDrop: fused dropout; kSplit: split-KV partial (key range per blockIdx.z,
+// fp32 partial outputs for the merge kernel).
+template <bool kDrop, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
   int j_begin = 0, j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
-  if (args.n_split > 0) {
+  if (kSplit) {
     // split-KV (no causal, no block mask): this CTA's contiguous range of key tiles
     const int per = (n_kv + args.n_split - 1) / args.n_split;
     j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const float inv = (n > 0 && l > 0.f) ? (kDrop ? pr.keep_scale : 1.f) / l : 0.f;
         const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        if (args.n_split > 0) {
+        if (kSplit) {
           // split-KV partial: O_s = O / l_s (fp32) and lse_s of this row, for the merge
           if (qrow < pr.N) {
             const size_t prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     named_bar_sync(1, 128);
-    if (tid == 0 && ok && !s.abort && args.n_split == 0) {
+    if (!kSplit && tid == 0 && ok && !s.abort) {
       tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
       bulk_commit();
       bulk_wait_all();
@@ -517,11 +519,14 @@ cudaError_t launch_fwd_config() {
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
     const int smem = static_cast<int>(fwd_smem_bytes());
-    e = cudaFuncSetAttribute(fa_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
+    e = cudaFuncSetAttribute(fa_fwd_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fa_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem);
+      e = cudaFuncSetAttribute(fa_fwd_kernel<true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_fwd_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
@@ -535,8 +540,9 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   const size_t smem = fwd_smem_bytes();
   dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
   if (a.pr.drop_p8 > 0)
-    return launch_pdl(fa_fwd_kernel<true>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
-  return launch_pdl(fa_fwd_kernel<false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
+    return launch_pdl(fa_fwd_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to,
+                      a);
+  return launch_pdl(fa_fwd_kernel<false, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
 }
 
 cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
@@ -545,8 +551,8 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
   if (e != cudaSuccess) return e;
   const dim3 grid(a.pr.B * a.pr.H, a.pr.nt, a.n_split);
   // the O tensor map is not used in split mode (the merge kernel writes O)
-  e = launch_pdl(fa_fwd_kernel<false>, grid, dim3(kThreads), fwd_smem_bytes(), st, tq, tk, tv, tq,
-                 a);
+  e = launch_pdl(fa_fwd_kernel<false, true>, grid, dim3(kThreads), fwd_smem_bytes(), st, tq, tk, tv,
+                 tq, a);
   if (e != cudaSuccess) return e;
   const dim3 mgrid((a.pr.N + 31) / 32, a.pr.B * a.pr.H);
   return launch_pdl(fa_fwd_merge_kernel, mgrid, dim3(256), 0, st, a);
