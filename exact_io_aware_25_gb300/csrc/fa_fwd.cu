@@ -107,12 +107,15 @@ __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2
                                          uint32_t jp0) {
 #pragma unroll
   for (int c = half * 64; c < half * 64 + 64; c += 8) {
+    float x[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float x = fmaf(sv[c + u], sl2, -m);
-      sv[c + u] = (u < kPoly) ? exp2_poly(x) : ex2_approx(x);
-      rs8[u] += sv[c + u];
-    }
+    for (int u = 0; u < 8; u += 2)
+      fma2(x[u], x[u + 1], sv[c + u], sv[c + u + 1], sl2, sl2, -m, -m);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sv[c + u] = (u < kPoly) ? exp2_poly(x[u]) : ex2_approx(x[u]);
+#pragma unroll
+    for (int u = 0; u < 8; u += 2)
+      add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
       float a = sv[c + u], b = sv[c + u + 1];
@@ -339,14 +342,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < kTile; ++c)
           if (c >= lim_kv || c > lim_c) sv[c] = -INFINITY;
       }
-      // row max: eight independent chains, then a tree
+      // row max: eight independent chains of three-input maxima, then a tree
       float mx8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = sv[u];
+      for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[u], sv[8 + u]);
 #pragma unroll
-      for (int c = 8; c < kTile; c += 8)
+      for (int c = 16; c < kTile; c += 16)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], sv[c + u]);
+        for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[c + u], sv[c + 8 + u]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_cand = fmaxf(m, mx * sl2);
