@@ -294,10 +294,14 @@ __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int kr, bo
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     const float4 l4 = ld_shared_f4(lse2 + (qc + 4 * g) * 4);
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    float x[4];
+    fma2(x[0], x[1], __uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]), sl2, sl2, -l4.x,
+         -l4.y);
+    fma2(x[2], x[3], __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]), sl2, sl2,
+         -l4.z, -l4.w);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      float p = ex2_approx(fmaf(__uint_as_float(v[4 * g + u]), sl2, -lv[u]));
+      float p = ex2_approx(x[u]);
       if (kMask) {
         const bool masked = !key_ok || (diag && kr > qc + 4 * g + u);
         p = masked ? 0.f : p;
@@ -358,14 +362,16 @@ __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint3
     for (int g = 0; g < 4; ++g) {
       const int e0 = 16 * c + 4 * g;
       const float4 d4 = ld_shared_f4(dsum + (qc + e0) * 4);
-      const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-      float ds[4];
+      float dp[4], ds[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float dp = __uint_as_float(dv[e0 + u]);
-        if (kDrop) dp = (keep >> (e0 + u)) & 1u ? dp * keep_scale : 0.f;
-        ds[u] = __uint_as_float(pv[e0 + u]) * (dp - dl[u]);
+        dp[u] = __uint_as_float(dv[e0 + u]);
+        if (kDrop) dp[u] = (keep >> (e0 + u)) & 1u ? dp[u] * keep_scale : 0.f;
       }
+      sub2(dp[0], dp[1], dp[0], dp[1], d4.x, d4.y);
+      sub2(dp[2], dp[3], dp[2], dp[3], d4.z, d4.w);
+      mul2(ds[0], ds[1], __uint_as_float(pv[e0]), __uint_as_float(pv[e0 + 1]), dp[0], dp[1]);
+      mul2(ds[2], ds[3], __uint_as_float(pv[e0 + 2]), __uint_as_float(pv[e0 + 3]), dp[2], dp[3]);
       dw[2 * g] = pack_bf16(ds[0], ds[1]);
       dw[2 * g + 1] = pack_bf16(ds[2], ds[3]);
     }
