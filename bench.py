@@ -510,6 +510,118 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+# ---------------------------------------------------------------- forward only (any head dim)
+
+def run_fwd_only(args, rank, world, local):
+    """Times fa_fwd alone on a workload with its head dimension overridden
+    (--head-dim 128: the wide forward kernel, whose backward is not built).
+    Same timing rules as the fwd+bwd line; the metric is forward TFLOP/s."""
+    import numpy as np
+    import torch
+
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+
+    fa.lib()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = W.make(args.workload, d=args.head_dim)
+    s = w.spec
+    B, H, N, d = s.B, s.H, s.N, s.d
+    fl = counted_flops(s, w.kv_len, w.block_mask)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(torch.bfloat16)
+
+    q, k, v = dev(w.q), dev(w.k), dev(w.v)
+    kv_len = torch.from_numpy(w.kv_len).to(device) if w.kv_len is not None else None
+    mask = (torch.from_numpy(w.block_mask).to(device) if w.block_mask is not None else None)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, B, H, N, d, s.scale, s.causal, kv_len, mask, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step()
+    fa.fa_check(stream)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    barrier(world, device)
+    fa.fa_check(stream)
+    t_job = max_over_ranks(sum(ev0[i].elapsed_time(ev1[i]) for i in range(K)) / 1e3, world,
+                           device)
+    value = fl["fwd"] * K * world / t_job / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    kernel = "fa_fwd_d128_kernel" if d == 128 else "fa_fwd_kernel"
+    roofline = {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": UNIT,
+                "frac": value / world / peak, "traffic": None, "kernel": kernel,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "algorithmic_flops_per_launch": fl["fwd"], "avg_launch_ms": 1e3 * t_job / K}
+
+    e2e_steps = max(3, min(args.e2e_steps, K))
+    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (w.q, w.k, w.v))
+    ho = torch.empty(q.shape, dtype=torch.int16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    qi, ki, vi, oi = (t.view(torch.int16) for t in (q, k, v, o))
+
+    def e2e_step():
+        qi.copy_(hq, non_blocking=True)
+        ki.copy_(hk, non_blocking=True)
+        vi.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(oi, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.fill_(i & 0xFF)
+        e0[i].record(stream)
+        e2e_step()
+        e1[i].record(stream)
+    torch.cuda.synchronize(device)
+    fa.fa_check(stream)
+    e2e_t = max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
+                           world, device)
+    t_bytes = q.numel() * 2
+    e2e = {"value": fl["fwd"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 3 * t_bytes, "d2h_bytes_per_step": t_bytes + hlse.numel() * 4,
+           "steps": e2e_steps}
+    if rank == 0:
+        cfg = workload_config(w)
+        cfg["workload"] = cfg["workload"].replace("fwd+bwd", f"forward only, d={d}")
+        line = {
+            "metric": f"attention fwd TFLOP/s (bf16, d={d}, 1\u00d7GB300) and % of dense BF16 peak",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_job / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "pct_of_peak": value / world / peak, "roofline": roofline, "cpu_baseline": None,
+            "e2e": e2e, "gpu_launches": K, "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- split-KV decode
 
 DECODE = {"B": 16, "H": 16, "Nq": 1, "Nk": 32768, "d": 64, "scale": 0.125, "seed": 6}
@@ -671,6 +783,9 @@ def main(argv=None):
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="drop probability of the fused dropout (0 = plain attention)")
     ap.add_argument("--seed", type=int, default=1234, help="dropout seed")
+    ap.add_argument("--head-dim", type=int, default=64, choices=[64, 128],
+                    help="head dimension; 128 times the forward alone")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward alone")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
     if world > 1:
@@ -685,6 +800,8 @@ def main(argv=None):
             return run_reference(args, rank, world)
         if args.workload == "decode":
             return run_decode(args, rank, world, local)
+        if args.head_dim != 64 or args.fwd_only:
+            return run_fwd_only(args, rank, world, local)
         return run_ours(args, rank, world, local)
     finally:
         if world > 1:

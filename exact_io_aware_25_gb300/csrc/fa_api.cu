@@ -68,16 +68,17 @@ fa_status device_setup(int *dev_out, int **err_out) {
   return FA_OK;
 }
 
-// [B*H, N, 64] bf16 viewed as a 3-D tensor {d, N, B*H}; 128 x 64 boxes,
-// 128-byte swizzle; rows past N read as zeros and are dropped on store.
-bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N) {
+// [B*H, N, d] bf16 viewed as a 3-D tensor {d, N, B*H}; 128-row x 64-column
+// boxes (one 128-byte swizzle span; a d = 128 tile is two boxes), 128-byte
+// swizzle; rows past N read as zeros and are dropped on store.
+bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N, int d = kHeadDim) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(N),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
-                                 static_cast<cuuint64_t>(N) * kHeadDim * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kTile), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -100,12 +101,14 @@ bool encode_dq_acc(CUtensorMap *m, const void *ptr, size_t rows) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask) {
+// wide: the forward, which also takes d = 128.
+fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask,
+                          bool wide = false) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows >= (1LL << 31) || static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
-  if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  if (d != kHeadDim && !(wide && d == kHeadDimWide)) return FA_ERR_UNSUPPORTED;
   const int nt = (N + kTile - 1) / kTile;
   if (nt > kMaxGridTiles) return FA_ERR_UNSUPPORTED;
   if (block_mask && nt > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
@@ -132,6 +135,7 @@ Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t
   p.H = H;
   p.N = N;
   p.Nk = N;
+  p.d = kHeadDim;
   p.nt = (N + kTile - 1) / kTile;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -195,12 +199,12 @@ struct SplitWs {
   int nq_pad;
 };
 
-SplitWs splitkv_ws(int B, int H, int Nq, int S) {
+SplitWs splitkv_ws(int B, int H, int Nq, int d, int S) {
   SplitWs w{};
   w.nq_pad = static_cast<int>(align_up(static_cast<size_t>(Nq), kTile));
   const size_t rows = static_cast<size_t>(S) * B * H * w.nq_pad;
   w.part_o = 0;
-  w.part_lse = align_up(rows * kHeadDim * sizeof(float), 256);
+  w.part_lse = align_up(rows * static_cast<size_t>(d) * sizeof(float), 256);
   w.total = align_up(w.part_lse + rows * sizeof(float), 256);
   return w;
 }
@@ -211,7 +215,7 @@ fa_status validate_splitkv(int B, int H, int Nq, int Nk, int d, float scale, int
   if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
   const long long bh = static_cast<long long>(B) * H;
   if (bh >= 65536 || bh * Nq >= (1LL << 31) || bh * Nk >= (1LL << 31)) return FA_ERR_INVALID_ARG;
-  if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+  if (d != kHeadDim && d != kHeadDimWide) return FA_ERR_UNSUPPORTED;
   if ((Nq + kTile - 1) / kTile > kMaxGridTiles) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -228,7 +232,7 @@ fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, f
                          const int32_t *kv_len, const uint8_t *block_mask, float p,
                          unsigned long long seed, void *stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  fa_status st = validate_common(B, H, N, d, scale, block_mask);
+  fa_status st = validate_common(B, H, N, d, scale, block_mask, true);
   if (st != FA_OK) return st;
   const int p8 = drop_threshold(p);
   if (p8 < 0) return FA_ERR_INVALID_ARG;
@@ -240,20 +244,22 @@ fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, f
   if ((st = device_setup(&dev, &err)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bhnd(&tq, q, BH, N) || !encode_bhnd(&tk, k, BH, N) || !encode_bhnd(&tv, v, BH, N) ||
-      !encode_bhnd(&to, o, BH, N))
+  if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, N, d) ||
+      !encode_bhnd(&tv, v, BH, N, d) || !encode_bhnd(&to, o, BH, N, d))
     return FA_ERR_CUDA;
   FwdArgs a{};
   a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
+  a.pr.d = d;
   a.lse = lse;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     a.starve = g_starve_next;
     g_starve_next = 0;
   }
-  return launch_fwd(tq, tk, tv, to, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == kHeadDimWide ? launch_fwd_d128(tq, tk, tv, to, a, cs)
+                                          : launch_fwd(tq, tk, tv, to, a, cs);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
@@ -324,7 +330,7 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (validate_splitkv(B, H, Nq, Nk, d, 1.f, num_splits) != FA_OK) return 0;
-  return splitkv_ws(B, H, Nq, splitkv_splits(B, H, Nq, Nk, num_splits)).total;
+  return splitkv_ws(B, H, Nq, d, splitkv_splits(B, H, Nq, Nk, num_splits)).total;
 }
 
 fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -336,18 +342,20 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
   const int S = splitkv_splits(B, H, Nq, Nk, num_splits);
-  const SplitWs wl = splitkv_ws(B, H, Nq, S);
+  const SplitWs wl = splitkv_ws(B, H, Nq, d, S);
   if (!workspace || !aligned16(workspace) || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
   int dev = 0;
   int *err = nullptr;
   if ((st = device_setup(&dev, &err)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
-  if (!encode_bhnd(&tq, q, BH, Nq) || !encode_bhnd(&tk, k, BH, Nk) || !encode_bhnd(&tv, v, BH, Nk))
+  if (!encode_bhnd(&tq, q, BH, Nq, d) || !encode_bhnd(&tk, k, BH, Nk, d) ||
+      !encode_bhnd(&tv, v, BH, Nk, d))
     return FA_ERR_CUDA;
   FwdArgs a{};
   a.pr = make_problem(B, H, Nq, scale, 0, kv_len, nullptr, err);
   a.pr.Nk = Nk;
+  a.pr.d = d;
   a.lse = lse;
   a.n_split = S;
   a.nq_pad = wl.nq_pad;
@@ -355,9 +363,10 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
   a.part_o = reinterpret_cast<float *>(ws + wl.part_o);
   a.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
   a.o = static_cast<uint16_t *>(o);
-  return launch_fwd_splitkv(tq, tk, tv, a, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == kHeadDimWide ? launch_fwd_splitkv_d128(tq, tk, tv, a, cs)
+                                          : launch_fwd_splitkv(tq, tk, tv, a, cs);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -389,7 +398,8 @@ const char *fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, bad size or bad scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 on an sm_103 GPU";
+    case FA_ERR_UNSUPPORTED:
+      return "FA_ERR_UNSUPPORTED: head dim (64; 128 forward only), size limit or device (sm_103)";
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel's bounded wait ran out";

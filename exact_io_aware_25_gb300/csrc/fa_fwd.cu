@@ -27,6 +27,7 @@
 // Division by l is deferred to the epilogue; the result equals the pages'
 // per-step normalised update because both use the same running max.
 #include "fa_kernels.cuh"
+#include "fa_fwd_common.cuh"
 
 namespace fa {
 namespace {
@@ -64,76 +65,6 @@ constexpr uint32_t kColS = 0, kColP = 128, kColO = 192, kTmemCols = 256;
 __device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
   return sparse ? static_cast<int>(s.tiles[it]) : s.tile0 + it;
 }
-
-// The running reference max of a row is only moved when the row max exceeds
-// it by more than this (base-2 units), so P~ <= 2^8 and the O rescale is rare.
-// Exact: O / l and lse use the same reference.
-constexpr float kLazyRescale = 8.f;
-
-// 2^x for x in [-126, 9) without the MUFU unit: n = round(x) from the
-// 1.5 * 2^23 rounding trick, f = x - n in [-1/2, 1/2], 2^f by a degree-4
-// polynomial (Chebyshev interpolation of 2^f at 5 nodes, coefficients from
-// gen_exp2_poly.py; relative error below 4e-6), and n added to the exponent
-// field.  Inputs below -126 are clamped (result ~1e-38, never used where an
-// exact 0 is required: edge tiles take the MUFU path).
-__device__ __forceinline__ float exp2_poly(float x) {
-  constexpr float c0 = 1.000000000e+00f, c1 = 6.931210160e-01f, c2 = 2.402234972e-01f,
-                  c3 = 5.592197552e-02f, c4 = 9.666368365e-03f;
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;
-  const float n = t - 12582912.f;
-  const float r = x - n;
-  const float q = fmaf(fmaf(fmaf(fmaf(c4, r, c3), r, c2), r, c1), r, c0);
-  const int ni = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(q) + (ni << 23));
-}
-
-// Dropout state of one query row: hash key with the row pair folded in, the
-// bit offset of the row's two bytes in each block word, the threshold.
-struct RowDrop {
-  uint32_t key;    // head key ^ ((i >> 1) << 16)
-  uint32_t shift;  // 16 * (i & 1)
-  uint32_t p8;
-};
-
-// Exponentials of one 64-column half of a row: sv[c] <- 2^(sv[c]*sl2 - m),
-// accumulated into the eight partial sums (before dropout) and packed to
-// bf16 pairs, with dropped elements packed as 0 when kDrop (jp0 = index of
-// the tile's first key pair).  In every group of eight columns the first
-// kPoly use exp2_poly (FMA pipe), the rest the MUFU unit.
-template <int kPoly, bool kDrop>
-__device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
-                                         float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
-                                         uint32_t jp0) {
-#pragma unroll
-  for (int c = half * 64; c < half * 64 + 64; c += 8) {
-    float x[8];
-#pragma unroll
-    for (int u = 0; u < 8; u += 2)
-      fma2(x[u], x[u + 1], sv[c + u], sv[c + u + 1], sl2, sl2, -m, -m);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) sv[c + u] = (u < kPoly) ? exp2_poly(x[u]) : ex2_approx(x[u]);
-#pragma unroll
-    for (int u = 0; u < 8; u += 2)
-      add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
-#pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      float a = sv[c + u], b = sv[c + u + 1];
-      if (kDrop) {
-        // keys c + u (even) and c + u + 1 share one block word
-        const uint32_t r = pcg_hash(rd.key ^ (jp0 + static_cast<uint32_t>((c + u) >> 1))) >> rd.shift;
-        a = (r & 0xffu) >= rd.p8 ? a : 0.f;
-        b = ((r >> 8) & 0xffu) >= rd.p8 ? b : 0.f;
-      }
-      pk[((c - half * 64) + u) >> 1] = pack_bf16(a, b);
-    }
-  }
-}
-
-#ifndef FA_FWD_POLY_PER8
-#define FA_FWD_POLY_PER8 0
-#endif
-constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 constexpr uint32_t kSoftmaxWarps = 4;
 
@@ -196,19 +127,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ([EXPL] "Extension: Block-Sparse FlashAttention": only nonzero blocks
   // are evaluated).
   if (warp == 0) {
-    int count = 0;
-    if (sparse) {
-      const uint8_t *row = pr.block_mask + static_cast<size_t>(qt) * pr.nt;
-      for (int base = 0; base < j_end; base += 32) {
-        const int j = base + lane;
-        const bool keep = j < j_end && __ldg(row + j) != 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-        if (keep) s.tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(j);
-        count += __popc(bal);
-      }
-    } else {
-      count = j_end - j_begin;
-    }
+    const int count = sparse ? compact_mask_row(pr.block_mask + static_cast<size_t>(qt) * pr.nt,
+                                                j_end, s.tiles, lane)
+                             : j_end - j_begin;
     if (lane == 0) {
       s.n_tiles = count;
       s.tile0 = j_begin;
@@ -336,22 +257,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int key0 = j * kTile;
       const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
       if (edge) {
-        const int lim_kv = kv_bound - key0;                        // keys >= this are padding
-        const int lim_c = pr.causal ? (qrow - key0) : kTile;       // keys > this are in the future
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c >= lim_kv || c > lim_c) sv[c] = -INFINITY;
+        // keys >= kv_bound are padding; keys > qrow are in the future
+        mask_row(sv, kv_bound - key0, pr.causal ? (qrow - key0) : kTile);
       }
-      // row max: eight independent chains of three-input maxima, then a tree
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[u], sv[8 + u]);
-#pragma unroll
-      for (int c = 16; c < kTile; c += 16)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[c + u], sv[c + 8 + u]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx = row_max(sv);
       const float m_cand = fmaxf(m, mx * sl2);
       const bool bump = (m == -INFINITY) || (m_cand > m + kLazyRescale);
       const float m_ref = bump ? m_cand : m;
@@ -461,55 +370,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// Split-KV merge ([MATH] §4: the softmax-weighted sum over the keys splits
-// into independent ranges whose (max, sum, output) states combine by
-// rescaling).  Each split s left O_s = (sum over its keys of P~ V) / l_s and
-// lse_s = m_s + ln l_s; then lse = ln sum_s e^{lse_s} and
-// O = sum_s e^{lse_s - lse} O_s.  8 threads per query row, 8 columns each.
-__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const FwdArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int bh = blockIdx.y;
-  const int row = blockIdx.x * 32 + static_cast<int>(threadIdx.x >> 3);
-  const int sub = threadIdx.x & 7;
-  if (row >= a.pr.N) return;
-  const int S = a.n_split, BH = a.pr.B * a.pr.H;
-  const size_t stride = static_cast<size_t>(BH) * a.nq_pad;   // between splits
-  const size_t base = static_cast<size_t>(bh) * a.nq_pad + row;
-  float mx = -INFINITY;
-  for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, a.part_lse[base + sp * stride]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  if (mx != -INFINITY) {
-    for (int sp = 0; sp < S; ++sp) {
-      const float ls = a.part_lse[base + sp * stride];
-      if (ls == -INFINITY) continue;
-      const float w = __expf(ls - mx);
-      den += w;
-      const float4 *src =
-          reinterpret_cast<const float4 *>(a.part_o + (base + sp * stride) * kHeadDim + sub * 8);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] = fmaf(w, x0.x, acc[0]);
-      acc[1] = fmaf(w, x0.y, acc[1]);
-      acc[2] = fmaf(w, x0.z, acc[2]);
-      acc[3] = fmaf(w, x0.w, acc[3]);
-      acc[4] = fmaf(w, x1.x, acc[4]);
-      acc[5] = fmaf(w, x1.y, acc[5]);
-      acc[6] = fmaf(w, x1.z, acc[6]);
-      acc[7] = fmaf(w, x1.w, acc[7]);
-    }
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  uint4 out;
-  out.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  out.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  out.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  out.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  const size_t orow = static_cast<size_t>(bh) * a.pr.N + row;
-  *reinterpret_cast<uint4 *>(a.o + orow * kHeadDim + sub * 8) = out;
-  if (sub == 0) a.lse[orow] = den > 0.f ? mx + __logf(den) : -INFINITY;
-}
-
 }  // namespace
 
 size_t fwd_smem_bytes() { return sizeof(FwdSmem) + 1024; }
@@ -558,7 +418,7 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
                  tq, a);
   if (e != cudaSuccess) return e;
   const dim3 mgrid((a.pr.N + 31) / 32, a.pr.B * a.pr.H);
-  return launch_pdl(fa_fwd_merge_kernel, mgrid, dim3(256), 0, st, a);
+  return launch_pdl(fa_fwd_merge_kernel<kHeadDim>, mgrid, dim3(256), 0, st, a);
 }
 
 }  // namespace fa

@@ -1,0 +1,444 @@
+// fa_fwd_d128.cu -- forward kernel of exact tiled attention for head
+// dimension d = 128 on sm_103a.
+//
+// Same method as the d = 64 kernel ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness" (explainer page),
+// "Method": S_ij on chip, running max and exponential sum, rescaled partial
+// output, only O and lse written), with a layout for the wider head:
+//
+// One CTA per (query tile, b*h) and per SM (192 KiB of shared memory, all
+// 512 TMEM columns); 6 warps:
+//   warp 4   TMA producer: Q once, K_j (3-stage ring, two tiles ahead) and
+//            V_j (2-stage ring).  Each 128 x 128 bf16 tile is two 128 x 64
+//            boxes (the 128-byte swizzle spans 64 bf16), 16 KiB apart.
+//   warp 5   TMEM owner and MMA issuer: S_j = Q K_j^T (M=128, N=128, K=128)
+//            into one of two S buffers, and O += P~_j V_j (M=128, N=128,
+//            K=128) with P~_j from one of two P~ buffers in TMEM.  S_{j+2}
+//            is issued as soon as the softmax has pulled S_j into registers,
+//            ahead of PV_j, so the next S is always ready when the softmax
+//            finishes a tile.
+//   warps 0-3 softmax: thread t owns query row t; as in the d = 64 kernel,
+//            except that the P~ store waits only for PV_{j-2} (the other
+//            buffer's reader) and the O rescale, when the lazily moved max
+//            requires one, waits for PV_{j-1}.
+// TMEM columns: S buffers 0-127 and 128-255, P~ buffers 256-319 and
+// 320-383 (bf16 pairs), O accumulator 384-511.
+#include "fa_kernels.cuh"
+#include "fa_fwd_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kD = kHeadDimWide;
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kSoftmaxWarps = 4;
+constexpr uint32_t kHalfBytes = kTile * 64 * 2;  // 128 rows x 64 bf16: one swizzle span
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KiB: d 0-63, then d 64-127
+
+struct __align__(1024) Fwd128Smem {
+  uint8_t q[kTileBytes];  // Q_i; reused to stage O for the TMA stores
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
+  uint64_t bar_q;
+  uint64_t bar_k_full[kKStages];
+  uint64_t bar_k_empty[kKStages];
+  uint64_t bar_v_full[kVStages];
+  uint64_t bar_v_empty[kVStages];
+  uint64_t bar_s_full[2];
+  uint64_t bar_s_free[2];
+  uint64_t bar_p_full[2];
+  uint64_t bar_o_done[2];
+  uint64_t bar_final;
+  uint32_t tmem_base;
+  int abort;
+  int n_tiles;
+  int tile0;
+  int16_t tiles[kMaxMaskTiles];
+};
+
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384, kTmemCols = 512;
+
+__device__ __forceinline__ int tile_at(const Fwd128Smem &s, bool sparse, int it) {
+  return sparse ? static_cast<int>(s.tiles[it]) : s.tile0 + it;
+}
+
+template <bool kDrop, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o, const FwdArgs args) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  Fwd128Smem &s = *reinterpret_cast<Fwd128Smem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const Problem &pr = args.pr;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heads vary fastest in launch order; the heaviest (last) query tiles go first
+  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.y);
+  const int bh = blockIdx.x;
+  const int b = bh / pr.H;
+  const int kv_bound = key_bound(pr, b);
+  const int n_kv = (kv_bound + kTile - 1) / kTile;
+  int j_begin = 0, j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
+  if (kSplit) {
+    const int per = (n_kv + args.n_split - 1) / args.n_split;
+    j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
+    j_end = min(n_kv, j_begin + per);
+  }
+  const bool sparse = pr.block_mask != nullptr;
+
+  if (tid == 0) {
+    mbar_init(&s.bar_q, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&s.bar_k_full[i], 1);
+      mbar_init(&s.bar_k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&s.bar_v_full[i], 1);
+      mbar_init(&s.bar_v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.bar_s_full[i], 1);
+      mbar_init(&s.bar_s_free[i], kSoftmaxWarps);
+      mbar_init(&s.bar_p_full[i], kSoftmaxWarps);
+      mbar_init(&s.bar_o_done[i], 1);
+    }
+    mbar_init(&s.bar_final, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 0) {
+    const int count = sparse ? compact_mask_row(pr.block_mask + static_cast<size_t>(qt) * pr.nt,
+                                                j_end, s.tiles, lane)
+                             : j_end - j_begin;
+    if (lane == 0) {
+      s.n_tiles = count;
+      s.tile0 = j_begin;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int n = s.n_tiles;
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (n > 0) {
+      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      tma_load_3d_w(s.q + kHalfBytes, &tm_q, &s.bar_q, 64, qt * kTile, bh);
+      if (!args.starve) {
+        auto load_k = [&](int it) -> bool {
+          const int st = it % kKStages;
+          const uint32_t use = it / kKStages;
+          if (use > 0 && !mbar_wait_warp(&s.bar_k_empty[st], (use - 1) & 1, pr.wait, &s.abort))
+            return false;
+          const int row = tile_at(s, sparse, it) * kTile;
+          mbar_arrive_expect_tx_w(&s.bar_k_full[st], kTileBytes);
+          tma_load_3d_w(s.k[st], &tm_k, &s.bar_k_full[st], 0, row, bh);
+          tma_load_3d_w(s.k[st] + kHalfBytes, &tm_k, &s.bar_k_full[st], 64, row, bh);
+          return true;
+        };
+        bool ok = load_k(0);
+        if (ok && n > 1) ok = load_k(1);
+        for (int it = 0; ok && it < n; ++it) {
+          if (it + 2 < n && !load_k(it + 2)) break;
+          const int st = it % kVStages;
+          const uint32_t use = it / kVStages;
+          if (use > 0 && !mbar_wait_warp(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort))
+            break;
+          const int row = tile_at(s, sparse, it) * kTile;
+          mbar_arrive_expect_tx_w(&s.bar_v_full[st], kTileBytes);
+          tma_load_3d_w(s.v[st], &tm_v, &s.bar_v_full[st], 0, row, bh);
+          tma_load_3d_w(s.v[st] + kHalfBytes, &tm_v, &s.bar_v_full[st], 64, row, bh);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (n > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 128, false, true);
+      const uint64_t d_q0 = sdesc_sw128(smem_u32(s.q), 16, 1024);
+      const uint64_t d_q1 = sdesc_sw128(smem_u32(s.q + kHalfBytes), 16, 1024);
+      bool ok = mbar_wait_warp(&s.bar_q, 0, pr.wait, &s.abort);
+      // S_it = Q K_it^T into S buffer it & 1: K = 128 as two 64-wide halves.
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % kKStages;
+        if (!mbar_wait_warp(&s.bar_k_full[st], (it / kKStages) & 1, pr.wait, &s.abort))
+          return false;
+        tc_fence_after();
+        const uint64_t d_k0 = sdesc_sw128(smem_u32(s.k[st]), 16, 1024);
+        const uint64_t d_k1 = sdesc_sw128(smem_u32(s.k[st] + kHalfBytes), 16, 1024);
+        const uint32_t dst = tmem + kColS + static_cast<uint32_t>(it & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss_w(dst, d_q0 + kk * 2, d_k0 + kk * 2, idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss_w(dst, d_q1 + kk * 2, d_k1 + kk * 2, idesc_s, 1u);
+        mma_commit_w(&s.bar_s_full[it & 1]);
+        mma_commit_w(&s.bar_k_empty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      for (int it = 0; ok && it < n; ++it) {
+        const int bf = it & 1;
+        const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (it + 2 < n) {
+          // the softmax has copied S_it into registers: its buffer takes S_{it+2}
+          if (!mbar_wait_warp(&s.bar_s_free[bf], ph, pr.wait, &s.abort)) break;
+          if (!issue_s(it + 2)) break;
+        }
+        if (!mbar_wait_warp(&s.bar_p_full[bf], ph, pr.wait, &s.abort)) break;
+        const int st = it % kVStages;
+        if (!mbar_wait_warp(&s.bar_v_full[st], (it / kVStages) & 1, pr.wait, &s.abort)) break;
+        tc_fence_after();
+        // A = P~_it from TMEM (16 keys = 8 packed columns per step); B = V_j,
+        // [keys][d] with d contiguous: MN-major, two 64-wide swizzle spans
+        // along N (leading offset 16 KiB), 8-key groups 1024 bytes apart.
+        const uint64_t d_v = sdesc_sw128(smem_u32(s.v[st]), kHalfBytes, 1024);
+        const uint32_t pa = tmem + kColP + static_cast<uint32_t>(bf) * 64;
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ts_w(tmem + kColO, pa + kk * 8, d_v + kk * 128, idesc_o, kk > 0 ? 1u : acc0);
+        mma_commit_w(&s.bar_o_done[bf]);
+        mma_commit_w(&s.bar_v_empty[st]);
+      }
+    }
+    mma_commit_w(&s.bar_final);
+    mbar_wait_drain(&s.bar_final, 0, pr.wait);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (rows)
+    const int row = tid;
+    const int qrow = qt * kTile + row;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = pr.scale_log2;
+    float m = -INFINITY;
+    float l = 0.f;
+    RowDrop rd{0u, 0u, 0u};
+    if (kDrop) {
+      rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
+      rd.shift = 16u * static_cast<uint32_t>(qrow & 1);
+      rd.p8 = pr.drop_p8;
+    }
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int bf = it & 1;
+      const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+      const int j = tile_at(s, sparse, it);
+      if (!mbar_wait_warp(&s.bar_s_full[bf], ph, pr.wait, &s.abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[kTile];
+      {
+        uint32_t raw[kTile];
+        const uint32_t t0 = tmem + lane_base + kColS + static_cast<uint32_t>(bf) * 128;
+        tmem_ld32(t0 + 0, raw + 0);
+        tmem_ld32(t0 + 32, raw + 32);
+        tmem_ld32(t0 + 64, raw + 64);
+        tmem_ld32(t0 + 96, raw + 96);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar_s_free[bf]);
+      const int key0 = j * kTile;
+      const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
+      if (edge) mask_row(sv, kv_bound - key0, pr.causal ? (qrow - key0) : kTile);
+      const float mx = row_max(sv);
+      const float m_cand = fmaxf(m, mx * sl2);
+      const bool bump = (m == -INFINITY) || (m_cand > m + kLazyRescale);
+      const float m_ref = bump ? m_cand : m;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float alpha = bump ? ex2_approx(m - m_use) : 1.f;
+      float rs8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+      const uint32_t p_base = tmem + lane_base + kColP + static_cast<uint32_t>(bf) * 64;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+        const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
+        if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
+        else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
+        if (half == 0 && it >= 2) {
+          // PV_{it-2} read this P~ buffer
+          if (!mbar_wait_warp(&s.bar_o_done[bf], ph ^ 1u, pr.wait, &s.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(p_base + half * 32, pk);
+      }
+      if (!ok) break;
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O must hold every PV up to it-1 before it is rescaled
+        const int pb = (it - 1) & 1;
+        if (!mbar_wait_warp(&s.bar_o_done[pb], static_cast<uint32_t>((it - 1) >> 1) & 1u, pr.wait,
+                            &s.abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t to = tmem + lane_base + kColO;
+        uint32_t ov[32];
+#pragma unroll
+        for (int q4 = 0; q4 < kD / 32; ++q4) {
+          tmem_ld32(to + q4 * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(to + q4 * 32, ov);
+        }
+      }
+      tmem_wait_st();
+      l = l * alpha + rs;
+      m = m_ref;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar_p_full[bf]);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok && n > 0) {
+      // the last PV's commit also covers every earlier MMA of the issuer
+      ok = mbar_wait_warp(&s.bar_o_done[(n - 1) & 1], static_cast<uint32_t>((n - 1) >> 1) & 1u,
+                          pr.wait, &s.abort);
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv = (n > 0 && l > 0.f) ? (kDrop ? pr.keep_scale : 1.f) / l : 0.f;
+      const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      size_t prow = 0;
+      if (kSplit)
+        prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
+                   static_cast<size_t>(args.nq_pad) + qrow;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float ov[64];
+        if (n > 0) {
+          uint32_t raw[64];
+          const uint32_t to = tmem + lane_base + kColO + h * 64;
+          tmem_ld32(to, raw);
+          tmem_ld32(to + 32, raw + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 64; ++c) ov[c] = __uint_as_float(raw[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) ov[c] = 0.f;
+        }
+        if (kSplit) {
+          if (qrow < pr.N) {
+            float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kD + h * 64);
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4)
+              dst[c4] = make_float4(ov[4 * c4] * inv, ov[4 * c4 + 1] * inv, ov[4 * c4 + 2] * inv,
+                                    ov[4 * c4 + 3] * inv);
+          }
+        } else {
+          const uint32_t q_base = smem_u32(s.q + h * kHalfBytes) + row * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const float *x = ov + ch * 8;
+            st_shared_v4(q_base + ((ch ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                         pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                         pack_bf16(x[6] * inv, x[7] * inv));
+          }
+        }
+      }
+      if (kSplit) {
+        if (qrow < pr.N) args.part_lse[prow] = lse;
+      } else {
+        if (qrow < pr.N) args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
+        fence_proxy_async_smem();
+      }
+    }
+    named_bar_sync(1, 128);
+    if (!kSplit && tid == 0 && ok && !s.abort) {
+      tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
+      tma_store_3d(&tm_o, s.q + kHalfBytes, 64, qt * kTile, bh);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t fwd_d128_smem_bytes() { return sizeof(Fwd128Smem) + 1024; }
+
+namespace {
+cudaError_t launch_fwd_d128_config() {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    const int smem = static_cast<int>(fwd_d128_smem_bytes());
+    e = cudaFuncSetAttribute(fa_fwd_d128_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_fwd_d128_kernel<true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fa_fwd_d128_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_fwd_d128(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &to, const FwdArgs &a, cudaStream_t st) {
+  cudaError_t e = launch_fwd_d128_config();
+  if (e != cudaSuccess) return e;
+  const size_t smem = fwd_d128_smem_bytes();
+  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
+  if (a.pr.drop_p8 > 0)
+    return launch_pdl(fa_fwd_d128_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv,
+                      to, a);
+  return launch_pdl(fa_fwd_d128_kernel<false, false>, grid, dim3(kThreads), smem, st, tq, tk, tv,
+                    to, a);
+}
+
+cudaError_t launch_fwd_splitkv_d128(const CUtensorMap &tq, const CUtensorMap &tk,
+                                    const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st) {
+  cudaError_t e = launch_fwd_d128_config();
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt, a.n_split);
+  e = launch_pdl(fa_fwd_d128_kernel<false, true>, grid, dim3(kThreads), fwd_d128_smem_bytes(), st,
+                 tq, tk, tv, tq, a);
+  if (e != cudaSuccess) return e;
+  const dim3 mgrid((a.pr.N + 31) / 32, a.pr.B * a.pr.H);
+  return launch_pdl(fa_fwd_merge_kernel<kD>, mgrid, dim3(256), 0, st, a);
+}
+
+}  // namespace fa

@@ -11,7 +11,8 @@
 namespace fa {
 
 constexpr int kTile = 128;      // B_r = B_c = 128 query / key rows per tile
-constexpr int kHeadDim = 64;    // d
+constexpr int kHeadDim = 64;    // d of the main kernels; the forward also has a d = 128 kernel
+constexpr int kHeadDimWide = 128;
 constexpr int kMaxMaskTiles = 1024;  // block-sparse: at most 1024 tiles per row (N <= 131072)
 // Query tiles per head are a grid dimension of the forward launch (y, at most 65535).
 constexpr int kMaxGridTiles = 65535;
@@ -19,6 +20,7 @@ constexpr int kMaxGridTiles = 65535;
 struct Problem {
   int B, H, N;            // N: query rows (and key rows, except in the split-KV forward)
   int Nk;                 // key rows
+  int d;                  // head dimension (64 or 128)
   int nt;                 // ceil(N / 128) query tiles per head
   float scale;            // S = scale * Q K^T
   float scale_log2;       // scale * log2(e)
@@ -57,9 +59,9 @@ struct FwdArgs {
   // to the workspace instead of O and lse, and a merge kernel combines them.
   int n_split;
   int nq_pad;             // query rows per head in the partial arrays (N rounded up to 128)
-  float *part_o;          // [n_split, B*H, nq_pad, 64] fp32
+  float *part_o;          // [n_split, B*H, nq_pad, d] fp32
   float *part_lse;        // [n_split, B*H, nq_pad] fp32, natural log
-  uint16_t *o;            // [B, H, N, 64] bf16, written by the merge kernel
+  uint16_t *o;            // [B, H, N, d] bf16, written by the merge kernel
 };
 
 struct BwdArgs {
@@ -118,6 +120,12 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st);
+// The same two entry points for d = 128 (fa_fwd_d128.cu); the tensor maps
+// have 128 x 64 boxes, two per tile.
+cudaError_t launch_fwd_d128(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
+cudaError_t launch_fwd_splitkv_d128(const CUtensorMap &tq, const CUtensorMap &tk,
+                                    const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st);
 
 // ev_start / ev_stop (may be null) are recorded around the main kernel.
 // tdq_acc: the fp32 dQ accumulators [B*H*n_pad, 64] as a 2-D map with 128 x 32

@@ -75,7 +75,8 @@ def _fwd_status(fa, **kw):
     (dict(q=None), -1), (dict(lse=None), -1), (dict(B=0), -1), (dict(N=0), -1),
     (dict(H=-1), -1), (dict(scale=0.0), -1), (dict(scale=-1.0), -1),
     (dict(scale=float("inf")), -1), (dict(scale=float("nan")), -1),
-    (dict(d=128), -2), (dict(d=32), -2), (dict(N=1 << 20, block_mask=FAKE), -2),
+    (dict(d=96), -2), (dict(d=32), -2), (dict(d=256), -2), (dict(N=1 << 20, block_mask=FAKE), -2),
+    (dict(d=128, lse=FAKE + 4), -3),  # d = 128 passes the head-dim check (forward only)
     (dict(k=FAKE + 8), -3), (dict(lse=FAKE + 4), -3),
     (dict(B=1 << 16, H=1 << 16, N=1), -1), (dict(N=65535 * 128 + 1), -2),
 ])
@@ -112,25 +113,23 @@ def test_product_path_never_touches_the_oracle():
     assert not bad, bad
 
 
-def _fwd_drop_status(fa, p, N=128, seed=1):
+def _fwd_drop_status(fa, p, N=128, seed=1, lse=FAKE):
     L = fa.lib()
-    return L.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, N, 64, 0.125, 0, None, None,
+    return L.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, lse, 1, 1, N, 64, 0.125, 0, None, None,
                             p, seed, None)
 
 
 @pytest.mark.parametrize("p,N,status", [
     (-0.1, 128, -1), (1.0, 128, -1), (1.5, 128, -1), (float("nan"), 128, -1),
-    (float("inf"), 128, -1), (0.1, 131072 + 1, -2), (0.0, 131072 + 1, -4),
+    (float("inf"), 128, -1), (0.1, 131072 + 1, -2), (0.0, 131072 + 1, -3),
 ])
 def test_dropout_validation_without_gpu(fa_lib, p, N, status):
     """Bad drop probabilities are rejected before anything else happens; a
     positive one needs N <= 131072; p = 0 is plain attention at any N (here it
-    gets as far as the missing device)."""
-    got = _fwd_drop_status(fa_lib, p, N)
-    if status == -4:
-        assert got in (-2, -4)   # no GPU here: device setup fails
-    else:
-        assert got == status
+    gets as far as the alignment check, which a misaligned lse fails: no call
+    of this test reaches a device)."""
+    got = _fwd_drop_status(fa_lib, p, N, lse=FAKE + 4)
+    assert got == status
     L = fa_lib.lib()
     need = fa_lib.fa_bwd_workspace_size(1, 1, 128, 64)
     if status in (-1,):
@@ -152,9 +151,11 @@ def test_splitkv_workspace_and_validation_without_gpu(fa_lib):
             S_eff = S
         S_eff = max(1, min(S_eff, nk_t))
         rows = S_eff * B * H * nq_pad
-        want = up(up(rows * 64 * 4) + rows * 4)
-        assert fa_lib.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, 64, S) == want, (B, H, Nq, Nk, S)
-    assert fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 128, 0) == 0
+        for d in (64, 128):
+            want = up(up(rows * d * 4) + rows * 4)
+            got = fa_lib.fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, S)
+            assert got == want, (B, H, Nq, Nk, S, d)
+    assert fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 96, 0) == 0
     assert fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 64, 2000) == 0
     L = fa_lib.lib()
     need = fa_lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 256, 64, 0)
@@ -169,6 +170,8 @@ def test_splitkv_workspace_and_validation_without_gpu(fa_lib):
     assert call(Nq=0) == -1 and call(Nk=0) == -1
     assert call(scale=-1.0) == -1
     assert call(S=-1) == -1 and call(S=1025) == -1
-    assert call(d=128) == -2
+    assert call(d=96) == -2
+    assert call(d=128, nbytes=need) == -6   # the d = 128 partials need twice the bytes
+    assert call(d=128, o=FAKE + 8) == -3
     assert call(o=FAKE + 8) == -3
     assert call(ws=None) == -6 and call(nbytes=need - 1) == -6

@@ -1,0 +1,140 @@
+"""GPU parity of the head-dimension-128 forward (fa_fwd, fa_fwd_dropout and
+fa_fwd_splitkv with d = 128) against the fp64 oracle, which takes any d.
+Same tolerances as d = 64; masks, ragged tails, empty rows and the lazy
+rescale under peaky keys are covered as for d = 64."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+D = 128
+
+
+@pytest.fixture(scope="module")
+def H(fa_lib, oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gpu_harness
+    return gpu_harness
+
+
+def _full(H, oracle, x):
+    o, lse = H.run_fwd(x)
+    o_ref, lse_ref = oracle.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
+                                    **x.oracle_kwargs())
+    H.assert_o(H.host_f64(o), o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d128_tiny(H, oracle_mod, causal):
+    import workloads as W
+    _full(H, oracle_mod, H.Inputs(W.make("tiny", d=D, B=2, H=2, causal=causal)))
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 129, 300, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d128_ragged(H, oracle_mod, N, causal):
+    """Several tiles with a ragged tail (and N = 1, a single key)."""
+    import workloads as W
+    _full(H, oracle_mod, H.Inputs(W.make("tiny", seed=10 + N, d=D, B=1, H=3, N=N,
+                                         causal=causal)))
+
+
+def test_d128_key_padding(H, oracle_mod):
+    """BERT-shaped key padding, with lengths 0 (O = 0, lse = -inf), 1 and a
+    tile edge."""
+    import workloads as W
+    w = W.make("bert", d=D, B=4, H=2)
+    x = H.Inputs(w, kv_len=np.array([0, 1, 128, 437], np.int32))
+    o, lse = _full(H, oracle_mod, x)
+    assert torch.all(o[0].float() == 0) and torch.all(torch.isinf(lse[0]))
+
+
+def test_d128_block_sparse_with_an_empty_row(H, oracle_mod):
+    import workloads as W
+    w = W.make("tiny", seed=21, d=D, B=1, H=2, N=1024)
+    rng = np.random.default_rng(22)
+    mask = (rng.random((8, 8)) < 0.4).astype(np.uint8)
+    mask[3, :] = 0                              # query tile 3 attends nothing
+    np.fill_diagonal(mask[4:, 4:], 1)
+    for causal in (False, True):
+        x = H.Inputs(w, causal=causal, block_mask=mask)
+        o, lse = _full(H, oracle_mod, x)
+        assert torch.all(o[:, :, 384:512].float() == 0)
+
+
+def test_d128_all_ones_mask_equals_dense(H, oracle_mod):
+    import workloads as W
+    w = W.make("tiny", seed=23, d=D, B=1, H=2, N=1024)
+    o1, l1 = H.run_fwd(H.Inputs(w))
+    o2, l2 = H.run_fwd(H.Inputs(w, block_mask=np.ones((8, 8), np.uint8)))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_d128_long_causal_peaky_sampled_rows(H, oracle_mod):
+    """The long-context causal workload at d = 128 (peaky keys stress the
+    lazy rescale), checked on 256 sampled query rows per head."""
+    import workloads as W
+    w = W.make("gpt2_4k", d=D, B=1, H=4)
+    x = H.Inputs(w)
+    o, lse = H.run_fwd(x)
+    rng = np.random.default_rng(24)
+    rows = W.sample_rows(rng, 1, 4, w.spec.N, 256)
+    o_ref, lse_ref = oracle_mod.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
+                                        rows=rows, **x.oracle_kwargs())
+    H.assert_o(H.host_f64(o).reshape(-1, D)[rows], o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64).reshape(-1)[rows], lse_ref)
+
+
+@pytest.mark.parametrize("p,seed", [(0.1, 5), (0.5, 2**33 + 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d128_dropout_forward(H, oracle_mod, p, seed, causal):
+    import workloads as W
+    x = H.Inputs(W.make("tiny", seed=30, d=D, B=2, H=2, N=300, causal=causal))
+    o, lse = H.run_fwd_dropout(x, p, seed)
+    o_ref, lse_ref = oracle_mod.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
+                                        p8=oracle_mod.drop_p8(p), seed=seed,
+                                        **x.oracle_kwargs())
+    H.assert_o(H.host_f64(o), o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+
+
+@pytest.mark.parametrize("Nq,Nk,S", [(1, 8192, 0), (1, 8192, 7), (16, 1000, 0), (200, 333, 3),
+                                     (3, 1, 0)])
+def test_d128_splitkv(H, oracle_mod, Nq, Nk, S):
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    rng = np.random.default_rng(40 + Nq)
+    B, Hh = 2, 4
+    q, k, v = (W.f32_to_bf16_bits(rng.standard_normal((B, Hh, n, D), dtype=np.float32))
+               for n in (Nq, Nk, Nk))
+    kv_len = np.array([Nk, max(0, Nk // 3)], np.int32)
+    dq, dk, dv = (H.dev_bf16(t) for t in (q, k, v))
+    o = H.nan_like_bf16((B, Hh, Nq, D))
+    lse = torch.full((B, Hh, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    kl = torch.from_numpy(kv_len).cuda()
+    nbytes = fa.fa_fwd_splitkv_workspace_size(B, Hh, Nq, Nk, D, S)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    fa.fa_fwd_splitkv(dq, dk, dv, o, lse, B, Hh, Nq, Nk, D, 0.125, kl, S, ws, nbytes, st)
+    fa.fa_check(st)
+    o_ref, lse_ref = oracle_mod.forward_qk(W.bf16_bits_to_f64(q), W.bf16_bits_to_f64(k),
+                                           W.bf16_bits_to_f64(v), 0.125, kv_len=kv_len)
+    H.assert_o(H.host_f64(o), o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+
+
+def test_d128_backward_is_reported_unsupported(H):
+    import exact_io_aware_25_gb300 as fa
+    assert fa.fa_bwd_workspace_size(1, 1, 128, D) == 0
+    t = torch.zeros((1, 1, 128, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_bwd(t, t, t, t, lse, t, t, t, t, 1, 1, 128, D, 0.125, workspace=lse,
+                  workspace_bytes=512)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED

@@ -1,4 +1,4 @@
-"""The forward kernel's FMA-pipe exponential (exp2_poly in fa_fwd.cu): its
+"""The forward kernels' FMA-pipe exponential (exp2_poly in fa_fwd_common.cuh): its
 coefficients match the generator, and the float32 algorithm (round-to-
 nearest split by the 1.5*2^23 trick, degree-4 polynomial on [-1/2, 1/2],
 exponent-field add) stays within its stated error bound against 2^x."""
@@ -13,7 +13,7 @@ CSRC = os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc")
 
 
 def kernel_coefficients():
-    text = open(os.path.join(CSRC, "fa_fwd.cu")).read()
+    text = open(os.path.join(CSRC, "fa_fwd_common.cuh")).read()
     body = text[text.index("float exp2_poly(float x)"):]
     vals = dict(re.findall(r"\b(c[0-4]) = ([-+0-9.e]+)f", body[:600]))
     return np.array([float(vals[f"c{i}"]) for i in range(5)], np.float32)
