@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int j = tile_at(s, sparse, it);
-      if (!mbar_wait_warp(&s.bar_s_full, it & 1, pr.wait, &s.abort)) {
+      if (!mbar_wait_warp_fast(&s.bar_s_full, it & 1, pr.wait, &s.abort)) {
         ok = false;
         break;
       }
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);  // exact zeros where masked
         else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
         if (half == 0 && it > 0) {
-          if (!mbar_wait_warp(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
+          if (!mbar_wait_warp_fast(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
             ok = false;
             break;
           }

@@ -12,15 +12,17 @@
 //            V_j (2-stage ring).  Each 128 x 128 bf16 tile is two 128 x 64
 //            boxes (the 128-byte swizzle spans 64 bf16), 16 KiB apart.
 //   warp 5   TMEM owner and MMA issuer: S_j = Q K_j^T (M=128, N=128, K=128)
-//            into one of two S buffers, and O += P~_j V_j (M=128, N=128,
-//            K=128) with P~_j from one of two P~ buffers in TMEM.  S_{j+2}
-//            is issued as soon as the softmax has pulled S_j into registers,
-//            ahead of PV_j, so the next S is always ready when the softmax
-//            finishes a tile.
+//            into S buffer j & 1, and O += P~_j V_j (M=128, N=128, K=128)
+//            with P~_j from P~ buffer j & 1 in TMEM.  Per tile j it waits
+//            for P~_j, issues PV_j and then S_{j+2} into S_j's buffer, so
+//            the commit that announces S_{j+2} also covers PV_j: when the
+//            softmax sees S_{j+2} ready, P~ buffer j & 1 is free again, and
+//            the softmax has no other barrier to pass per tile.  S_{j+1} is
+//            computed while the softmax works on S_j.
 //   warps 0-3 softmax: thread t owns query row t; as in the d = 64 kernel,
-//            except that the P~ store waits only for PV_{j-2} (the other
-//            buffer's reader) and the O rescale, when the lazily moved max
-//            requires one, waits for PV_{j-1}.
+//            with one wait (S_j ready) and one arrival (P~_j stored) per
+//            tile; the O rescale, when the lazily moved max requires one,
+//            first waits for PV_{j-1}.
 // TMEM columns: S buffers 0-127 and 128-255, P~ buffers 256-319 and
 // 320-383 (bf16 pairs), O accumulator 384-511.
 #include "fa_kernels.cuh"
@@ -46,7 +48,6 @@ struct __align__(1024) Fwd128Smem {
   uint64_t bar_v_full[kVStages];
   uint64_t bar_v_empty[kVStages];
   uint64_t bar_s_full[2];
-  uint64_t bar_s_free[2];
   uint64_t bar_p_full[2];
   uint64_t bar_o_done[2];
   uint64_t bar_final;
@@ -102,7 +103,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.bar_s_full[i], 1);
-      mbar_init(&s.bar_s_free[i], kSoftmaxWarps);
       mbar_init(&s.bar_p_full[i], kSoftmaxWarps);
       mbar_init(&s.bar_o_done[i], 1);
     }
@@ -196,11 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; ok && it < n; ++it) {
         const int bf = it & 1;
         const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-        if (it + 2 < n) {
-          // the softmax has copied S_it into registers: its buffer takes S_{it+2}
-          if (!mbar_wait_warp(&s.bar_s_free[bf], ph, pr.wait, &s.abort)) break;
-          if (!issue_s(it + 2)) break;
-        }
+        // P~_it stored (so S_it has been read into registers as well)
         if (!mbar_wait_warp(&s.bar_p_full[bf], ph, pr.wait, &s.abort)) break;
         const int st = it % kVStages;
         if (!mbar_wait_warp(&s.bar_v_full[st], (it / kVStages) & 1, pr.wait, &s.abort)) break;
@@ -216,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts_w(tmem + kColO, pa + kk * 8, d_v + kk * 128, idesc_o, kk > 0 ? 1u : acc0);
         mma_commit_w(&s.bar_o_done[bf]);
         mma_commit_w(&s.bar_v_empty[st]);
+        // S_{it+2} into S_it's buffer, behind PV_it
+        if (it + 2 < n && !issue_s(it + 2)) break;
       }
     }
     mma_commit_w(&s.bar_final);
@@ -240,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bf = it & 1;
       const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
       const int j = tile_at(s, sparse, it);
-      if (!mbar_wait_warp(&s.bar_s_full[bf], ph, pr.wait, &s.abort)) {
+      // S_it ready; PV_{it-2}, the last reader of P~ buffer bf, has completed
+      if (!mbar_wait_warp_fast(&s.bar_s_full[bf], ph, pr.wait, &s.abort)) {
         ok = false;
         break;
       }
@@ -257,9 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.bar_s_free[bf]);
       const int key0 = j * kTile;
       const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
       if (edge) mask_row(sv, kv_bound - key0, pr.causal ? (qrow - key0) : kTile);
@@ -279,17 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
         if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
         else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
-        if (half == 0 && it >= 2) {
-          // PV_{it-2} read this P~ buffer
-          if (!mbar_wait_warp(&s.bar_o_done[bf], ph ^ 1u, pr.wait, &s.abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         tmem_st32(p_base + half * 32, pk);
       }
-      if (!ok) break;
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O must hold every PV up to it-1 before it is rescaled

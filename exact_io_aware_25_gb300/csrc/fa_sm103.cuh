@@ -96,6 +96,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Non-blocking probe of the phase (no suspend): the cheap first test for a
+// wait whose phase has usually completed already.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Same bound, but not cut short by the abort flag: used for the final drain
 // of in-flight tensor-core work before TMEM is released.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, const WaitCtl &w) {
@@ -116,6 +130,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const WaitCtl &w,
                                                volatile int *abort) {
   const bool ok = mbar_wait(bar, parity, w, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// mbar_wait_warp for a phase that has usually completed: one non-blocking
+// probe first, then the bounded suspending wait.
+__device__ __forceinline__ bool mbar_wait_warp_fast(uint64_t *bar, uint32_t parity,
+                                                    const WaitCtl &w, volatile int *abort) {
+  const bool ok = mbar_test_wait(smem_u32(bar), parity) || mbar_wait(bar, parity, w, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
