@@ -91,8 +91,11 @@ def _load():
                                                   u8p, ci, ci, u64, i64p, cl, i64p, cl, dp, dp,
                                                   dp, ci]
             lib.fa_oracle_bwd_dropout.restype = ci
-            lib.fa_oracle_fwd_qk.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, i32p, i64p, cl,
-                                             dp, dp, ci]
+            lib.fa_oracle_fwd_qk.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, ci, i32p, i64p,
+                                             cl, dp, dp, ci]
+            lib.fa_oracle_fwd_stats.argtypes = [dp, dp, dp, ci, ci, ci, ci, cd, ci, i32p, u8p,
+                                                ci, i64p, cl, dp, dp, dp, dp, ci]
+            lib.fa_oracle_fwd_stats.restype = ci
             lib.fa_oracle_fwd_qk.restype = ci
             lib.fa_oracle_keep.argtypes = [u64, ci, ci, ci, ci]
             lib.fa_oracle_keep.restype = ci
@@ -177,9 +180,10 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=Non
     return o, lse
 
 
-def forward_qk(q, k, v, scale, kv_len=None, rows=None, nthreads=None):
+def forward_qk(q, k, v, scale, kv_len=None, rows=None, nthreads=None, causal=False):
     """Forward with Nq query rows and Nk key rows (q [B, H, Nq, d]; k, v
-    [B, H, Nk, d]; no causal, no block mask).  Returns (o, lse) like forward,
+    [B, H, Nk, d]; no block mask; causal keeps key j for query i iff
+    j <= i + Nk - Nq, bottom-right aligned).  Returns (o, lse) like forward,
     row ids bh * Nq + i."""
     lib = _load()
     B, H, Nq, d = _shape(q)
@@ -192,13 +196,40 @@ def forward_qk(q, k, v, scale, kv_len=None, rows=None, nthreads=None):
     nrows = B * H * Nq if rows is None else len(ra)
     o = np.zeros((nrows, d), np.float64)
     lse = np.zeros((nrows,), np.float64)
-    rc = lib.fa_oracle_fwd_qk(qp, kp, vp, B, H, Nq, Nk, d, float(scale), klp, rp, nrows,
-                              _f64(o)[1], _f64(lse)[1], _threads(nthreads))
+    rc = lib.fa_oracle_fwd_qk(qp, kp, vp, B, H, Nq, Nk, d, float(scale), int(bool(causal)), klp,
+                              rp, nrows, _f64(o)[1], _f64(lse)[1], _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"fa_oracle_fwd_qk failed ({rc})")
     if rows is None:
         return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
     return o, lse
+
+
+def forward_stats(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=None,
+                  nthreads=None, block=BLOCK):
+    """forward() plus the row statistics: returns (o, lse, m, l) with
+    m_i = max_j s_ij and l_i = sum_j exp(s_ij - m_i) over the allowed keys
+    (-inf and 0 for a row without any)."""
+    lib = _load()
+    B, H, N, d = _shape(q)
+    qa, qp = _f64(q)
+    ka, kp = _f64(k)
+    va, vp = _f64(v)
+    kl, klp = _opt_i32(kv_len)
+    bm, bmp = _opt_u8(block_mask)
+    ra, rp = _opt_i64(rows)
+    nrows = B * H * N if rows is None else len(ra)
+    o = np.zeros((nrows, d), np.float64)
+    lse, m, l = (np.zeros((nrows,), np.float64) for _ in range(3))
+    rc = lib.fa_oracle_fwd_stats(qp, kp, vp, B, H, N, d, float(scale), int(bool(causal)), klp,
+                                 bmp, int(block), rp, nrows, _f64(o)[1], _f64(lse)[1],
+                                 _f64(m)[1], _f64(l)[1], _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"fa_oracle_fwd_stats failed ({rc})")
+    if rows is None:
+        return (o.reshape(B, H, N, d), lse.reshape(B, H, N), m.reshape(B, H, N),
+                l.reshape(B, H, N))
+    return o, lse, m, l
 
 
 def probs(q, k, scale, bh=0, causal=False, kv_len=None, block_mask=None, block=BLOCK):

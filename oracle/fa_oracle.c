@@ -47,10 +47,19 @@
  *
  * Layout: Q, K, V, dO, O, dQ, dK, dV are [B, H, N, d] row-major doubles;
  * lse is [B, H, N].  fa_oracle_fwd_qk allows a query length Nq different
- * from the key length Nk (Q, O [B, H, Nq, d]; K, V [B, H, Nk, d]; no causal
- * or block mask there): the same definition, row by row.  kv_len is int32[B] (NULL = N; values clamped to
- * [0, N]); block_mask is uint8[nb * nb], nb = ceil(N / blk), one mask shared
- * by every (b, h) (NULL = all ones).
+ * from the key length Nk (Q, O [B, H, Nq, d]; K, V [B, H, Nk, d]; no block
+ * mask there): the same definition, row by row.  Its causal mask is aligned
+ * to the bottom right: query i keeps key j iff j <= i + (Nk - Nq), so the
+ * last query sees every key and Nq == Nk is the top-left rule above (the
+ * pages fix only the square case; this is the reading for a query block
+ * that continues a longer key sequence).  kv_len is int32[B] (NULL = N;
+ * values clamped to [0, N]); block_mask is uint8[nb * nb], nb = ceil(N / blk),
+ * one mask shared by every (b, h) (NULL = all ones).
+ *
+ * fa_oracle_fwd_stats also returns the two row statistics the pages keep in
+ * HBM ([EXPL] "Method": the running max m and the exponential sum l of each
+ * row): m_i = max_j s_ij and l_i = sum_j exp(s_ij - m_i) over A_i
+ * (-inf and 0 for an empty row).
  */
 #include <math.h>
 #include <pthread.h>
@@ -64,6 +73,7 @@ typedef struct {
     int Nk;             /* key rows (= N except in fa_oracle_fwd_qk) */
     double scale;
     int causal;
+    int causal_off;     /* causal keeps j <= i + causal_off (Nk - Nq in fa_oracle_fwd_qk) */
     const int32_t *kv_len;
     const uint8_t *block_mask;
     int blk, nb;
@@ -80,6 +90,7 @@ static void problem_init(problem *p, const double *q, const double *k, const dou
     p->B = B; p->H = H; p->N = N; p->d = d;
     p->Nk = N;
     p->scale = scale; p->causal = causal;
+    p->causal_off = 0;
     p->kv_len = kv_len; p->block_mask = block_mask;
     p->blk = blk > 0 ? blk : 128;
     p->nb = (N + p->blk - 1) / p->blk;
@@ -133,7 +144,7 @@ static int key_bound(const problem *p, int b) {
 
 /* Is key j in A_i for batch b? */
 static int allowed(const problem *p, int b, int i, int j) {
-    if (p->causal && j > i) return 0;
+    if (p->causal && j > i + p->causal_off) return 0;
     if (j >= key_bound(p, b)) return 0;
     if (p->block_mask && !p->block_mask[(size_t)(i / p->blk) * p->nb + (size_t)(j / p->blk)])
         return 0;
@@ -259,6 +270,7 @@ typedef struct {
     const problem *p;
     const int64_t *rows; /* global row ids bh * N + i, or NULL = all */
     double *o, *lse;
+    double *m, *l;       /* optional row statistics */
 } fwd_ctx;
 
 static void fwd_item(void *vctx, int64_t item, double *s) {
@@ -268,6 +280,8 @@ static void fwd_item(void *vctx, int64_t item, double *s) {
     const int bh = (int)(g / p->N), i = (int)(g % p->N);
     double m, l;
     forward_row(p, bh, i, s, &m, &l, c->o + (size_t)item * p->d, c->lse + item);
+    if (c->m) c->m[item] = m;
+    if (c->l) c->l[item] = l;
 }
 
 /*
@@ -289,7 +303,23 @@ int fa_oracle_fwd_dropout(const double *q, const double *k, const double *v, int
     if (!rows) nrows = total;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= total) return -1;
-    fwd_ctx c = {&p, rows, o, lse};
+    fwd_ctx c = {&p, rows, o, lse, NULL, NULL};
+    return parallel_for(nrows, nthreads, (size_t)N, fwd_item, &c);
+}
+
+/* fa_oracle_fwd plus the row statistics m [nrows] and l [nrows]. */
+int fa_oracle_fwd_stats(const double *q, const double *k, const double *v, int B, int H,
+                        int N, int d, double scale, int causal, const int32_t *kv_len,
+                        const uint8_t *block_mask, int blk, const int64_t *rows, int64_t nrows,
+                        double *o, double *lse, double *m, double *l, int nthreads) {
+    if (!q || !k || !v || !o || !lse || !m || !l || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    problem p;
+    problem_init(&p, q, k, v, NULL, B, H, N, d, scale, causal, kv_len, block_mask, blk);
+    const int64_t total = (int64_t)B * H * N;
+    if (!rows) nrows = total;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= total) return -1;
+    fwd_ctx c = {&p, rows, o, lse, m, l};
     return parallel_for(nrows, nthreads, (size_t)N, fwd_item, &c);
 }
 
@@ -302,22 +332,24 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v, int B, int 
 }
 
 /*
- * Forward with a query length Nq and a key length Nk (no causal, no block
- * mask; kv_len clamped to [0, Nk]): q [B, H, Nq, d], k and v [B, H, Nk, d];
- * rows as in fa_oracle_fwd with ids bh * Nq + i; o [nrows, d], lse [nrows].
+ * Forward with a query length Nq and a key length Nk (no block mask; kv_len
+ * clamped to [0, Nk]; causal aligned to the bottom right, see the top of the
+ * file): q [B, H, Nq, d], k and v [B, H, Nk, d]; rows as in fa_oracle_fwd
+ * with ids bh * Nq + i; o [nrows, d], lse [nrows].
  */
 int fa_oracle_fwd_qk(const double *q, const double *k, const double *v, int B, int H, int Nq,
-                     int Nk, int d, double scale, const int32_t *kv_len, const int64_t *rows,
-                     int64_t nrows, double *o, double *lse, int nthreads) {
+                     int Nk, int d, double scale, int causal, const int32_t *kv_len,
+                     const int64_t *rows, int64_t nrows, double *o, double *lse, int nthreads) {
     if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
     problem p;
-    problem_init(&p, q, k, v, NULL, B, H, Nq, d, scale, 0, kv_len, NULL, 128);
+    problem_init(&p, q, k, v, NULL, B, H, Nq, d, scale, causal, kv_len, NULL, 128);
     p.Nk = Nk;
+    p.causal_off = Nk - Nq;
     const int64_t total = (int64_t)B * H * Nq;
     if (!rows) nrows = total;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= total) return -1;
-    fwd_ctx cx = {&p, rows, o, lse};
+    fwd_ctx cx = {&p, rows, o, lse, NULL, NULL};
     return parallel_for(nrows, nthreads, (size_t)Nk, fwd_item, &cx);
 }
 

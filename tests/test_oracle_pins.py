@@ -510,3 +510,114 @@ def test_short_queries_special_cases(oracle_mod):
     np.testing.assert_allclose(o0, np.broadcast_to(vv.mean(axis=2, keepdims=True), o0.shape),
                                rtol=0, atol=1e-13)
     np.testing.assert_allclose(l0, np.log(Nk), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- Nq != Nk with a causal mask
+
+
+def test_bottom_right_causal_square_case_is_the_top_left_rule(oracle_mod):
+    """Nq == Nk: the bottom-right alignment (j <= i + Nk - Nq) is j <= i,
+    the causal rule of the square forward."""
+    rng = np.random.default_rng(50)
+    B, H, N, d = 2, 2, 19, 5
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    kv_len = np.array([19, 7], np.int32)
+    o, lse = oracle_mod.forward_qk(q, k, vv, 0.4, kv_len=kv_len, causal=True)
+    o2, lse2 = oracle_mod.forward(q, k, vv, 0.4, causal=True, kv_len=kv_len)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 9), (4, 9), (9, 9), (12, 9)])
+def test_bottom_right_causal_closed_form(oracle_mod, Nq, Nk):
+    """Q = 0: every allowed key has score 0, so o_i is the mean of v_j over
+    j <= i + Nk - Nq and lse_i = ln(i + Nk - Nq + 1); rows with no key
+    (i < Nq - Nk) get o = 0 and lse = -inf.  The last query sees all keys."""
+    rng = np.random.default_rng(51)
+    B, H, d = 1, 2, 3
+    k, vv = _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d)
+    o, lse = oracle_mod.forward_qk(np.zeros((B, H, Nq, d)), k, vv, 0.7, causal=True)
+    for i in range(Nq):
+        n_allowed = min(Nk, max(0, i + Nk - Nq + 1))
+        if n_allowed == 0:
+            assert np.all(o[:, :, i] == 0) and np.all(np.isneginf(lse[:, :, i]))
+            continue
+        np.testing.assert_allclose(o[:, :, i], vv[:, :, :n_allowed].mean(axis=2), rtol=0,
+                                   atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, i], math.log(n_allowed), rtol=0, atol=1e-14)
+
+
+def test_bottom_right_causal_against_numpy_softmax(oracle_mod):
+    """Brute force with numpy on a tiny case: the mask j <= i + Nk - Nq
+    written out, softmax and product by V."""
+    rng = np.random.default_rng(52)
+    B, H, Nq, Nk, d, scale = 1, 2, 6, 11, 4, 0.5
+    q, k, vv = _rand(rng, B, H, Nq, d), _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d)
+    o, lse = oracle_mod.forward_qk(q, k, vv, scale, causal=True)
+    s = scale * np.einsum("bhic,bhjc->bhij", q, k)
+    allowed = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    s = np.where(allowed, s, -np.inf)
+    mx = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - mx)
+    np.testing.assert_allclose(o, np.einsum("bhij,bhjc->bhic", e / e.sum(-1, keepdims=True), vv),
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, (mx + np.log(e.sum(-1, keepdims=True)))[..., 0], rtol=1e-12,
+                               atol=1e-13)
+
+
+# ---------------------------------------------------------------- row statistics (m, l)
+
+
+@pytest.mark.parametrize("v", VARIANTS)
+def test_row_statistics_against_numpy(oracle_mod, v):
+    """m_i = max over the allowed keys of s_ij and l_i = sum exp(s_ij - m_i),
+    recomputed with numpy from a mask written out here; the forward's o and
+    lse are unchanged by asking for them."""
+    rng = np.random.default_rng(60)
+    B, H, N, d, scale, blk = 2, 2, 23, 4, 0.45, 8
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    causal = v.get("causal", False)
+    kv_len = np.array([23, 9], np.int32) if v.get("kv_len") else None
+    mask = _mask_for(rng, N, blk) if v.get("mask") else None
+    o, lse, m, l = oracle_mod.forward_stats(q, k, vv, scale, causal=causal, kv_len=kv_len,
+                                            block_mask=mask, block=blk)
+    o2, lse2 = oracle_mod.forward(q, k, vv, scale, causal=causal, kv_len=kv_len,
+                                  block_mask=mask, block=blk)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    s = scale * np.einsum("bhic,bhjc->bhij", q, k)
+    i, j = np.arange(N)[:, None], np.arange(N)[None, :]
+    for b in range(B):
+        allowed = np.ones((N, N), bool)
+        if causal:
+            allowed &= j <= i
+        if kv_len is not None:
+            allowed &= j < kv_len[b]
+        if mask is not None:
+            allowed &= mask[i // blk, j // blk] != 0
+        sb = np.where(allowed, s[b], -np.inf)
+        m_ref = sb.max(axis=-1)
+        for h in range(H):
+            for r in range(N):
+                if not np.isfinite(m_ref[h, r]):
+                    assert np.isneginf(m[b, h, r]) and l[b, h, r] == 0
+                    continue
+                # same scores up to the summation order of the dot products
+                np.testing.assert_allclose(m[b, h, r], m_ref[h, r], rtol=1e-14, atol=1e-15)
+                np.testing.assert_allclose(l[b, h, r], np.exp(sb[h, r] - m_ref[h, r]).sum(),
+                                           rtol=1e-12)
+    fin = np.isfinite(m)
+    np.testing.assert_allclose(lse[fin], m[fin] + np.log(l[fin]), rtol=0, atol=1e-13)
+
+
+def test_row_statistics_special_cases(oracle_mod):
+    """Causal row 0 has one key: m = s_00, l = 1.  Q = 0: m = 0, l = |A_i|."""
+    rng = np.random.default_rng(61)
+    B, H, N, d = 1, 1, 10, 3
+    q, k, vv = (_rand(rng, B, H, N, d) for _ in range(3))
+    _, _, m, l = oracle_mod.forward_stats(q, k, vv, 0.8, causal=True)
+    assert math.isclose(m[0, 0, 0], 0.8 * float(q[0, 0, 0] @ k[0, 0, 0]), rel_tol=1e-14)
+    assert l[0, 0, 0] == 1.0
+    _, _, m0, l0 = oracle_mod.forward_stats(np.zeros_like(q), k, vv, 0.8, causal=True)
+    assert np.all(m0 == 0)
+    np.testing.assert_array_equal(l0[0, 0], np.arange(1, N + 1))
