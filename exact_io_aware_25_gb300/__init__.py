@@ -76,6 +76,19 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, ci, vp,
                                          sz, vp]
             L.fa_fwd_splitkv.restype = ci
+            L.fa_fwd_stats.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp,
+                                       vp, vp]
+            L.fa_fwd_stats.restype = ci
+            L.fa_fwd_csr.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp, vp, vp, ci,
+                                     vp]
+            L.fa_fwd_csr.restype = ci
+            L.fa_bwd_csr_workspace_size.argtypes = [ci, ci, ci, ci]
+            L.fa_bwd_csr_workspace_size.restype = sz
+            L.fa_bwd_csr.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci,
+                                     vp, vp, vp, ci, vp, sz, vp]
+            L.fa_bwd_csr.restype = ci
+            L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp]
+            L.fa_fwd_qk.restype = ci
             L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                          ci, vp, vp, vp]
             L.fa_bwd_noalloc.restype = ci
@@ -181,6 +194,52 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, kv_len=None, num_spl
                                 int(Nq), int(Nk), int(d), float(scale), _ptr(kv_len),
                                 int(num_splits), _ptr(workspace), int(workspace_bytes),
                                 _stream(stream)), "fa_fwd_splitkv")
+
+
+def fa_fwd_stats(q, k, v, o, lse, row_max, row_sum, B, H, N, d, scale, causal=0, kv_len=None,
+                 block_mask=None, stream=None) -> None:
+    """fa_fwd that also writes the row statistics m (row max of scale*QK^T)
+    and l (sum of exp(s - m)) as fp32 [B, H, N]."""
+    _check(lib().fa_fwd_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(row_max),
+                              _ptr(row_sum), int(B), int(H), int(N), int(d), float(scale),
+                              int(bool(causal)), _ptr(kv_len), _ptr(block_mask),
+                              _stream(stream)), "fa_fwd_stats")
+
+
+def fa_fwd_csr(q, k, v, o, lse, B, H, N, d, scale, causal=0, kv_len=None, row_ptr=None,
+               col_idx=None, nnz=0, stream=None) -> None:
+    """fa_fwd with the block mask as CSR over query tiles (device int32
+    row_ptr [nb + 1] and col_idx [nnz])."""
+    _check(lib().fa_fwd_csr(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                            int(N), int(d), float(scale), int(bool(causal)), _ptr(kv_len),
+                            _ptr(row_ptr), _ptr(col_idx), int(nnz), _stream(stream)),
+           "fa_fwd_csr")
+
+
+def fa_bwd_csr_workspace_size(B, H, N, d) -> int:
+    return int(lib().fa_bwd_csr_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def fa_bwd_csr(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0, kv_len=None,
+               row_ptr=None, col_idx=None, nnz=0, workspace=None, workspace_bytes=0,
+               stream=None) -> None:
+    """Backward of fa_fwd_csr (workspace of fa_bwd_csr_workspace_size bytes)."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_csr(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                            _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
+                            int(bool(causal)), _ptr(kv_len), _ptr(row_ptr), _ptr(col_idx),
+                            int(nnz), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "fa_bwd_csr")
+
+
+def fa_fwd_qk(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal=0, kv_len=None,
+              stream=None) -> None:
+    """Forward of Nq query rows against Nk key rows; causal is aligned to the
+    bottom right (query i keeps key j iff j <= i + Nk - Nq)."""
+    _check(lib().fa_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                           int(Nq), int(Nk), int(d), float(scale), int(bool(causal)),
+                           _ptr(kv_len), _stream(stream)), "fa_fwd_qk")
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0,

@@ -227,30 +227,55 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
-                         int B, int H, int N, int d, float scale, int causal,
-                         const int32_t *kv_len, const uint8_t *block_mask, float p,
-                         unsigned long long seed, void *stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// Optional parts of a forward call beyond fa_fwd_dropout's arguments.
+struct FwdExtra {
+  float *row_m = nullptr, *row_l = nullptr;             // row statistics
+  const int32_t *csr_ptr = nullptr, *csr_idx = nullptr;  // CSR block mask
+  int csr_nnz = 0;
+  int Nk = 0;                                            // key rows (0: N)
+};
+
+fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int N, int d, float scale, int causal, const int32_t *kv_len,
+                   const uint8_t *block_mask, float p, unsigned long long seed,
+                   const FwdExtra &x, void *stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status st = validate_common(B, H, N, d, scale, block_mask, true);
   if (st != FA_OK) return st;
+  if (x.csr_ptr && (N + kTile - 1) / kTile > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
+  const int Nk = x.Nk > 0 ? x.Nk : N;
+  if (static_cast<long long>(B) * H * Nk >= (1LL << 31)) return FA_ERR_INVALID_ARG;
   const int p8 = drop_threshold(p);
   if (p8 < 0) return FA_ERR_INVALID_ARG;
-  if (p8 > 0 && N > kMaxDropN) return FA_ERR_UNSUPPORTED;
+  if (p8 > 0 && (N > kMaxDropN || Nk > kMaxDropN)) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if ((x.row_m && !aligned16(x.row_m)) || (x.row_l && !aligned16(x.row_l)))
     return FA_ERR_MISALIGNED;
   int dev = 0;
   int *err = nullptr;
   if ((st = device_setup(&dev, &err)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, N, d) ||
-      !encode_bhnd(&tv, v, BH, N, d) || !encode_bhnd(&to, o, BH, N, d))
+  if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, Nk, d) ||
+      !encode_bhnd(&tv, v, BH, Nk, d) || !encode_bhnd(&to, o, BH, N, d))
     return FA_ERR_CUDA;
   FwdArgs a{};
   a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
   a.pr.d = d;
+  a.pr.Nk = Nk;
+  a.pr.causal_off = Nk - N;
   a.lse = lse;
+  a.row_m = x.row_m;
+  a.row_l = x.row_l;
+  a.csr_ptr = x.csr_ptr;
+  a.csr_idx = x.csr_idx;
+  a.csr_nnz = x.csr_nnz;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     a.starve = g_starve_next;
@@ -262,11 +287,65 @@ fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, f
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// CSR block mask arguments: row_ptr [nb + 1] always, col_idx [nnz] when nnz > 0.
+fa_status validate_csr(const int32_t *row_ptr, const int32_t *col_idx, int nnz) {
+  if (!row_ptr || nnz < 0 || (nnz > 0 && !col_idx)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t *kv_len, const uint8_t *block_mask, float p,
+                         unsigned long long seed, void *stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, block_mask, p, seed,
+                  FwdExtra{}, stream);
+}
+
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                  int N, int d, float scale, int causal, const int32_t *kv_len,
                  const uint8_t *block_mask, void *stream) {
-  return fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, block_mask, 0.f, 0ull,
-                        stream);
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, block_mask, 0.f, 0ull,
+                  FwdExtra{}, stream);
+}
+
+fa_status fa_fwd_stats(const void *q, const void *k, const void *v, void *o, float *lse,
+                       float *row_max, float *row_sum, int B, int H, int N, int d, float scale,
+                       int causal, const int32_t *kv_len, const uint8_t *block_mask,
+                       void *stream) {
+  if (!row_max || !row_sum) return FA_ERR_INVALID_ARG;
+  FwdExtra x;
+  x.row_m = row_max;
+  x.row_l = row_sum;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, block_mask, 0.f, 0ull, x,
+                  stream);
+}
+
+fa_status fa_fwd_csr(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int N, int d, float scale, int causal, const int32_t *kv_len,
+                     const int32_t *row_ptr, const int32_t *col_idx, int nnz, void *stream) {
+  const fa_status st = validate_csr(row_ptr, col_idx, nnz);
+  if (st != FA_OK) return st;
+  FwdExtra x;
+  x.csr_ptr = row_ptr;
+  x.csr_idx = col_idx;
+  x.csr_nnz = nnz;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, nullptr, 0.f, 0ull, x,
+                  stream);
+}
+
+fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int H, int Nq, int Nk, int d, float scale, int causal, const int32_t *kv_len,
+                    void *stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  FwdExtra x;
+  x.Nk = Nk;
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, d, scale, causal, kv_len, nullptr, 0.f, 0ull, x,
+                  stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -377,6 +456,42 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                         block_mask, 0.f, 0ull, workspace, workspace_bytes, stream);
 }
 
+size_t fa_bwd_csr_workspace_size(int B, int H, int N, int d) {
+  if (validate_common(B, H, N, d, 1.f, nullptr) != FA_OK) return 0;
+  const size_t nt = (static_cast<size_t>(N) + kTile - 1) / kTile;
+  if (nt > static_cast<size_t>(kMaxMaskTiles)) return 0;
+  return ws_layout(B, H, N).total + align_up(nt * nt, 256);
+}
+
+fa_status fa_bwd_csr(const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                     int H, int N, int d, float scale, int causal, const int32_t *kv_len,
+                     const int32_t *row_ptr, const int32_t *col_idx, int nnz, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa_status st = validate_csr(row_ptr, col_idx, nnz);
+  if (st != FA_OK) return st;
+  if ((st = validate_common(B, H, N, d, scale, nullptr)) != FA_OK) return st;
+  const size_t need = fa_bwd_csr_workspace_size(B, H, N, d);
+  if (need == 0) return FA_ERR_UNSUPPORTED;  // more than 1024 tiles per row
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int *err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  // the dense copy of the mask sits after the backward's own workspace
+  const size_t own = ws_layout(B, H, N).total;
+  uint8_t *dense = static_cast<uint8_t *>(workspace) + own;
+  const int nb = (N + kTile - 1) / kTile;
+  if (launch_csr_to_dense(row_ptr, col_idx, nnz, nb, dense, err,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, kv_len,
+                        dense, 0.f, 0ull, workspace, own, stream);
+}
+
 fa_status fa_check(void *stream) {
   int dev = 0;
   int *err = nullptr;
@@ -389,7 +504,7 @@ fa_status fa_check(void *stream) {
     const int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return FA_ERR_CUDA;
-    return h == kDevTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+    return h == kDevTimeout ? FA_ERR_TIMEOUT : h == kDevBadArg ? FA_ERR_INVALID_ARG : FA_ERR_CUDA;
   }
   return FA_OK;
 }

@@ -873,4 +873,42 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   return launch_pdl(fa_bwd_dq_kernel, dq_grid, dim3(256), 0, st, a);
 }
 
+
+namespace {
+
+// CSR block mask -> dense nb x nb bytes; one CTA per query tile (row):
+// the row is cleared, then every in-range entry sets its byte.  Duplicate
+// entries write the same value.  Out-of-range rows or columns are skipped
+// and recorded as kDevBadArg.
+__global__ void __launch_bounds__(256) fa_csr_to_dense_kernel(const int32_t *row_ptr,
+                                                               const int32_t *col_idx, int nnz,
+                                                               int nb, uint8_t *dense, int *err) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x;
+  uint8_t *row = dense + static_cast<size_t>(r) * nb;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) row[j] = 0;
+  __syncthreads();
+  int beg = __ldg(row_ptr + r), end = __ldg(row_ptr + r + 1);
+  bool bad = false;
+  if (beg < 0 || end < beg || end > nnz) {
+    bad = true;
+    beg = end = 0;
+  }
+  for (int e = beg + static_cast<int>(threadIdx.x); e < end; e += blockDim.x) {
+    const int c = __ldg(col_idx + e);
+    if (c < 0 || c >= nb) bad = true;
+    else row[c] = 1;
+  }
+  if (bad) atomicCAS(err, 0, kDevBadArg);
+}
+
+}  // namespace
+
+cudaError_t launch_csr_to_dense(const int32_t *row_ptr, const int32_t *col_idx, int nnz, int nb,
+                                uint8_t *dense, int *err, cudaStream_t st) {
+  return launch_pdl(fa_csr_to_dense_kernel, dim3(nb), dim3(256), 0, st, row_ptr, col_idx, nnz, nb,
+                    dense, err);
+}
+
 }  // namespace fa

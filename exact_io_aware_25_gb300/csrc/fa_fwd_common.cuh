@@ -120,6 +120,49 @@ __device__ __forceinline__ int compact_mask_row(const uint8_t *row, int j_end, i
 }
 
 
+// Block-sparse from a CSR row: the entries col_idx[row_ptr[qt] ..
+// row_ptr[qt + 1]) of query tile qt are marked in a bitmap (any order;
+// duplicates merge), then the marked key tiles j < j_end are listed
+// ascending in tiles[] and counted, as compact_mask_row does for the dense
+// form.  A row range outside [0, nnz] or a tile index outside [0, nb) is
+// skipped and recorded as kDevBadArg.  One warp; bits holds ceil(nb / 32)
+// words of shared memory.
+__device__ __forceinline__ int compact_csr_row(const int32_t *row_ptr, const int32_t *col_idx,
+                                               int nnz, int qt, int nb, int j_end, uint32_t *bits,
+                                               int16_t *tiles, int lane, const WaitCtl &w) {
+  for (int i = lane; i < (nb + 31) / 32; i += 32) bits[i] = 0u;
+  __syncwarp();
+  int beg = __ldg(row_ptr + qt), end = __ldg(row_ptr + qt + 1);
+  bool bad = false;
+  if (beg < 0 || end < beg || end > nnz) {
+    bad = true;
+    beg = end = 0;
+  }
+  for (int e = beg + lane; e < end; e += 32) {
+    const int c = __ldg(col_idx + e);
+    if (c < 0 || c >= nb) bad = true;
+    else if (c < j_end) atomicOr(&bits[c >> 5], 1u << (c & 31));
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(w, kDevBadArg);
+  __syncwarp();
+  int count = 0;
+  for (int base = 0; base < j_end; base += 32) {
+    const int j = base + lane;
+    const bool keep = j < j_end && ((bits[base >> 5] >> lane) & 1u) != 0u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(j);
+    count += __popc(bal);
+  }
+  return count;
+}
+
+// Causal: one past the last key tile any row of query tile qt may see
+// (keys j <= i + off), clamped to the n_kv tiles below the key bound.
+__device__ __forceinline__ int causal_tile_end(int qt, int off, int n_kv) {
+  const int last = qt * kTile + kTile - 1 + off;
+  return last < 0 ? 0 : min(n_kv, last / kTile + 1);
+}
+
 // Split-KV merge ([MATH] §4: the softmax-weighted sum over the keys splits
 // into independent ranges whose (max, sum, output) states combine by
 // rescaling).  Each split s left O_s = (sum over its keys of P~ V) / l_s and

@@ -56,6 +56,7 @@ struct __align__(1024) Fwd128Smem {
   int n_tiles;
   int tile0;
   int16_t tiles[kMaxMaskTiles];
+  uint32_t bits[kMaxMaskTiles / 32];  // CSR block mask: the row's tiles as a bitmap
 };
 
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384, kTmemCols = 512;
@@ -83,13 +84,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / pr.H;
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
-  int j_begin = 0, j_end = pr.causal ? min(n_kv, qt + 1) : n_kv;
+  int j_begin = 0, j_end = pr.causal ? causal_tile_end(qt, pr.causal_off, n_kv) : n_kv;
   if (kSplit) {
     const int per = (n_kv + args.n_split - 1) / args.n_split;
     j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
     j_end = min(n_kv, j_begin + per);
   }
-  const bool sparse = pr.block_mask != nullptr;
+  const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
 
   if (tid == 0) {
     mbar_init(&s.bar_q, 1);
@@ -118,9 +119,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_o);
   }
   if (warp == 0) {
-    const int count = sparse ? compact_mask_row(pr.block_mask + static_cast<size_t>(qt) * pr.nt,
-                                                j_end, s.tiles, lane)
-                             : j_end - j_begin;
+    const int count =
+        !sparse ? j_end - j_begin
+        : args.csr_ptr
+            ? compact_csr_row(args.csr_ptr, args.csr_idx, args.csr_nnz, qt, pr.nt, j_end, s.bits,
+                              s.tiles, lane, pr.wait)
+            : compact_mask_row(pr.block_mask + static_cast<size_t>(qt) * pr.nt, j_end, s.tiles,
+                               lane);
     if (lane == 0) {
       s.n_tiles = count;
       s.tile0 = j_begin;
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = pr.scale_log2;
     float m = -INFINITY;
     float l = 0.f;
+    float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)
     RowDrop rd{0u, 0u, 0u};
     if (kDrop) {
       rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
@@ -257,10 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
       }
       const int key0 = j * kTile;
-      const bool edge = (key0 + kTile > kv_bound) || (pr.causal && j == qt);
-      if (edge) mask_row(sv, kv_bound - key0, pr.causal ? (qrow - key0) : kTile);
-      const float mx = row_max(sv);
-      const float m_cand = fmaxf(m, mx * sl2);
+      const bool edge =
+          (key0 + kTile > kv_bound) || (pr.causal && key0 + kTile - 1 > qt * kTile + pr.causal_off);
+      if (edge) mask_row(sv, kv_bound - key0, pr.causal ? (qrow + pr.causal_off - key0) : kTile);
+      const float mxs = row_max(sv) * sl2;
+      m_hi = fmaxf(m_hi, mxs);
+      const float m_cand = fmaxf(m, mxs);
       const bool bump = (m == -INFINITY) || (m_cand > m + kLazyRescale);
       const float m_ref = bump ? m_cand : m;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -358,6 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (qrow < pr.N) args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
         fence_proxy_async_smem();
+        if (args.row_m && qrow < pr.N) {
+          // the pages' row statistics: m = max_j s_ij, l = sum_j exp(s_ij - m)
+          const bool any = n > 0 && l > 0.f;
+          const size_t r = static_cast<size_t>(bh) * pr.N + qrow;
+          args.row_m[r] = any ? m_hi * 0.69314718055994531f : -INFINITY;
+          args.row_l[r] = any ? l * ex2_approx(m - m_hi) : 0.f;
+        }
       }
     }
     named_bar_sync(1, 128);

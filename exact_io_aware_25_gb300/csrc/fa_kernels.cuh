@@ -25,6 +25,7 @@ struct Problem {
   float scale;            // S = scale * Q K^T
   float scale_log2;       // scale * log2(e)
   int causal;
+  int causal_off;         // causal keeps key j for query i iff j <= i + causal_off (Nk - Nq)
   const int32_t *kv_len;  // device [B] or nullptr
   const uint8_t *block_mask;  // device [nt * nt] or nullptr
   WaitCtl wait;
@@ -62,6 +63,16 @@ struct FwdArgs {
   float *part_o;          // [n_split, B*H, nq_pad, d] fp32
   float *part_lse;        // [n_split, B*H, nq_pad] fp32, natural log
   uint16_t *o;            // [B, H, N, d] bf16, written by the merge kernel
+  // Optional row statistics (plain forward): row max m_i of S and the
+  // exponential sum l_i = sum_j exp(s_ij - m_i), fp32 [B, H, N].
+  float *row_m;
+  float *row_l;
+  // Block-sparse mask given as CSR over query tiles (instead of
+  // pr.block_mask): key tiles of query tile I are csr_idx[csr_ptr[I] ..
+  // csr_ptr[I + 1]), in any order, duplicates allowed.
+  const int32_t *csr_ptr;
+  const int32_t *csr_idx;
+  int csr_nnz;
 };
 
 struct BwdArgs {
@@ -115,6 +126,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 size_t fwd_smem_bytes();
 size_t bwd_smem_bytes();
+
+// Expands a CSR block mask (row_ptr [nb + 1], col_idx [nnz]) into the dense
+// nb x nb uint8 form (fa_bwd.cu); bad entries are skipped and recorded as
+// kDevBadArg in *err.
+cudaError_t launch_csr_to_dense(const int32_t *row_ptr, const int32_t *col_idx, int nnz, int nb,
+                                uint8_t *dense, int *err, cudaStream_t st);
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);

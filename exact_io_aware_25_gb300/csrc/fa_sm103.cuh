@@ -17,6 +17,7 @@ namespace fa {
 enum : int {
   kDevOk = 0,
   kDevTimeout = 1,
+  kDevBadArg = 2,   // a device-side argument (a CSR block mask) was out of range
 };
 
 struct WaitCtl {

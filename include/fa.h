@@ -14,7 +14,9 @@
  *     contiguous, so one (b, h) is a plain N x d operand of [EXPL] "Method".
  *   - All tensor pointers are DEVICE pointers owned by the caller, and must be
  *     16-byte aligned (TMA requirement).  The library never frees them.
- *   - d must be 64.  N >= 1, B >= 1, H >= 1, B*H*N < 2^31.
+ *   - d must be 64; the forward entry points (fa_fwd, fa_fwd_dropout,
+ *     fa_fwd_stats, fa_fwd_csr, fa_fwd_qk, fa_fwd_splitkv) also take d = 128.
+ *     N >= 1, B >= 1, H >= 1, B*H*N < 2^31.
  *   - scale multiplies Q K^T (S = scale * Q K^T); it must be finite and > 0.
  *   - causal != 0 keeps key j for query i iff j <= i (top-left aligned).
  *   - kv_len: NULL, or a DEVICE int32 array [B]; keys j >= kv_len[b] of batch b
@@ -51,8 +53,9 @@ extern "C" {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, non-finite or non-positive scale */
-    FA_ERR_UNSUPPORTED = -2,  /* d != 64, N > 65535 * 128, N > 1024 * 128 with a block
-                                 mask, N > 131072 with dropout, or no sm_103 device */
+    FA_ERR_UNSUPPORTED = -2,  /* d not 64 (or 128 in a forward), N > 65535 * 128,
+                                 N > 1024 * 128 with a block mask, N > 131072 with
+                                 dropout, or no sm_103 device */
     FA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     FA_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed */
     FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait ran out (reported by fa_check) */
@@ -156,7 +159,7 @@ FA_API fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, con
  * ([MATH] section 4: the softmax-weighted sum splits into independent key
  * ranges whose states combine by rescaling).  The result is the fa_fwd
  * result with Nq query rows and Nk key rows, no causal mask and no block
- * mask (kv_len as in fa_fwd, clamped to [0, Nk]).
+ * mask (kv_len as in fa_fwd, clamped to [0, Nk]).  d = 64 or 128.
  *   q              in : bf16 [B, H, Nq, d]
  *   k, v           in : bf16 [B, H, Nk, d]
  *   o              out: bf16 [B, H, Nq, d]
@@ -166,7 +169,7 @@ FA_API fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, con
  *   workspace      in : device scratch of >= fa_fwd_splitkv_workspace_size()
  *                       bytes (same num_splits), 16-byte aligned, caller-owned:
  *                       fp32 partial outputs and lse, S * B * H * ceil(Nq/128)
- *                       * 128 * 260 bytes.
+ *                       * 128 * (4 d + 4) bytes, each part rounded up to 256.
  */
 FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
@@ -203,11 +206,77 @@ FA_API fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, con
 FA_API size_t fa_bwd_noalloc_max_scratch_bytes(void);
 
 /*
+ * fa_fwd that also writes the two row statistics the pages keep in HBM
+ * ([EXPL] "Method" and "Key ideas": the running max m and the exponential
+ * sum l of every query row, from which the backward can rebuild P):
+ *   row_max  out: fp32 [B, H, N], m_i = max over the allowed keys of s_ij,
+ *                 s = scale * Q K^T (natural units, not base 2)
+ *   row_sum  out: fp32 [B, H, N], l_i = sum over the allowed keys of
+ *                 exp(s_ij - m_i)
+ * so that lse_i = m_i + ln l_i; a row with no allowed key gets m = -inf,
+ * l = 0.  Both pointers are required and 16-byte aligned.  Everything else
+ * as fa_fwd.
+ */
+FA_API fa_status fa_fwd_stats(const void *q, const void *k, const void *v, void *o, float *lse,
+                              float *row_max, float *row_sum, int B, int H, int N, int d,
+                              float scale, int causal, const int32_t *kv_len,
+                              const uint8_t *block_mask, void *stream);
+
+/*
+ * fa_fwd with the block-sparse mask given in compressed-row form instead of
+ * the dense nb x nb bytes ([EXPL] "Extension: Block-Sparse FlashAttention":
+ * only the nonzero blocks of the mask are evaluated; a CSR list of them is
+ * the same mask):
+ *   row_ptr  in : DEVICE int32 [nb + 1], nb = ceil(N / 128); row_ptr[0] = 0,
+ *                 non-decreasing, row_ptr[nb] = nnz
+ *   col_idx  in : DEVICE int32 [nnz]; the key tiles of query tile I are
+ *                 col_idx[row_ptr[I] .. row_ptr[I + 1]), in any order;
+ *                 repeated entries count once.  May be NULL when nnz = 0.
+ * A row range or tile index out of range is skipped and reported by
+ * fa_check as FA_ERR_INVALID_ARG (the values live on the device, so they are
+ * checked by the kernel, not before the launch).  N <= 1024 * 128.
+ */
+FA_API fa_status fa_fwd_csr(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t *kv_len, const int32_t *row_ptr,
+                            const int32_t *col_idx, int nnz, void *stream);
+
+/*
+ * Backward of fa_fwd_csr: the CSR mask is expanded into the dense form in
+ * the workspace, then fa_bwd runs with it.  The workspace is
+ * fa_bwd_csr_workspace_size() bytes: fa_bwd_workspace_size() plus nb * nb
+ * rounded up to 256.  Same errors as fa_fwd_csr and fa_bwd.
+ */
+FA_API size_t fa_bwd_csr_workspace_size(int B, int H, int N, int d);
+
+FA_API fa_status fa_bwd_csr(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t *kv_len, const int32_t *row_ptr,
+                            const int32_t *col_idx, int nnz, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * Forward of Nq query rows against Nk key rows (a query block that continues
+ * a longer key sequence, such as the new tokens of a decoder attending to
+ * their cache).  The pages fix only the square case; causal is aligned to
+ * the bottom right: query i keeps key j iff j <= i + (Nk - Nq), so the last
+ * query sees every key and Nq == Nk is fa_fwd's rule; query rows with
+ * i < Nq - Nk have no key and get O = 0, lse = -inf.  No block mask, no
+ * dropout; kv_len as in fa_fwd, clamped to [0, Nk].
+ *   q, o  : bf16 [B, H, Nq, d];  k, v : bf16 [B, H, Nk, d];  lse : fp32 [B, H, Nq]
+ */
+FA_API fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                           const int32_t *kv_len, void *stream);
+
+/*
  * Synchronises stream and reports the first device-side error recorded since
  * the previous fa_check: FA_ERR_TIMEOUT when a bounded wait inside a kernel
  * ran out (the kernel then returned early and its outputs are invalid),
- * FA_ERR_CUDA for an asynchronous CUDA error, FA_OK otherwise.  Clears the
- * recorded error.
+ * FA_ERR_INVALID_ARG when a kernel found a device-side argument out of range
+ * (a CSR block mask), FA_ERR_CUDA for an asynchronous CUDA error, FA_OK
+ * otherwise.  Clears the recorded error.
  */
 FA_API fa_status fa_check(void *stream);
 

@@ -175,3 +175,51 @@ def test_splitkv_workspace_and_validation_without_gpu(fa_lib):
     assert call(d=128, o=FAKE + 8) == -3
     assert call(o=FAKE + 8) == -3
     assert call(ws=None) == -6 and call(nbytes=need - 1) == -6
+
+
+def test_api_variant_validation_without_gpu(fa_lib):
+    """fa_fwd_stats, fa_fwd_csr, fa_fwd_qk and fa_bwd_csr reject bad arguments
+    on the host; every call here stops before the device (a misaligned
+    pointer is the last check passed arguments meet)."""
+    L = fa_lib.lib()
+
+    def stats(rm=FAKE, rs=FAKE, lse=FAKE, d=64):
+        return L.fa_fwd_stats(FAKE, FAKE, FAKE, FAKE, lse, rm, rs, 1, 1, 128, d, 0.125, 0, None,
+                              None, None)
+
+    assert stats(rm=None) == -1 and stats(rs=None) == -1
+    assert stats(rm=FAKE + 4) == -3 and stats(lse=FAKE + 4) == -3
+    assert stats(d=96) == -2
+    assert stats(d=128, rs=FAKE + 8) == -3
+
+    def csr(rp=FAKE, ci=FAKE, nnz=4, N=1000, lse=FAKE + 4, d=64):
+        return L.fa_fwd_csr(FAKE, FAKE, FAKE, FAKE, lse, 1, 1, N, d, 0.125, 0, None, rp, ci, nnz,
+                            None)
+
+    assert csr(rp=None) == -1 and csr(nnz=-1) == -1 and csr(ci=None) == -1
+    assert csr(ci=None, nnz=0) == -3             # no entries: col_idx may be NULL
+    assert csr(N=1024 * 128 + 1) == -2           # more than 1024 tiles per row
+    assert csr() == -3 and csr(d=128) == -3
+
+    def qk(Nq=5, Nk=300, d=64, lse=FAKE + 4):
+        return L.fa_fwd_qk(FAKE, FAKE, FAKE, FAKE, lse, 2, 3, Nq, Nk, d, 0.125, 1, None, None)
+
+    assert qk(Nk=0) == -1 and qk(Nq=0) == -1 and qk(d=32) == -2
+    assert qk() == -3 and qk(d=128) == -3 and qk(Nq=300, Nk=5) == -3
+
+    up = lambda x: -(-x // 256) * 256
+    for N in (1, 128, 1000, 65536):
+        nt = -(-N // 128)
+        want = fa_lib.fa_bwd_workspace_size(2, 3, N, 64) + up(nt * nt)
+        assert fa_lib.fa_bwd_csr_workspace_size(2, 3, N, 64) == want
+    assert fa_lib.fa_bwd_csr_workspace_size(1, 1, 1024 * 128 + 1, 64) == 0
+    assert fa_lib.fa_bwd_csr_workspace_size(1, 1, 128, 128) == 0
+    need = fa_lib.fa_bwd_csr_workspace_size(1, 1, 1000, 64)
+
+    def bcsr(rp=FAKE, ws=FAKE, nbytes=need, dq=FAKE):
+        return L.fa_bwd_csr(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, 1, 1, 1000, 64,
+                            0.125, 0, None, rp, FAKE, 3, ws, nbytes, None)
+
+    assert bcsr(rp=None) == -1
+    assert bcsr(nbytes=need - 1) == -6 and bcsr(ws=None) == -6
+    assert bcsr(dq=FAKE + 2) == -3
