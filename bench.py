@@ -57,7 +57,10 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "fa_bwd_main_kernel": ("fa_bwd.cu", "fa_sm103.cuh", "fa_kernels.cuh"),
-    "fa_fwd_kernel": ("fa_fwd.cu", "fa_sm103.cuh", "fa_kernels.cuh"),
+    "fa_fwd_kernel": ("fa_fwd.cu", "fa_fwd_common.cuh", "fa_sm103.cuh", "fa_kernels.cuh"),
+    "fa_bwd_d128_kernel": ("fa_bwd_d128.cu", "fa_sm103.cuh", "fa_kernels.cuh"),
+    "fa_fwd_d128_kernel": ("fa_fwd_d128.cu", "fa_fwd_common.cuh", "fa_sm103.cuh",
+                           "fa_kernels.cuh"),
 }
 
 
@@ -342,7 +345,7 @@ def run_ours(args, rank, world, local):
     fa.lib()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    w = W.make(args.workload)
+    w = W.make(args.workload) if args.head_dim == 64 else W.make(args.workload, d=args.head_dim)
     s = w.spec
     B, H, N, d = s.B, s.H, s.N, s.d
     fl = counted_flops(s, w.kv_len, w.block_mask)
@@ -425,9 +428,13 @@ def run_ours(args, rank, world, local):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     fwd_avg = statistics.mean(fwd_ms) / 1e3
     bwd_avg = statistics.mean(bwd_main_ms) / 1e3
-    dominant = "fa_bwd_main_kernel" if bwd_avg >= fwd_avg else "fa_fwd_kernel"
-    dom_flops = fl["bwd"] if dominant == "fa_bwd_main_kernel" else fl["fwd"]
-    dom_t = bwd_avg if dominant == "fa_bwd_main_kernel" else fwd_avg
+    bwd_dominant = bwd_avg >= fwd_avg
+    if d == 64:
+        dominant = "fa_bwd_main_kernel" if bwd_dominant else "fa_fwd_kernel"
+    else:
+        dominant = "fa_bwd_d128_kernel" if bwd_dominant else "fa_fwd_d128_kernel"
+    dom_flops = fl["bwd"] if bwd_dominant else fl["fwd"]
+    dom_t = bwd_avg if bwd_dominant else fwd_avg
     achieved = dom_flops / dom_t / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
@@ -491,7 +498,8 @@ def run_ours(args, rank, world, local):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "metric": METRIC if d == 64 else METRIC.replace("(bf16,", f"(bf16, d={d},"),
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_job / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(w, p_drop, seed),
@@ -513,9 +521,9 @@ def run_ours(args, rank, world, local):
 # ---------------------------------------------------------------- forward only (any head dim)
 
 def run_fwd_only(args, rank, world, local):
-    """Times fa_fwd alone on a workload with its head dimension overridden
-    (--head-dim 128: the wide forward kernel, whose backward is not built).
-    Same timing rules as the fwd+bwd line; the metric is forward TFLOP/s."""
+    """Times fa_fwd alone (--fwd-only) on a workload, at its head dimension
+    or the one --head-dim gives.  Same timing rules as the fwd+bwd line; the
+    metric is forward TFLOP/s."""
     import numpy as np
     import torch
 
@@ -784,7 +792,7 @@ def main(argv=None):
                     help="drop probability of the fused dropout (0 = plain attention)")
     ap.add_argument("--seed", type=int, default=1234, help="dropout seed")
     ap.add_argument("--head-dim", type=int, default=64, choices=[64, 128],
-                    help="head dimension; 128 times the forward alone")
+                    help="head dimension of the workload (the reported line uses 64)")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward alone")
     args = ap.parse_args(argv)
     rank, world, local = dist_env()
@@ -800,7 +808,7 @@ def main(argv=None):
             return run_reference(args, rank, world)
         if args.workload == "decode":
             return run_decode(args, rank, world, local)
-        if args.head_dim != 64 or args.fwd_only:
+        if args.fwd_only:
             return run_fwd_only(args, rank, world, local)
         return run_ours(args, rank, world, local)
     finally:

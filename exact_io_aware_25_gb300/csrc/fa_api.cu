@@ -71,28 +71,30 @@ fa_status device_setup(int *dev_out, int **err_out) {
 // [B*H, N, d] bf16 viewed as a 3-D tensor {d, N, B*H}; 128-row x 64-column
 // boxes (one 128-byte swizzle span; a d = 128 tile is two boxes), 128-byte
 // swizzle; rows past N read as zeros and are dropped on store.
-bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N, int d = kHeadDim) {
+bool encode_bhnd(CUtensorMap *m, const void *ptr, int BH, int N, int d = kHeadDim,
+                 int box_rows = kTile) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 [rows, 64] dQ accumulators as a 2-D tensor {64, rows}; 128 x 32 boxes
-// (128 bytes wide) with 128-byte swizzle.
-bool encode_dq_acc(CUtensorMap *m, const void *ptr, size_t rows) {
+// fp32 [rows, d] dQ accumulators as a 2-D tensor {d, rows}; boxes of 32
+// columns (128 bytes) by 128 rows (d = 64) or 64 rows (d = 128, whose
+// backward steps cover 64 queries), 128-byte swizzle.
+bool encode_dq_acc(CUtensorMap *m, const void *ptr, size_t rows, int d) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 4};
-  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(d == kHeadDimWide ? 64 : kTile)};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -101,14 +103,12 @@ bool encode_dq_acc(CUtensorMap *m, const void *ptr, size_t rows) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// wide: the forward, which also takes d = 128.
-fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask,
-                          bool wide = false) {
+fa_status validate_common(int B, int H, int N, int d, float scale, const uint8_t *block_mask) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows >= (1LL << 31) || static_cast<long long>(B) * H >= 65536) return FA_ERR_INVALID_ARG;
-  if (d != kHeadDim && !(wide && d == kHeadDimWide)) return FA_ERR_UNSUPPORTED;
+  if (d != kHeadDim && d != kHeadDimWide) return FA_ERR_UNSUPPORTED;
   const int nt = (N + kTile - 1) / kTile;
   if (nt > kMaxGridTiles) return FA_ERR_UNSUPPORTED;
   if (block_mask && nt > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
@@ -162,7 +162,7 @@ struct WsLayout {
 // [B*H, n_pad, 64] fp32, and the block-sparse column lists (key tile ->
 // ascending query tiles): counts int32 [nt] and indices int16 [nt, nt]; one
 // int32 work counter for the persistent main kernel.
-WsLayout ws_layout(int B, int H, int N) {
+WsLayout ws_layout(int B, int H, int N, int d) {
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t n_pad = align_up(static_cast<size_t>(N), kTile);
   const size_t nt = n_pad / kTile;
@@ -172,7 +172,7 @@ WsLayout ws_layout(int B, int H, int N) {
   w.dq_acc = align_up(w.lse2 + bh * n_pad * sizeof(float), 256);
   // column lists exist only with a block mask, which limits nt to kMaxMaskTiles
   const size_t nl = nt < static_cast<size_t>(kMaxMaskTiles) ? nt : kMaxMaskTiles;
-  w.col_cnt = align_up(w.dq_acc + bh * n_pad * kHeadDim * sizeof(float), 256);
+  w.col_cnt = align_up(w.dq_acc + bh * n_pad * static_cast<size_t>(d) * sizeof(float), 256);
   w.col_idx = align_up(w.col_cnt + nl * sizeof(int), 256);
   w.sched = align_up(w.col_idx + nl * nl * sizeof(int16_t), 256);
   w.total = align_up(w.sched + sizeof(int), 256);
@@ -245,7 +245,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
                    const uint8_t *block_mask, float p, unsigned long long seed,
                    const FwdExtra &x, void *stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  fa_status st = validate_common(B, H, N, d, scale, block_mask, true);
+  fa_status st = validate_common(B, H, N, d, scale, block_mask);
   if (st != FA_OK) return st;
   if (x.csr_ptr && (N + kTile - 1) / kTile > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
   const int Nk = x.Nk > 0 ? x.Nk : N;
@@ -350,7 +350,7 @@ fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o, float 
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (validate_common(B, H, N, d, 1.f, nullptr) != FA_OK) return 0;
-  return ws_layout(B, H, N).total;
+  return ws_layout(B, H, N, d).total;
 }
 
 fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
@@ -367,19 +367,22 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  const WsLayout wl = ws_layout(B, H, N);
+  const WsLayout wl = ws_layout(B, H, N, d);
   if (!workspace || !aligned16(workspace) || workspace_bytes < wl.total) return FA_ERR_WORKSPACE;
   int dev = 0;
   int *err = nullptr;
   if ((st = device_setup(&dev, &err)) != FA_OK) return st;
   const int BH = B * H;
+  // the d = 128 backward steps over 64 query rows at a time
+  const int qrows = d == kHeadDimWide ? 64 : kTile;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!encode_bhnd(&tq, q, BH, N) || !encode_bhnd(&tk, k, BH, N) || !encode_bhnd(&tv, v, BH, N) ||
-      !encode_bhnd(&tdo, dout, BH, N) || !encode_bhnd(&tdk, dk, BH, N) ||
-      !encode_bhnd(&tdv, dv, BH, N))
+  if (!encode_bhnd(&tq, q, BH, N, d, qrows) || !encode_bhnd(&tk, k, BH, N, d) ||
+      !encode_bhnd(&tv, v, BH, N, d) || !encode_bhnd(&tdo, dout, BH, N, d, qrows) ||
+      !encode_bhnd(&tdk, dk, BH, N, d) || !encode_bhnd(&tdv, dv, BH, N, d))
     return FA_ERR_CUDA;
   BwdArgs a{};
   a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
+  a.pr.d = d;
   a.n_pad = static_cast<int>(align_up(static_cast<size_t>(N), kTile));
   a.o = static_cast<const uint16_t *>(o);
   a.dout = static_cast<const uint16_t *>(dout);
@@ -393,7 +396,7 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
   a.sched = reinterpret_cast<int *>(ws + wl.sched);
   a.dq = static_cast<uint16_t *>(dq);
   CUtensorMap tdq_acc;
-  if (!encode_dq_acc(&tdq_acc, a.dq_acc, static_cast<size_t>(BH) * a.n_pad)) return FA_ERR_CUDA;
+  if (!encode_dq_acc(&tdq_acc, a.dq_acc, static_cast<size_t>(BH) * a.n_pad, d)) return FA_ERR_CUDA;
   cudaEvent_t ev0, ev1;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -460,7 +463,7 @@ size_t fa_bwd_csr_workspace_size(int B, int H, int N, int d) {
   if (validate_common(B, H, N, d, 1.f, nullptr) != FA_OK) return 0;
   const size_t nt = (static_cast<size_t>(N) + kTile - 1) / kTile;
   if (nt > static_cast<size_t>(kMaxMaskTiles)) return 0;
-  return ws_layout(B, H, N).total + align_up(nt * nt, 256);
+  return ws_layout(B, H, N, d).total + align_up(nt * nt, 256);
 }
 
 fa_status fa_bwd_csr(const void *q, const void *k, const void *v, const void *o,
@@ -482,7 +485,7 @@ fa_status fa_bwd_csr(const void *q, const void *k, const void *v, const void *o,
   int *err = nullptr;
   if ((st = device_setup(&dev, &err)) != FA_OK) return st;
   // the dense copy of the mask sits after the backward's own workspace
-  const size_t own = ws_layout(B, H, N).total;
+  const size_t own = ws_layout(B, H, N, d).total;
   uint8_t *dense = static_cast<uint8_t *>(workspace) + own;
   const int nb = (N + kTile - 1) / kTile;
   if (launch_csr_to_dense(row_ptr, col_idx, nnz, nb, dense, err,
@@ -514,7 +517,7 @@ const char *fa_status_string(int status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, bad size or bad scale";
     case FA_ERR_UNSUPPORTED:
-      return "FA_ERR_UNSUPPORTED: head dim (64; 128 forward only), size limit or device (sm_103)";
+      return "FA_ERR_UNSUPPORTED: head dim (64 or 128), size limit or device (sm_103)";
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: tensor pointers must be 16-byte aligned";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel's bounded wait ran out";

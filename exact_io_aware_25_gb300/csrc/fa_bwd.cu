@@ -39,26 +39,31 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRowsPerThread = 4;
 constexpr int kRowsPerBlock = 256 / 8;  // rows one pass of a block covers
 
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
   pdl_wait();
   pdl_trigger();
+  constexpr int kV = D / 64;  // 16-byte words of O (and of dO) per thread and row
   const Problem &pr = a.pr;
   const int bh = blockIdx.y;
   const int sub = threadIdx.x & 7;
   const int r0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.sched = 0;
-  const uint16_t *o_head = a.o + static_cast<size_t>(bh) * pr.N * kHeadDim;
-  const uint16_t *do_head = a.dout + static_cast<size_t>(bh) * pr.N * kHeadDim;
+  const uint16_t *o_head = a.o + static_cast<size_t>(bh) * pr.N * D;
+  const uint16_t *do_head = a.dout + static_cast<size_t>(bh) * pr.N * D;
   const size_t ws_row0 = static_cast<size_t>(bh) * a.n_pad;
-  uint4 ov[kRowsPerThread], dv[kRowsPerThread];
+  uint4 ov[kRowsPerThread][kV], dv[kRowsPerThread][kV];
 #pragma unroll
   for (int u = 0; u < kRowsPerThread; ++u) {
     const int i = r0 + u * kRowsPerBlock;
-    ov[u] = make_uint4(0u, 0u, 0u, 0u);
-    dv[u] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < pr.N) {
-      ov[u] = __ldg(reinterpret_cast<const uint4 *>(o_head + i * kHeadDim + sub * 8));
-      dv[u] = __ldg(reinterpret_cast<const uint4 *>(do_head + i * kHeadDim + sub * 8));
+#pragma unroll
+    for (int w = 0; w < kV; ++w) {
+      ov[u][w] = make_uint4(0u, 0u, 0u, 0u);
+      dv[u][w] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < pr.N) {
+        ov[u][w] = __ldg(reinterpret_cast<const uint4 *>(o_head + i * D + (sub * kV + w) * 8));
+        dv[u][w] = __ldg(reinterpret_cast<const uint4 *>(do_head + i * D + (sub * kV + w) * 8));
+      }
     }
   }
   // n_pad is a multiple of 128 and the grid covers it exactly: every row
@@ -66,21 +71,25 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
 #pragma unroll
   for (int u = 0; u < kRowsPerThread; ++u) {
     const int i = r0 + u * kRowsPerBlock;
-    const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
-    const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
     float dsum = 0.f;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(dw[t] << 16), dsum);
-      dsum = fmaf(__uint_as_float(ow[t] & 0xFFFF0000u), __uint_as_float(dw[t] & 0xFFFF0000u), dsum);
+    for (int w = 0; w < kV; ++w) {
+      const uint32_t ow[4] = {ov[u][w].x, ov[u][w].y, ov[u][w].z, ov[u][w].w};
+      const uint32_t dw[4] = {dv[u][w].x, dv[u][w].y, dv[u][w].z, dv[u][w].w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(dw[t] << 16), dsum);
+        dsum = fmaf(__uint_as_float(ow[t] & 0xFFFF0000u), __uint_as_float(dw[t] & 0xFFFF0000u),
+                    dsum);
+      }
     }
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
     const size_t g = ws_row0 + i;
-    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + g * kHeadDim + sub * 8);
-    acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + g * D + sub * (D / 8));
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) acc[w] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sub == 0) {
       a.dsum[g] = dsum;
       float l2 = INFINITY;  // padding rows and rows with no allowed key: P = 0
@@ -98,15 +107,16 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
 // dQ = scale * accumulator -> bf16, one (b, h) per blockIdx.y; a thread
 // converts 8 consecutive values of a row (chunk c: row c / 8, part c % 8) for
 // kRowsPerThread chunks spaced one block apart.
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
   pdl_wait();
   pdl_trigger();
   const Problem &pr = a.pr;
   const int bh = blockIdx.y;
-  const int chunks = pr.N * (kHeadDim / 8);
+  const int chunks = pr.N * (D / 8);
   const int c0 = blockIdx.x * (256 * kRowsPerThread) + threadIdx.x;
-  const float *acc_head = a.dq_acc + static_cast<size_t>(bh) * a.n_pad * kHeadDim;
-  uint16_t *dq_head = a.dq + static_cast<size_t>(bh) * pr.N * kHeadDim;
+  const float *acc_head = a.dq_acc + static_cast<size_t>(bh) * a.n_pad * D;
+  uint16_t *dq_head = a.dq + static_cast<size_t>(bh) * pr.N * D;
   float4 x[kRowsPerThread], y[kRowsPerThread];
 #pragma unroll
   for (int u = 0; u < kRowsPerThread; ++u) {
@@ -856,8 +866,20 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     return e;
   // preprocess: n_pad / (32 rows x 4) blocks per head cover the padded rows exactly
   const dim3 pre_grid(a.n_pad / (kRowsPerBlock * kRowsPerThread), a.pr.B * a.pr.H);
-  if ((e = launch_pdl(fa_bwd_pre_kernel, pre_grid, dim3(256), 0, st, a)) != cudaSuccess)
+  if ((e = a.pr.d == kHeadDimWide
+               ? launch_pdl(fa_bwd_pre_kernel<kHeadDimWide>, pre_grid, dim3(256), 0, st, a)
+               : launch_pdl(fa_bwd_pre_kernel<kHeadDim>, pre_grid, dim3(256), 0, st, a)) !=
+      cudaSuccess)
     return e;
+  if (a.pr.d == kHeadDimWide) {
+    if ((e = launch_bwd_main_d128(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a, st, ev_start, ev_stop)) !=
+        cudaSuccess)
+      return e;
+    const int chunks = a.pr.N * (kHeadDimWide / 8);
+    const dim3 dq_grid((chunks + 256 * kRowsPerThread - 1) / (256 * kRowsPerThread),
+                       a.pr.B * a.pr.H);
+    return launch_pdl(fa_bwd_dq_kernel<kHeadDimWide>, dq_grid, dim3(256), 0, st, a);
+  }
   const int n_items = a.pr.nt * a.pr.B * a.pr.H;
   const dim3 grid(n_items < num_sms ? n_items : num_sms);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
@@ -870,7 +892,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
   const int chunks = a.pr.N * (kHeadDim / 8);
   const dim3 dq_grid((chunks + 256 * kRowsPerThread - 1) / (256 * kRowsPerThread), a.pr.B * a.pr.H);
-  return launch_pdl(fa_bwd_dq_kernel, dq_grid, dim3(256), 0, st, a);
+  return launch_pdl(fa_bwd_dq_kernel<kHeadDim>, dq_grid, dim3(256), 0, st, a);
 }
 
 

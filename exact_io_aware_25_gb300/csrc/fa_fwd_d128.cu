@@ -59,6 +59,9 @@ struct __align__(1024) Fwd128Smem {
   uint32_t bits[kMaxMaskTiles / 32];  // CSR block mask: the row's tiles as a bitmap
 };
 
+// one CTA per SM: the buffers plus the 1 KiB alignment slack within 227 KiB
+static_assert(sizeof(Fwd128Smem) + 1024 <= 227 * 1024, "shared memory");
+
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384, kTmemCols = 512;
 
 __device__ __forceinline__ int tile_at(const Fwd128Smem &s, bool sparse, int it) {

@@ -78,16 +78,16 @@ struct FwdArgs {
 struct BwdArgs {
   Problem pr;
   int n_pad;              // N rounded up to a multiple of 128
-  const uint16_t *o;      // [B, H, N, 64] bf16
-  const uint16_t *dout;   // [B, H, N, 64] bf16
+  const uint16_t *o;      // [B, H, N, d] bf16
+  const uint16_t *dout;   // [B, H, N, d] bf16
   const float *lse;       // [B, H, N]
   float *dsum;            // workspace D   [B*H, n_pad]
   float *lse2;            // workspace lse * log2(e) [B*H, n_pad] (+inf in padding rows)
-  float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, 64]
+  float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, d]
   int *col_cnt;           // workspace, block mask only: query tiles per key tile [nt]
   int16_t *col_idx;       // workspace, block mask only: their indices [nt][nt], ascending
   int *sched;             // workspace: work counter of the persistent main kernel
-  uint16_t *dq;           // [B, H, N, 64] bf16
+  uint16_t *dq;           // [B, H, N, d] bf16
 };
 
 // Key bound of batch b: kv_len[b] clamped to [0, Nk].
@@ -143,6 +143,16 @@ cudaError_t launch_fwd_d128(const CUtensorMap &tq, const CUtensorMap &tk, const 
                             const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_splitkv_d128(const CUtensorMap &tq, const CUtensorMap &tk,
                                     const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st);
+
+// The d = 128 main backward kernel (fa_bwd_d128.cu), launched by launch_bwd
+// between its preprocess and dQ-convert kernels.  Tensor maps: tq, tdo with
+// 64-row x 64-column boxes; tk, tv, tdk, tdv with 128 x 64 boxes; tdq_acc
+// {128, rows} fp32 with 64-row x 32-column boxes.
+cudaError_t launch_bwd_main_d128(const CUtensorMap &tq, const CUtensorMap &tk,
+                                 const CUtensorMap &tv, const CUtensorMap &tdo,
+                                 const CUtensorMap &tdk, const CUtensorMap &tdv,
+                                 const CUtensorMap &tdq_acc, const BwdArgs &a, cudaStream_t st,
+                                 cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 // ev_start / ev_stop (may be null) are recorded around the main kernel.
 // tdq_acc: the fp32 dQ accumulators [B*H*n_pad, 64] as a 2-D map with 128 x 32

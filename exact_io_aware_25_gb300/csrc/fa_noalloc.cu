@@ -44,7 +44,8 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
                          int H, int N, int d, float scale, int causal, const int32_t *kv_len,
                          const uint8_t *block_mask, void *stream) {
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
-  if (need == 0) return (d != fa::kHeadDim && B > 0 && H > 0 && N > 0) ? FA_ERR_UNSUPPORTED
+  if (need == 0) return (d != fa::kHeadDim && d != fa::kHeadDimWide && B > 0 && H > 0 && N > 0)
+                            ? FA_ERR_UNSUPPORTED
                                                                          : FA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   int dev = 0;

@@ -41,23 +41,24 @@ def test_status_strings(fa_lib):
 
 
 def test_workspace_size_formula(fa_lib):
-    # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + 64 fp32 dQ accumulators;
+    # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + d fp32 dQ accumulators;
     # plus the block-sparse column lists: nl int32 counts and nl*nl int16 indices
     # (nl = min(nt, 1024), the most tiles a block mask may have), and one int32
     # work counter
     up = lambda x: -(-x // 256) * 256
     for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536), (1, 1, 1 << 20)]:
-        n_pad = -(-N // 128) * 128
-        nl = min(n_pad // 128, 1024)
-        bh = B * H
-        want = up(bh * n_pad * 4)
-        want = up(want + bh * n_pad * 4)
-        want = up(want + bh * n_pad * 64 * 4)
-        want = up(want + nl * 4)
-        want = up(want + nl * nl * 2)
-        want = up(want + 4)
-        assert fa_lib.fa_bwd_workspace_size(B, H, N, 64) == want
-    assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 128) == 0
+        for d in (64, 128):
+            n_pad = -(-N // 128) * 128
+            nl = min(n_pad // 128, 1024)
+            bh = B * H
+            want = up(bh * n_pad * 4)
+            want = up(want + bh * n_pad * 4)
+            want = up(want + bh * n_pad * d * 4)
+            want = up(want + nl * 4)
+            want = up(want + nl * nl * 2)
+            want = up(want + 4)
+            assert fa_lib.fa_bwd_workspace_size(B, H, N, d) == want
+    assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 96) == 0
     assert fa_lib.fa_bwd_workspace_size(0, 1, 128, 64) == 0
     assert fa_lib.fa_bwd_workspace_size(1, 1, 65536 * 128, 64) == 0  # too many tiles
 
@@ -213,7 +214,7 @@ def test_api_variant_validation_without_gpu(fa_lib):
         want = fa_lib.fa_bwd_workspace_size(2, 3, N, 64) + up(nt * nt)
         assert fa_lib.fa_bwd_csr_workspace_size(2, 3, N, 64) == want
     assert fa_lib.fa_bwd_csr_workspace_size(1, 1, 1024 * 128 + 1, 64) == 0
-    assert fa_lib.fa_bwd_csr_workspace_size(1, 1, 128, 128) == 0
+    assert fa_lib.fa_bwd_csr_workspace_size(1, 1, 128, 96) == 0
     need = fa_lib.fa_bwd_csr_workspace_size(1, 1, 1000, 64)
 
     def bcsr(rp=FAKE, ws=FAKE, nbytes=need, dq=FAKE):

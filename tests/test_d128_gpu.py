@@ -1,7 +1,7 @@
-"""GPU parity of the head-dimension-128 forward (fa_fwd, fa_fwd_dropout and
-fa_fwd_splitkv with d = 128) against the fp64 oracle, which takes any d.
-Same tolerances as d = 64; masks, ragged tails, empty rows and the lazy
-rescale under peaky keys are covered as for d = 64."""
+"""GPU parity of head dimension 128 (fa_fwd / fa_bwd, the dropout and CSR
+variants, fa_fwd_splitkv with d = 128) against the fp64 oracle, which takes
+any d.  Same tolerances as d = 64; masks, ragged tails, empty rows and the
+lazy rescale under peaky keys are covered as for d = 64."""
 import numpy as np
 import pytest
 
@@ -20,12 +20,18 @@ def H(fa_lib, oracle_mod):
     return gpu_harness
 
 
-def _full(H, oracle, x):
+def _full(H, oracle, x, bwd=True):
     o, lse = H.run_fwd(x)
-    o_ref, lse_ref = oracle.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
-                                    **x.oracle_kwargs())
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    o_ref, lse_ref = oracle.forward(q, k, v, x.scale, **x.oracle_kwargs())
     H.assert_o(H.host_f64(o), o_ref)
     H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+    if bwd:
+        dq, dk, dv = H.run_bwd(x, o, lse)
+        dq_ref, dk_ref, dv_ref = oracle.backward(q, k, v, do, x.scale, **x.oracle_kwargs())
+        H.assert_grad(H.host_f64(dq), dq_ref, "dQ")
+        H.assert_grad(H.host_f64(dk), dk_ref, "dK")
+        H.assert_grad(H.host_f64(dv), dv_ref, "dV")
     return o, lse
 
 
@@ -78,30 +84,56 @@ def test_d128_all_ones_mask_equals_dense(H, oracle_mod):
 
 def test_d128_long_causal_peaky_sampled_rows(H, oracle_mod):
     """The long-context causal workload at d = 128 (peaky keys stress the
-    lazy rescale), checked on 256 sampled query rows per head."""
+    lazy rescale): forward on 256 sampled query rows per head, backward on
+    those rows (dQ) and on two sampled key tiles per head (dK, dV)."""
     import workloads as W
     w = W.make("gpt2_4k", d=D, B=1, H=4)
     x = H.Inputs(w)
     o, lse = H.run_fwd(x)
+    dq, dk, dv = H.run_bwd(x, o, lse)
     rng = np.random.default_rng(24)
     rows = W.sample_rows(rng, 1, 4, w.spec.N, 256)
-    o_ref, lse_ref = oracle_mod.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
-                                        rows=rows, **x.oracle_kwargs())
+    keys = W.sample_key_tiles(rng, 1, 4, w.spec.N, 2)
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    o_ref, lse_ref = oracle_mod.forward(q, k, v, x.scale, rows=rows, **x.oracle_kwargs())
     H.assert_o(H.host_f64(o).reshape(-1, D)[rows], o_ref)
     H.assert_lse(lse.cpu().numpy().astype(np.float64).reshape(-1)[rows], lse_ref)
+    dq_ref, dk_ref, dv_ref = oracle_mod.backward(q, k, v, do, x.scale, q_rows=rows, k_rows=keys,
+                                                 **x.oracle_kwargs())
+    H.assert_grad(H.host_f64(dq).reshape(-1, D)[rows], dq_ref, "dQ")
+    H.assert_grad(H.host_f64(dk).reshape(-1, D)[keys], dk_ref, "dK")
+    H.assert_grad(H.host_f64(dv).reshape(-1, D)[keys], dv_ref, "dV")
+
+
+def test_d128_backward_is_deterministic_in_dk_dv(H, oracle_mod):
+    """Two runs give bitwise equal dK and dV (no atomics there); dQ, summed
+    by reduce-adds in any order, agrees to fp32 rounding."""
+    import workloads as W
+    x = H.Inputs(W.make("tiny", seed=25, d=D, B=2, H=2, N=1000, causal=True))
+    o, lse = H.run_fwd(x)
+    a = H.run_bwd(x, o, lse)
+    b = H.run_bwd(x, o, lse)
+    assert torch.equal(a[1].view(torch.int16), b[1].view(torch.int16))
+    assert torch.equal(a[2].view(torch.int16), b[2].view(torch.int16))
+    assert H.rel_fro(H.host_f64(a[0]), H.host_f64(b[0])) <= 1e-2
 
 
 @pytest.mark.parametrize("p,seed", [(0.1, 5), (0.5, 2**33 + 1)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_d128_dropout_forward(H, oracle_mod, p, seed, causal):
+def test_d128_dropout(H, oracle_mod, p, seed, causal):
     import workloads as W
     x = H.Inputs(W.make("tiny", seed=30, d=D, B=2, H=2, N=300, causal=causal))
     o, lse = H.run_fwd_dropout(x, p, seed)
-    o_ref, lse_ref = oracle_mod.forward(x.f64("q"), x.f64("k"), x.f64("v"), x.scale,
-                                        p8=oracle_mod.drop_p8(p), seed=seed,
-                                        **x.oracle_kwargs())
+    dq, dk, dv = H.run_bwd_dropout(x, o, lse, p, seed)
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    kw = dict(x.oracle_kwargs(), p8=oracle_mod.drop_p8(p), seed=seed)
+    o_ref, lse_ref = oracle_mod.forward(q, k, v, x.scale, **kw)
     H.assert_o(H.host_f64(o), o_ref)
     H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+    dq_ref, dk_ref, dv_ref = oracle_mod.backward(q, k, v, do, x.scale, **kw)
+    H.assert_grad(H.host_f64(dq), dq_ref, "dQ")
+    H.assert_grad(H.host_f64(dk), dk_ref, "dK")
+    H.assert_grad(H.host_f64(dv), dv_ref, "dV")
 
 
 @pytest.mark.parametrize("Nq,Nk,S", [(1, 8192, 0), (1, 8192, 7), (16, 1000, 0), (200, 333, 3),
@@ -127,14 +159,3 @@ def test_d128_splitkv(H, oracle_mod, Nq, Nk, S):
                                            W.bf16_bits_to_f64(v), 0.125, kv_len=kv_len)
     H.assert_o(H.host_f64(o), o_ref)
     H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
-
-
-def test_d128_backward_is_reported_unsupported(H):
-    import exact_io_aware_25_gb300 as fa
-    assert fa.fa_bwd_workspace_size(1, 1, 128, D) == 0
-    t = torch.zeros((1, 1, 128, D), dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_bwd(t, t, t, t, lse, t, t, t, t, 1, 1, 128, D, 0.125, workspace=lse,
-                  workspace_bytes=512)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED
