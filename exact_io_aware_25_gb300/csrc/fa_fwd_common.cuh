@@ -42,17 +42,16 @@ struct RowDrop {
   uint32_t p8;
 };
 
-// Exponentials of one 64-column half of a row: sv[c] <- 2^(sv[c]*sl2 - m),
-// accumulated into the eight partial sums (before dropout) and packed to
-// bf16 pairs, with dropped elements packed as 0 when kDrop (jp0 = index of
-// the tile's first key pair).  In every group of eight columns the first
-// kPoly use exp2_poly (FMA pipe), the rest the MUFU unit.
+// Exponentials of 64 consecutive S columns sv[0..64) of a row: sv[c] <-
+// 2^(sv[c]*sl2 - m), accumulated into the eight partial sums (before
+// dropout) and packed to bf16 pairs in pk, with dropped elements packed as 0
+// when kDrop (jp0 = key pair index of sv[0]).  In every group of eight
+// columns the first kPoly use exp2_poly (FMA pipe), the rest the MUFU unit.
 template <int kPoly, bool kDrop>
-__device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
-                                         float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
-                                         uint32_t jp0) {
+__device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8)[8],
+                                      uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
 #pragma unroll
-  for (int c = half * 64; c < half * 64 + 64; c += 8) {
+  for (int c = 0; c < 64; c += 8) {
     float x[8];
 #pragma unroll
     for (int u = 0; u < 8; u += 2)
@@ -71,9 +70,18 @@ __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2
         a = (r & 0xffu) >= rd.p8 ? a : 0.f;
         b = ((r >> 8) & 0xffu) >= rd.p8 ? b : 0.f;
       }
-      pk[((c - half * 64) + u) >> 1] = pack_bf16(a, b);
+      pk[(c + u) >> 1] = pack_bf16(a, b);
     }
   }
+}
+
+// exp64 on the 64-column half `half` of a 128-column row (jp0: the tile's
+// first key pair).
+template <int kPoly, bool kDrop>
+__device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
+                                         float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
+                                         uint32_t jp0) {
+  exp64<kPoly, kDrop>(sv + half * 64, sl2, m, rs8, pk, rd, jp0 + static_cast<uint32_t>(half * 32));
 }
 
 #ifndef FA_FWD_POLY_PER8
@@ -82,27 +90,36 @@ __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2
 constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 
-// Masks of one S row on an edge tile: keys at or past lim_kv are padding,
-// keys past lim_c lie in the future of the row (causal); both become -inf.
-__device__ __forceinline__ void mask_row(float (&sv)[kTile], int lim_kv, int lim_c) {
+// Masks of C consecutive S columns of a row on an edge tile: columns at or
+// past lim_kv are padding, columns past lim_c lie in the future of the row
+// (causal); both become -inf.  Limits count from the first of the C columns.
+template <int C>
+__device__ __forceinline__ void mask_cols(float (&sv)[C], int lim_kv, int lim_c) {
 #pragma unroll
-  for (int c = 0; c < kTile; ++c)
+  for (int c = 0; c < C; ++c)
     if (c >= lim_kv || c > lim_c) sv[c] = -INFINITY;
 }
 
-// Row max of 128 values: eight independent chains of three-input maxima,
-// then a tree.
-__device__ __forceinline__ float row_max(const float (&sv)[kTile]) {
+__device__ __forceinline__ void mask_row(float (&sv)[kTile], int lim_kv, int lim_c) {
+  mask_cols<kTile>(sv, lim_kv, lim_c);
+}
+
+// Max of C values (C a multiple of 16): eight independent chains of
+// three-input maxima, then a tree.
+template <int C>
+__device__ __forceinline__ float max_cols(const float (&sv)[C]) {
   float mx8[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[u], sv[8 + u]);
 #pragma unroll
-  for (int c = 16; c < kTile; c += 16)
+  for (int c = 16; c < C; c += 16)
 #pragma unroll
     for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[c + u], sv[c + 8 + u]);
   return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
 }
+
+__device__ __forceinline__ float row_max(const float (&sv)[kTile]) { return max_cols<kTile>(sv); }
 
 // Block-sparse: writes the key tiles j < j_end whose mask byte in `row` is
 // nonzero to tiles[], ascending, and returns their count (one warp).

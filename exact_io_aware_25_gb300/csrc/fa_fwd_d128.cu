@@ -6,22 +6,24 @@
 // "Method": S_ij on chip, running max and exponential sum, rescaled partial
 // output, only O and lse written), with a layout for the wider head:
 //
-// One CTA per (query tile, b*h) and per SM (192 KiB of shared memory, all
-// 512 TMEM columns); 6 warps:
-//   warp 4   TMA producer: Q once, K_j (3-stage ring, two tiles ahead) and
+// One CTA per (query tile, b*h) and per SM (195 KiB of shared memory, all
+// 512 TMEM columns); 10 warps:
+//   warp 8   TMA producer: Q once, K_j (3-stage ring, two tiles ahead) and
 //            V_j (2-stage ring).  Each 128 x 128 bf16 tile is two 128 x 64
 //            boxes (the 128-byte swizzle spans 64 bf16), 16 KiB apart.
-//   warp 5   TMEM owner and MMA issuer: S_j = Q K_j^T (M=128, N=128, K=128)
+//   warp 9   TMEM owner and MMA issuer: S_j = Q K_j^T (M=128, N=128, K=128)
 //            into S buffer j & 1, and O += P~_j V_j (M=128, N=128, K=128)
 //            with P~_j from P~ buffer j & 1 in TMEM.  Per tile j it waits
-//            for P~_j, issues PV_j and then S_{j+2} into S_j's buffer, so
-//            the commit that announces S_{j+2} also covers PV_j: when the
-//            softmax sees S_{j+2} ready, P~ buffer j & 1 is free again, and
-//            the softmax has no other barrier to pass per tile.  S_{j+1} is
-//            computed while the softmax works on S_j.
-//   warps 0-3 softmax: thread t owns query row t; as in the d = 64 kernel,
-//            with one wait (S_j ready) and one arrival (P~_j stored) per
-//            tile; the O rescale, when the lazily moved max requires one,
+//            for P~_j (which implies S_j has been read), issues PV_j and then
+//            S_{j+2} into S_j's buffer, so the commit that announces S_{j+2}
+//            also covers PV_j: when the softmax sees S_{j+2} ready, P~ buffer
+//            j & 1 is free again.  S_{j+1} is computed while the softmax
+//            works on S_j.  (Issuing S_{j+2} ahead of PV_j was measured
+//            slower.)
+//   warps 0-7 softmax: warps w and w + 4 own query rows 32 (w & 3) .. + 31
+//            and split their 128 key columns (64 each; see below).  Per tile
+//            one wait (S_j ready), one pair barrier and one arrival (P~_j
+//            stored); the O rescale, when the lazily moved max requires one,
 //            first waits for PV_{j-1}.
 // TMEM columns: S buffers 0-127 and 128-255, P~ buffers 256-319 and
 // 320-383 (bf16 pairs), O accumulator 384-511.
@@ -33,8 +35,9 @@ namespace {
 
 constexpr int kD = kHeadDimWide;
 constexpr int kKStages = 3, kVStages = 2;
-constexpr int kThreads = 192;
-constexpr uint32_t kSoftmaxWarps = 4;
+constexpr int kThreads = 320;
+constexpr uint32_t kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kHalfBytes = kTile * 64 * 2;  // 128 rows x 64 bf16: one swizzle span
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KiB: d 0-63, then d 64-127
 
@@ -57,6 +60,8 @@ struct __align__(1024) Fwd128Smem {
   int tile0;
   int16_t tiles[kMaxMaskTiles];
   uint32_t bits[kMaxMaskTiles / 32];  // CSR block mask: the row's tiles as a bitmap
+  float xmax[2][2][kTile];            // [step parity][column half][row]: partial row maxima
+  float xl[2][kTile];                 // [column half][row]: partial row sums, at the end
 };
 
 // one CTA per SM: the buffers plus the 1 KiB alignment slack within 227 KiB
@@ -114,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&s.tmem_base, kTmemCols);
-  if (warp == 4 && lane == 0) {
+  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = s.n_tiles;
   const uint32_t tmem = s.tmem_base;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (n > 0) {
       mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (n > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
@@ -220,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts_w(tmem + kColO, pa + kk * 8, d_v + kk * 128, idesc_o, kk > 0 ? 1u : acc0);
         mma_commit_w(&s.bar_o_done[bf]);
         mma_commit_w(&s.bar_v_empty[st]);
-        // S_{it+2} into S_it's buffer, behind PV_it
+        // S_{it+2} into S_it's buffer, behind PV_it: the commit that
+        // announces it also covers PV_it, so P~ buffer bf is then free
         if (it + 2 < n && !issue_s(it + 2)) break;
       }
     }
@@ -228,13 +234,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(&s.bar_final, 0, pr.wait);
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax (rows)
-    const int row = tid;
+    // ------------------------------------------------------------ softmax (half rows)
+    // Warps w and w + 4 share TMEM lanes 32 (w & 3) .. + 31 (query rows) and
+    // split each row's 128 key columns: warp w takes columns 0-63, warp w + 4
+    // columns 64-127.  The pair combines its two partial row maxima through
+    // shared memory at a 64-thread named barrier (id 2 + (w & 3)), which also
+    // carries each warp's wait outcome so that both leave the loop together.
+    // Each warp keeps the row sum of its own columns; the two are added in the
+    // epilogue, where warp w writes O columns 0-63 and warp w + 4 columns 64-127.
+    const int row = (warp & 3) * 32 + lane;
+    const int ch = warp >> 2;                  // column half
+    const uint32_t pair_bar = 2u + static_cast<uint32_t>(warp & 3);
     const int qrow = qt * kTile + row;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = pr.scale_log2;
     float m = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;           // sum over this warp's columns
     float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)
     RowDrop rd{0u, 0u, 0u};
     if (kDrop) {
@@ -248,28 +263,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
       const int j = tile_at(s, sparse, it);
       // S_it ready; PV_{it-2}, the last reader of P~ buffer bf, has completed
-      if (!mbar_wait_warp_fast(&s.bar_s_full[bf], ph, pr.wait, &s.abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sv[kTile];
-      {
-        uint32_t raw[kTile];
-        const uint32_t t0 = tmem + lane_base + kColS + static_cast<uint32_t>(bf) * 128;
-        tmem_ld32(t0 + 0, raw + 0);
-        tmem_ld32(t0 + 32, raw + 32);
-        tmem_ld32(t0 + 64, raw + 64);
-        tmem_ld32(t0 + 96, raw + 96);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) sv[c] = __uint_as_float(raw[c]);
-      }
+      const bool got = mbar_wait_warp_fast(&s.bar_s_full[bf], ph, pr.wait, &s.abort);
+      float sv[64];
       const int key0 = j * kTile;
+      const int kc0 = key0 + ch * 64;          // key of this warp's first column
       const bool edge =
           (key0 + kTile > kv_bound) || (pr.causal && key0 + kTile - 1 > qt * kTile + pr.causal_off);
-      if (edge) mask_row(sv, kv_bound - key0, pr.causal ? (qrow + pr.causal_off - key0) : kTile);
-      const float mxs = row_max(sv) * sl2;
+      float mx_part = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        uint32_t raw[64];
+        const uint32_t t0 = tmem + lane_base + kColS + static_cast<uint32_t>(bf) * 128 + ch * 64;
+        tmem_ld32(t0, raw);
+        tmem_ld32(t0 + 32, raw + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(raw[c]);
+        if (edge)
+          mask_cols<64>(sv, kv_bound - kc0, pr.causal ? (qrow + pr.causal_off - kc0) : 64);
+        mx_part = max_cols<64>(sv);
+      }
+      s.xmax[bf][ch][row] = mx_part;
+      ok = named_bar_and(pair_bar, 64, ok && got);
+      if (!ok) break;
+      const float mxs = fmaxf(mx_part, s.xmax[bf][ch ^ 1][row]) * sl2;
       m_hi = fmaxf(m_hi, mxs);
       const float m_cand = fmaxf(m, mxs);
       const bool bump = (m == -INFINITY) || (m_cand > m + kLazyRescale);
@@ -279,34 +296,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
-      const uint32_t p_base = tmem + lane_base + kColP + static_cast<uint32_t>(bf) * 64;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
         uint32_t pk[32];
-        const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
-        if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
-        else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
-        tmem_st32(p_base + half * 32, pk);
+        const uint32_t jp0 = static_cast<uint32_t>(kc0 >> 1);
+        if (edge) exp64<0, kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
+        else exp64<kPolyPer8, kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
+        tmem_st32(tmem + lane_base + kColP + static_cast<uint32_t>(bf) * 64 + ch * 32, pk);
       }
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      // both warps of the pair hold the same alpha, so they take this branch together
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O must hold every PV up to it-1 before it is rescaled
         const int pb = (it - 1) & 1;
-        if (!mbar_wait_warp(&s.bar_o_done[pb], static_cast<uint32_t>((it - 1) >> 1) & 1u, pr.wait,
-                            &s.abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t to = tmem + lane_base + kColO;
-        uint32_t ov[32];
+        if (mbar_wait_warp(&s.bar_o_done[pb], static_cast<uint32_t>((it - 1) >> 1) & 1u, pr.wait,
+                           &s.abort)) {
+          tc_fence_after();
+          const uint32_t to = tmem + lane_base + kColO + ch * 64;
+          uint32_t ov[32];
 #pragma unroll
-        for (int q4 = 0; q4 < kD / 32; ++q4) {
-          tmem_ld32(to + q4 * 32, ov);
-          tmem_wait_ld();
+          for (int q2 = 0; q2 < 2; ++q2) {
+            tmem_ld32(to + q2 * 32, ov);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          tmem_st32(to + q4 * 32, ov);
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st32(to + q2 * 32, ov);
+          }
+        } else {
+          ok = false;  // reported to the partner at the next step's barrier
         }
       }
       tmem_wait_st();
@@ -317,6 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&s.bar_p_full[bf]);
     }
     // ---------------------------------------------------------- epilogue
+    // the pair adds its two partial row sums
+    s.xl[ch][row] = l;
+    ok = named_bar_and(pair_bar, 64, ok);
+    l += s.xl[ch ^ 1][row];
     if (ok && n > 0) {
       // the last PV's commit also covers every earlier MMA of the issuer
       ok = mbar_wait_warp(&s.bar_o_done[(n - 1) & 1], static_cast<uint32_t>((n - 1) >> 1) & 1u,
@@ -330,55 +350,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kSplit)
         prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
                    static_cast<size_t>(args.nq_pad) + qrow;
+      float ov[64];
+      if (n > 0) {
+        uint32_t raw[64];
+        const uint32_t to = tmem + lane_base + kColO + ch * 64;
+        tmem_ld32(to, raw);
+        tmem_ld32(to + 32, raw + 32);
+        tmem_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float ov[64];
-        if (n > 0) {
-          uint32_t raw[64];
-          const uint32_t to = tmem + lane_base + kColO + h * 64;
-          tmem_ld32(to, raw);
-          tmem_ld32(to + 32, raw + 32);
-          tmem_wait_ld();
+        for (int c = 0; c < 64; ++c) ov[c] = __uint_as_float(raw[c]);
+      } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) ov[c] = __uint_as_float(raw[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) ov[c] = 0.f;
-        }
-        if (kSplit) {
-          if (qrow < pr.N) {
-            float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kD + h * 64);
-#pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4)
-              dst[c4] = make_float4(ov[4 * c4] * inv, ov[4 * c4 + 1] * inv, ov[4 * c4 + 2] * inv,
-                                    ov[4 * c4 + 3] * inv);
-          }
-        } else {
-          const uint32_t q_base = smem_u32(s.q + h * kHalfBytes) + row * 128;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const float *x = ov + ch * 8;
-            st_shared_v4(q_base + ((ch ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
-                         pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
-                         pack_bf16(x[6] * inv, x[7] * inv));
-          }
-        }
+        for (int c = 0; c < 64; ++c) ov[c] = 0.f;
       }
       if (kSplit) {
-        if (qrow < pr.N) args.part_lse[prow] = lse;
+        if (qrow < pr.N) {
+          float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kD + ch * 64);
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4)
+            dst[c4] = make_float4(ov[4 * c4] * inv, ov[4 * c4 + 1] * inv, ov[4 * c4 + 2] * inv,
+                                  ov[4 * c4 + 3] * inv);
+          if (ch == 0) args.part_lse[prow] = lse;
+        }
       } else {
-        if (qrow < pr.N) args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
+        const uint32_t q_base = smem_u32(s.q + ch * kHalfBytes) + row * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const float *x = ov + c8 * 8;
+          st_shared_v4(q_base + ((c8 ^ (row & 7)) << 4), pack_bf16(x[0] * inv, x[1] * inv),
+                       pack_bf16(x[2] * inv, x[3] * inv), pack_bf16(x[4] * inv, x[5] * inv),
+                       pack_bf16(x[6] * inv, x[7] * inv));
+        }
         fence_proxy_async_smem();
-        if (args.row_m && qrow < pr.N) {
-          // the pages' row statistics: m = max_j s_ij, l = sum_j exp(s_ij - m)
-          const bool any = n > 0 && l > 0.f;
-          const size_t r = static_cast<size_t>(bh) * pr.N + qrow;
-          args.row_m[r] = any ? m_hi * 0.69314718055994531f : -INFINITY;
-          args.row_l[r] = any ? l * ex2_approx(m - m_hi) : 0.f;
+        if (ch == 0 && qrow < pr.N) {
+          args.lse[static_cast<size_t>(bh) * pr.N + qrow] = lse;
+          if (args.row_m) {
+            // the pages' row statistics: m = max_j s_ij, l = sum_j exp(s_ij - m)
+            const bool any = n > 0 && l > 0.f;
+            const size_t r = static_cast<size_t>(bh) * pr.N + qrow;
+            args.row_m[r] = any ? m_hi * 0.69314718055994531f : -INFINITY;
+            args.row_l[r] = any ? l * ex2_approx(m - m_hi) : 0.f;
+          }
         }
       }
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 32 * kSoftmaxWarps);
     if (!kSplit && tid == 0 && ok && !s.abort) {
       tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
       tma_store_3d(&tm_o, s.q + kHalfBytes, 64, qt * kTile, bh);
@@ -388,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
