@@ -668,6 +668,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           if (lane == 0) c = atomicAdd(a.sched, 1);
           t = static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, c, 0);
         }
+        const int kb = v & 1;
+        // The item two back has stored its dK / dV out of this buffer.  Taken
+        // for every item (those without steps stage zeros in the buffer too),
+        // and before item v is published, so that no later phase of the
+        // barrier (item v's own store) can complete before this wait looks.
+        if (v >= 2 && !mbar_wait_warp(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort))
+          break;
         if (lane == 0) {
           s.item_ring[slot] = t;
           mbar_arrive(&s.bar_item_full[slot]);
@@ -675,12 +682,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         __syncwarp();
         if (t >= n_items) break;
         const Item itm = item_at(a, t);
-        const int kb = v & 1;
-        // The item two back has stored its dK / dV out of this buffer.  Taken
-        // for items without steps as well (their zero dK / dV are staged in
-        // the buffer too), so that each wait is for the barrier's next phase.
-        if (v >= 2 && !mbar_wait_warp(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort))
-          break;
         if (itm.n == 0) continue;
         mbar_arrive_expect_tx_w(&s.bar_kv[kb], 2 * kTileBytes);
         tma_load_3d_w(s.kv[kb][0], &tm_k, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);

@@ -99,31 +99,44 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
 
-  if (tid == 0) {
-    mbar_init(&s.bar_q, 1);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&s.bar_k_full[i], 1);
-      mbar_init(&s.bar_k_empty[i], 1);
+  // The producer warp initialises the barriers and, for a row without a
+  // block mask, issues its first loads (Q, K_0, V_0) at once, so that their
+  // memory latency overlaps the TMEM allocation and the CTA-wide setup.
+  const bool early = !sparse && j_end > j_begin && !args.starve;
+  if (warp == 4) {
+    if (lane == 0) {
+      mbar_init(&s.bar_q, 1);
+      for (int i = 0; i < kKStages; ++i) {
+        mbar_init(&s.bar_k_full[i], 1);
+        mbar_init(&s.bar_k_empty[i], 1);
+      }
+      for (int i = 0; i < kVStages; ++i) {
+        mbar_init(&s.bar_v_full[i], 1);
+        mbar_init(&s.bar_v_empty[i], 1);
+      }
+      mbar_init(&s.bar_s_full, 1);
+      mbar_init(&s.bar_s_free, kSoftmaxWarps);   // one arrival per softmax warp
+      mbar_init(&s.bar_p_full, kSoftmaxWarps);
+      mbar_init(&s.bar_o_done, 1);
+      mbar_init(&s.bar_final, 1);
+      s.abort = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
     }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&s.bar_v_full[i], 1);
-      mbar_init(&s.bar_v_empty[i], 1);
+    __syncwarp();
+    if (early) {
+      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      mbar_arrive_expect_tx_w(&s.bar_k_full[0], kTileBytes);
+      tma_load_3d_w(s.k[0], &tm_k, &s.bar_k_full[0], 0, j_begin * kTile, bh);
+      mbar_arrive_expect_tx_w(&s.bar_v_full[0], kTileBytes);
+      tma_load_3d_w(s.v[0], &tm_v, &s.bar_v_full[0], 0, j_begin * kTile, bh);
     }
-    mbar_init(&s.bar_s_full, 1);
-    mbar_init(&s.bar_s_free, kSoftmaxWarps);   // one arrival per softmax warp
-    mbar_init(&s.bar_p_full, kSoftmaxWarps);
-    mbar_init(&s.bar_o_done, 1);
-    mbar_init(&s.bar_final, 1);
-    s.abort = 0;
-    fence_mbar_init();
   }
   if (warp == 5) tmem_alloc(&s.tmem_base, kTmemCols);
-  if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
-  }
   // Block-sparse: compact the allowed key tiles of this query-tile row
   // ([EXPL] "Extension: Block-Sparse FlashAttention": only nonzero blocks
   // are evaluated).
@@ -151,8 +164,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (n > 0) {
-      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
-      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      if (!early) {
+        mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+        tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      }
       if (!args.starve) {
         auto load_k = [&](int it) -> bool {
           const int st = it % kKStages;
@@ -163,9 +178,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           tma_load_3d_w(s.k[st], &tm_k, &s.bar_k_full[st], 0, tile_at(s, sparse, it) * kTile, bh);
           return true;
         };
-        bool ok = load_k(0);
+        bool ok = early || load_k(0);   // K_0 and V_0 went out with Q when early
         for (int it = 0; ok && it < n; ++it) {
           if (it + 1 < n && !load_k(it + 1)) break;
+          if (early && it == 0) continue;
           const int st = it % kVStages;
           const uint32_t use = it / kVStages;
           if (use > 0 && !mbar_wait_warp(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort))

@@ -100,32 +100,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
 
-  if (tid == 0) {
-    mbar_init(&s.bar_q, 1);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&s.bar_k_full[i], 1);
-      mbar_init(&s.bar_k_empty[i], 1);
+  // The producer warp initialises the barriers and, for a row without a
+  // block mask, issues its first loads (Q, K_0, V_0) at once, so that their
+  // memory latency overlaps the TMEM allocation and the CTA-wide setup.
+  const bool early = !sparse && j_end > j_begin && !args.starve;
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      mbar_init(&s.bar_q, 1);
+      for (int i = 0; i < kKStages; ++i) {
+        mbar_init(&s.bar_k_full[i], 1);
+        mbar_init(&s.bar_k_empty[i], 1);
+      }
+      for (int i = 0; i < kVStages; ++i) {
+        mbar_init(&s.bar_v_full[i], 1);
+        mbar_init(&s.bar_v_empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s.bar_s_full[i], 1);
+        mbar_init(&s.bar_p_full[i], kSoftmaxWarps);
+        mbar_init(&s.bar_o_done[i], 1);
+      }
+      mbar_init(&s.bar_final, 1);
+      s.abort = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_o);
     }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&s.bar_v_full[i], 1);
-      mbar_init(&s.bar_v_empty[i], 1);
+    __syncwarp();
+    if (early) {
+      const int row = j_begin * kTile;
+      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+      tma_load_3d_w(s.q + kHalfBytes, &tm_q, &s.bar_q, 64, qt * kTile, bh);
+      mbar_arrive_expect_tx_w(&s.bar_k_full[0], kTileBytes);
+      tma_load_3d_w(s.k[0], &tm_k, &s.bar_k_full[0], 0, row, bh);
+      tma_load_3d_w(s.k[0] + kHalfBytes, &tm_k, &s.bar_k_full[0], 64, row, bh);
+      mbar_arrive_expect_tx_w(&s.bar_v_full[0], kTileBytes);
+      tma_load_3d_w(s.v[0], &tm_v, &s.bar_v_full[0], 0, row, bh);
+      tma_load_3d_w(s.v[0] + kHalfBytes, &tm_v, &s.bar_v_full[0], 64, row, bh);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.bar_s_full[i], 1);
-      mbar_init(&s.bar_p_full[i], kSoftmaxWarps);
-      mbar_init(&s.bar_o_done[i], 1);
-    }
-    mbar_init(&s.bar_final, 1);
-    s.abort = 0;
-    fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
-  }
   if (warp == 0) {
     const int count =
         !sparse ? j_end - j_begin
@@ -148,9 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (n > 0) {
-      mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
-      tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
-      tma_load_3d_w(s.q + kHalfBytes, &tm_q, &s.bar_q, 64, qt * kTile, bh);
+      if (!early) {
+        mbar_arrive_expect_tx_w(&s.bar_q, kTileBytes);
+        tma_load_3d_w(s.q, &tm_q, &s.bar_q, 0, qt * kTile, bh);
+        tma_load_3d_w(s.q + kHalfBytes, &tm_q, &s.bar_q, 64, qt * kTile, bh);
+      }
       if (!args.starve) {
         auto load_k = [&](int it) -> bool {
           const int st = it % kKStages;
@@ -163,10 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_w(s.k[st] + kHalfBytes, &tm_k, &s.bar_k_full[st], 64, row, bh);
           return true;
         };
-        bool ok = load_k(0);
+        bool ok = early || load_k(0);   // K_0 and V_0 went out with Q when early
         if (ok && n > 1) ok = load_k(1);
         for (int it = 0; ok && it < n; ++it) {
           if (it + 2 < n && !load_k(it + 2)) break;
+          if (early && it == 0) continue;
           const int st = it % kVStages;
           const uint32_t use = it / kVStages;
           if (use > 0 && !mbar_wait_warp(&s.bar_v_empty[st], (use - 1) & 1, pr.wait, &s.abort))
