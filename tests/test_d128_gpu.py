@@ -159,3 +159,31 @@ def test_d128_splitkv(H, oracle_mod, Nq, Nk, S):
                                            W.bf16_bits_to_f64(v), 0.125, kv_len=kv_len)
     H.assert_o(H.host_f64(o), o_ref)
     H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+
+
+def test_d128_bert_full(H, oracle_mod):
+    """The BERT-shaped workload at d = 128, every output against the oracle."""
+    import workloads as W
+    _full(H, oracle_mod, H.Inputs(W.make("bert", d=D)))
+
+
+def test_d128_block_sparse_64k_sampled(H, oracle_mod):
+    """The 64K block-sparse workload at d = 128 (two heads), checked on sampled
+    query rows (O, lse, dQ) and sampled key tiles (dK, dV)."""
+    import workloads as W
+    w = W.make("sparse64k", d=D, H=2)
+    x = H.Inputs(w)
+    o, lse = H.run_fwd(x)
+    dq, dk, dv = H.run_bwd(x, o, lse)
+    rng = np.random.default_rng(26)
+    rows = W.sample_rows(rng, 1, 2, w.spec.N, 128)
+    keys = W.sample_key_tiles(rng, 1, 2, w.spec.N, 2)
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    o_ref, lse_ref = oracle_mod.forward(q, k, v, x.scale, rows=rows, **x.oracle_kwargs())
+    H.assert_o(H.host_f64(o).reshape(-1, D)[rows], o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64).reshape(-1)[rows], lse_ref)
+    dq_ref, dk_ref, dv_ref = oracle_mod.backward(q, k, v, do, x.scale, q_rows=rows, k_rows=keys,
+                                                 **x.oracle_kwargs())
+    H.assert_grad(H.host_f64(dq).reshape(-1, D)[rows], dq_ref, "dQ")
+    H.assert_grad(H.host_f64(dk).reshape(-1, D)[keys], dk_ref, "dK")
+    H.assert_grad(H.host_f64(dv).reshape(-1, D)[keys], dv_ref, "dV")
