@@ -14,9 +14,8 @@
  *     contiguous, so one (b, h) is a plain N x d operand of [EXPL] "Method".
  *   - All tensor pointers are DEVICE pointers owned by the caller, and must be
  *     16-byte aligned (TMA requirement).  The library never frees them.
- *   - d must be 64; the forward entry points (fa_fwd, fa_fwd_dropout,
- *     fa_fwd_stats, fa_fwd_csr, fa_fwd_qk, fa_fwd_splitkv) also take d = 128.
- *     N >= 1, B >= 1, H >= 1, B*H*N < 2^31.
+ *   - d is 64 or 128 (separate kernels for each).  N >= 1, B >= 1, H >= 1,
+ *     B*H*N < 2^31.
  *   - scale multiplies Q K^T (S = scale * Q K^T); it must be finite and > 0.
  *   - causal != 0 keeps key j for query i iff j <= i (top-left aligned).
  *   - kv_len: NULL, or a DEVICE int32 array [B]; keys j >= kv_len[b] of batch b
@@ -53,9 +52,9 @@ extern "C" {
 typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, non-finite or non-positive scale */
-    FA_ERR_UNSUPPORTED = -2,  /* d not 64 (or 128 in a forward), N > 65535 * 128,
-                                 N > 1024 * 128 with a block mask, N > 131072 with
-                                 dropout, or no sm_103 device */
+    FA_ERR_UNSUPPORTED = -2,  /* d not 64 or 128, N > 65535 * 128, N > 1024 * 128 with
+                                 a block mask, N > 131072 with dropout, or no sm_103
+                                 device */
     FA_ERR_MISALIGNED = -3,   /* a tensor pointer is not 16-byte aligned */
     FA_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed */
     FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait ran out (reported by fa_check) */
