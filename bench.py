@@ -276,7 +276,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import workloads as W
-    w = W.make(args.workload)
+    w = W.make(args.workload) if args.head_dim == 64 else W.make(args.workload, d=args.head_dim)
     # calibrate one head, then size each step to keep the whole run to ~2 minutes
     f1, t1, _, threads = time_oracle(w, 0.0, max_units=1, dropout=args.dropout, seed=args.seed)
     per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
@@ -293,7 +293,9 @@ def run_reference(args, rank, world):
     sample = (f"{heads_per_step} of {w.spec.B * w.spec.H} (b, h) heads per step "
               f"(forward + backward, full rows)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference",
+        "metric": METRIC if w.spec.d == 64 else METRIC.replace("(bf16,", f"(bf16, d={w.spec.d},"),
+        "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
