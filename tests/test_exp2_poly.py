@@ -14,9 +14,8 @@ CSRC = os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc")
 
 def kernel_coefficients():
     text = open(os.path.join(CSRC, "fa_fwd_common.cuh")).read()
-    body = text[text.index("float exp2_poly(float x)"):]
-    vals = dict(re.findall(r"\b(c[0-4]) = ([-+0-9.e]+)f", body[:600]))
-    return np.array([float(vals[f"c{i}"]) for i in range(5)], np.float32)
+    vals = dict(re.findall(r"\bkExp2C([0-4]) = ([-+0-9.e]+)f", text))
+    return np.array([float(vals[str(i)]) for i in range(5)], np.float32)
 
 
 def emulate(x, c):
