@@ -244,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int qrow = qt * kTile + row;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = pr.scale_log2;
-    float m = -INFINITY;  // running max of S*scale*log2e
-    float l = 0.f;
-    float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)        // running sum of 2^(S*scale*log2e - m)
+    float m = -INFINITY;     // running max of S*scale*log2e
+    float l = 0.f;           // running sum of 2^(S*scale*log2e - m)
+    float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)
     RowDrop rd{0u, 0u, 0u};
     if (kDrop) {
       rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
