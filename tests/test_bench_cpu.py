@@ -1,0 +1,80 @@
+"""Host-side pieces of bench.py without a GPU: the FLOP convention, the
+traffic lookup that goes stale when a kernel source changes, the reference
+arm (the fp64 oracle on the host cores) and its JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def test_flop_convention_by_hand():
+    """4 N L d per head forward (L = key bound), halved under causal, times the
+    nonzero-block fraction under a block mask; backward 2.5x, step 3.5x."""
+    s = W.SPECS["gpt2"]                      # B8 H12 N1024 d64 causal
+    fl = bench.counted_flops(s, None)
+    want = 4.0 * 1024 * 1024 * 64 * 12 * 8 / 2
+    assert fl["fwd"] == want and fl["bwd"] == 2.5 * want and fl["step"] == 3.5 * want
+    kv = np.array([256, 300, 512, 1000], np.int32)   # clamped to N = 512
+    b = W.Spec("t", 4, 2, 512, 64, False, 0.125)
+    fl = bench.counted_flops(b, kv)
+    assert fl["fwd"] == sum(4.0 * 512 * min(L, 512) * 64 * 2 for L in kv)
+    assert fl["nominal_step"] == 3.5 * 4.0 * 512 * 512 * 64 * 2 * 4
+    mask = np.zeros((4, 4), np.uint8)
+    mask[0, 0] = mask[1, 2] = mask[3, 3] = 1
+    c = W.Spec("m", 1, 1, 512, 64, False, 0.125)
+    assert bench.counted_flops(c, None, mask)["fwd"] == 4.0 * 512 * 512 * 64 * 3 / 16
+    d128 = W.Spec("w", 1, 1, 256, 128, False, 0.125)
+    assert bench.counted_flops(d128, None)["fwd"] == 4.0 * 256 * 256 * 128
+
+
+def test_traffic_lookup_goes_stale_with_the_sources(monkeypatch):
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    entries = json.load(open(path))
+    key = "fa_bwd_main_kernel:bert"
+    assert bench.load_traffic("fa_bwd_main_kernel", "bert") in (None, entries[key]["bytes"])
+    monkeypatch.setattr(bench, "_sources_hash", lambda names: entries[key]["sources"])
+    assert bench.load_traffic("fa_bwd_main_kernel", "bert") == entries[key]["bytes"]
+    monkeypatch.setattr(bench, "_sources_hash", lambda names: "0" * 16)
+    assert bench.load_traffic("fa_bwd_main_kernel", "bert") is None
+    assert bench.load_traffic("no_such_kernel", "bert") is None
+
+
+def test_every_captured_kernel_names_existing_sources():
+    csrc = os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc")
+    for kernel, names in bench.KERNEL_SOURCES.items():
+        for n in names:
+            assert os.path.exists(os.path.join(csrc, n)), (kernel, n)
+
+
+def test_workload_config_names_the_workload():
+    for name in ("tiny", "bert", "gpt2", "gpt2_4k"):
+        w = W.make(name, B=1, H=1, N=256) if name != "tiny" else W.make(name)
+        cfg = bench.workload_config(w)
+        assert cfg["workload"] and cfg["d"] == 64 and "flushed" in cfg["l2"]
+    cfg = bench.workload_config(W.make("tiny"), dropout=0.25, seed=7)
+    assert cfg["dropout"]["p"] == 0.25 and cfg["dropout"]["seed"] == 7
+
+
+def test_reference_arm_prints_one_json_line(fa_lib, oracle_mod):
+    """`bench.py --impl reference` runs the oracle on the host cores and
+    prints the contract's line with impl, cpu_baseline and e2e."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny", "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["higher_is_better"] is True and d["steps"] == 1
