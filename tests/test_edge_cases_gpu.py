@@ -1,0 +1,107 @@
+"""More GPU edge cases against the fp64 oracle: masks combined with dropout
+at d = 128, an empty CSR mask, many tiny heads (the persistent backward's
+scheduler with hundreds of items per CTA), concurrent calls on two streams
+with their own workspaces."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def H(fa_lib, oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gpu_harness
+    return gpu_harness
+
+
+def _check_all(H, oracle, x, o, lse, grads, **extra):
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    kw = dict(x.oracle_kwargs(), **extra)
+    o_ref, lse_ref = oracle.forward(q, k, v, x.scale, **kw)
+    H.assert_o(H.host_f64(o), o_ref)
+    H.assert_lse(lse.cpu().numpy().astype(np.float64), lse_ref)
+    refs = oracle.backward(q, k, v, do, x.scale, **kw)
+    for g, r, name in zip(grads, refs, ("dQ", "dK", "dV")):
+        H.assert_grad(H.host_f64(g), r, name)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_dropout_with_every_mask(H, oracle_mod, d):
+    """Causal, key padding and a block mask together, with dropout."""
+    import workloads as W
+    rng = np.random.default_rng(90 + d)
+    w = W.make("tiny", seed=91, d=d, B=2, H=2, N=700)
+    mask = (rng.random((6, 6)) < 0.6).astype(np.uint8)
+    np.fill_diagonal(mask, 1)
+    x = H.Inputs(w, causal=True, kv_len=np.array([700, 333], np.int32), block_mask=mask)
+    p, seed = 0.2, 2**35 + 11
+    o, lse = H.run_fwd_dropout(x, p, seed)
+    grads = H.run_bwd_dropout(x, o, lse, p, seed)
+    _check_all(H, oracle_mod, x, o, lse, grads, p8=oracle_mod.drop_p8(p), seed=seed)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_empty_csr_mask(H, oracle_mod, d):
+    """nnz = 0: no query row has a key; O = 0, lse = -inf, all gradients 0."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    w = W.make("tiny", seed=92, d=d, B=1, H=2, N=300)
+    x = H.Inputs(w)
+    B, Hh, N = x.B, x.H, x.N
+    ptr = torch.zeros(4, dtype=torch.int32, device="cuda")     # nb = 3
+    o = H.nan_like_bf16((B, Hh, N, d))
+    lse = torch.full((B, Hh, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    fa.fa_fwd_csr(x.q, x.k, x.v, o, lse, B, Hh, N, d, x.scale, 0, None, ptr, None, 0, st)
+    fa.fa_check(st)
+    assert torch.all(o.float() == 0) and torch.all(torch.isneginf(lse))
+    shape = (B, Hh, N, d)
+    dq, dk, dv = (H.nan_like_bf16(shape) for _ in range(3))
+    nbytes = fa.fa_bwd_csr_workspace_size(B, Hh, N, d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    fa.fa_bwd_csr(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hh, N, d, x.scale, 0, None, ptr,
+                  None, 0, ws, nbytes, st)
+    fa.fa_check(st)
+    for g in (dq, dk, dv):
+        assert torch.all(g.float() == 0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_tiny_heads(H, oracle_mod, d):
+    """B*H = 2048 heads of 70 rows: far more work items than SMs, each a
+    single ragged tile."""
+    import workloads as W
+    x = H.Inputs(W.make("tiny", seed=93, d=d, B=64, H=32, N=70, causal=True))
+    o, lse = H.run_fwd(x)
+    grads = H.run_bwd(x, o, lse)
+    _check_all(H, oracle_mod, x, o, lse, grads)
+
+
+def test_two_streams_with_their_own_workspaces(H, oracle_mod):
+    """Two problems enqueued on two streams at once; each backward has its own
+    workspace (and so its own work counter): both match their own oracle."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    xs = [H.Inputs(W.make("tiny", seed=94 + i, B=2, H=4, N=900, causal=bool(i))) for i in range(2)]
+    streams = [torch.cuda.Stream() for _ in xs]
+    outs = []
+    for x in xs:   # every buffer filled on the default stream before the two streams start
+        shape = (x.B, x.H, x.N, x.d)
+        nbytes = fa.fa_bwd_workspace_size(x.B, x.H, x.N, x.d)
+        outs.append((H.nan_like_bf16(shape),
+                     torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda"),
+                     tuple(H.nan_like_bf16(shape) for _ in range(3)),
+                     torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")))
+    torch.cuda.synchronize()
+    for x, st, (o, lse, (dq, dk, dv), ws) in zip(xs, streams, outs):
+        fa.fa_fwd(x.q, x.k, x.v, o, lse, x.B, x.H, x.N, x.d, x.scale, x.causal, None, None, st)
+        fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, x.B, x.H, x.N, x.d, x.scale, x.causal,
+                  None, None, ws, ws.numel(), st)
+    for st in streams:
+        fa.fa_check(st)
+    for x, (o, lse, grads, _) in zip(xs, outs):
+        _check_all(H, oracle_mod, x, o, lse, grads)

@@ -57,3 +57,24 @@ def test_noalloc_rejects_problems_beyond_its_scratch(fa_lib):
     with pytest.raises(fa.FaError) as ei:
         fa.fa_bwd_noalloc(16, 16, 16, 16, 16, 16, 16, 16, 16, 1, 8, 65536, 64, 0.125)
     assert ei.value.status == fa.FA_ERR_WORKSPACE
+
+
+def test_noalloc_backward_at_d128(fa_lib, oracle_mod):
+    """The d = 128 backward through the fixed scratch, against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_io_aware_25_gb300 as fa
+    import gpu_harness as H
+    import workloads as W
+    x = H.Inputs(W.make("tiny", seed=96, d=128, B=2, H=2, N=500, causal=True))
+    o, lse = H.run_fwd(x)
+    shape = (x.B, x.H, x.N, 128)
+    dq, dk, dv = (H.nan_like_bf16(shape) for _ in range(3))
+    st = torch.cuda.current_stream()
+    fa.fa_bwd_noalloc(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, x.B, x.H, x.N, 128, x.scale,
+                      x.causal, None, None, st)
+    fa.fa_check(st)
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    refs = oracle_mod.backward(q, k, v, do, x.scale, **x.oracle_kwargs())
+    for g, r, name in zip((dq, dk, dv), refs, ("dQ", "dK", "dV")):
+        H.assert_grad(H.host_f64(g), r, name)
