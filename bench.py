@@ -39,7 +39,9 @@ UNIT = "TFLOP/s"
 WORKLOAD = "bert"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 4  # forward, D preprocess, dK/dV/dQ, dQ convert
+# forward, D preprocess, dK/dV/dQ, dQ convert; plus the column-list kernel
+# when a block mask is given
+KERNELS_PER_STEP = 4
 
 
 # ---------------------------------------------------------------- helpers
@@ -510,7 +512,7 @@ def run_ours(args, rank, world, local):
             "bwd_main": {"tflops": fl["bwd"] / bwd_avg / 1e12, "ms": bwd_avg * 1e3},
             "nominal_tflops": fl["nominal_step"] * K * world / t_job / 1e12,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP * K,
+            "gpu_launches": (KERNELS_PER_STEP + (w.block_mask is not None)) * K,
             "clocks": sampler.summary(),
             "wall_s_timed_region": wall,
             "peak_aux_bytes": ws_bytes,
