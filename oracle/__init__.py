@@ -21,6 +21,9 @@ Function -> definition it follows (page titles as in ``fa_oracle.c``):
 * ``backward``     the textbook gradient of O = softmax(scale Q K^T) V
                    (dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dO o O)),
                    dQ = scale dS K, dK = scale dS^T Q).
+* ``forward_qk`` / ``backward_qk``  the same with Nq query rows and Nk key
+                   rows, causal aligned to the bottom right (key j is kept
+                   for query i iff j <= i + Nk - Nq).
 
 Pins (tests/test_oracle_pins.py): rows of P sum to 1, constant V gives that
 constant, every block split of the tiled forward equals the one-shot
@@ -93,6 +96,9 @@ def _load():
             lib.fa_oracle_bwd_dropout.restype = ci
             lib.fa_oracle_fwd_qk.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, ci, i32p, i64p,
                                              cl, dp, dp, ci]
+            lib.fa_oracle_bwd_qk.argtypes = [dp, dp, dp, dp, ci, ci, ci, ci, ci, cd, ci, i32p,
+                                             i64p, cl, i64p, cl, dp, dp, dp, ci]
+            lib.fa_oracle_bwd_qk.restype = ci
             lib.fa_oracle_fwd_stats.argtypes = [dp, dp, dp, ci, ci, ci, ci, cd, ci, i32p, u8p,
                                                 ci, i64p, cl, dp, dp, dp, dp, ci]
             lib.fa_oracle_fwd_stats.restype = ci
@@ -300,4 +306,38 @@ def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, q
         dq = dq.reshape(B, H, N, d)
     if k_rows is None:
         dk, dv = dk.reshape(B, H, N, d), dv.reshape(B, H, N, d)
+    return dq, dk, dv
+
+
+def backward_qk(q, k, v, dout, scale, kv_len=None, q_rows=None, k_rows=None, nthreads=None,
+                causal=False):
+    """Backward of forward_qk: q, dout [B, H, Nq, d]; k, v [B, H, Nk, d];
+    causal bottom-right aligned.  Returns (dq, dk, dv) shaped like q, k, v, or
+    [len(q_rows), d] / [len(k_rows), d] for selected rows (bh * Nq + i,
+    bh * Nk + j)."""
+    lib = _load()
+    B, H, Nq, d = _shape(q)
+    Nk = _shape(k)[2]
+    qa, qp = _f64(q)
+    ka, kp = _f64(k)
+    va, vp = _f64(v)
+    da, dp = _f64(dout)
+    kl, klp = _opt_i32(kv_len)
+    qr, qrp = _opt_i64(q_rows)
+    kr, krp = _opt_i64(k_rows)
+    nq = B * H * Nq if q_rows is None else len(qr)
+    nk = B * H * Nk if k_rows is None else len(kr)
+    dq = np.zeros((max(nq, 1), d), np.float64)
+    dk = np.zeros((max(nk, 1), d), np.float64)
+    dv = np.zeros((max(nk, 1), d), np.float64)
+    rc = lib.fa_oracle_bwd_qk(qp, kp, vp, dp, B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                              klp, qrp, nq, krp, nk, _f64(dq)[1], _f64(dk)[1], _f64(dv)[1],
+                              _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"fa_oracle_bwd_qk failed ({rc})")
+    dq, dk, dv = dq[:nq], dk[:nk], dv[:nk]
+    if q_rows is None:
+        dq = dq.reshape(B, H, Nq, d)
+    if k_rows is None:
+        dk, dv = dk.reshape(B, H, Nk, d), dv.reshape(B, H, Nk, d)
     return dq, dk, dv

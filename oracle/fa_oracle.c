@@ -523,13 +523,13 @@ static void dq_item(void *vctx, int64_t item, double *s) {
     if (l <= 0.0) return;
     const double *qi = row_of(p->q, p, bh, i), *doi = row_of(p->dout, p, bh, i);
     (void)s;
-    for (int j = 0; j < p->N; ++j) {
+    for (int j = 0; j < p->Nk; ++j) {
         if (!allowed(p, b, i, j)) continue;
-        const double sij = p->scale * dot(qi, row_of(p->k, p, bh, j), d);
+        const double sij = p->scale * dot(qi, key_row(p->k, p, bh, j), d);
         const double pij = exp(sij - m) / l;
-        const double dpij = dot(doi, row_of(p->v, p, bh, j), d);
+        const double dpij = dot(doi, key_row(p->v, p, bh, j), d);
         const double dsij = pij * (drop_factor(p, bh, i, j) * dpij - D);
-        const double *kj = row_of(p->k, p, bh, j);
+        const double *kj = key_row(p->k, p, bh, j);
         for (int cc = 0; cc < d; ++cc) dq[cc] += p->scale * dsij * kj[cc];
     }
 }
@@ -539,10 +539,10 @@ static void dkdv_item(void *vctx, int64_t item, double *s) {
     bwd_ctx *c = (bwd_ctx *)vctx;
     const problem *p = c->p;
     const int64_t g = c->k_rows ? c->k_rows[item] : item;
-    const int bh = (int)(g / p->N), j = (int)(g % p->N), b = bh / p->H, d = p->d;
+    const int bh = (int)(g / p->Nk), j = (int)(g % p->Nk), b = bh / p->H, d = p->d;
     double *dk = c->dk + (size_t)item * d, *dv = c->dv + (size_t)item * d;
     for (int cc = 0; cc < d; ++cc) { dk[cc] = 0.0; dv[cc] = 0.0; }
-    const double *kj = row_of(p->k, p, bh, j), *vj = row_of(p->v, p, bh, j);
+    const double *kj = key_row(p->k, p, bh, j), *vj = key_row(p->v, p, bh, j);
     (void)s;
     for (int i = 0; i < p->N; ++i) {
         if (!allowed(p, b, i, j)) continue;
@@ -562,33 +562,32 @@ static void dkdv_item(void *vctx, int64_t item, double *s) {
 }
 
 /*
- * Backward on selected rows.  q_rows (global bh * N + i, NULL = all) select
- * the dQ rows written to dq [nq, d]; k_rows (global bh * N + j, NULL = all)
- * select the key rows whose dK, dV go to dk, dv [nk, d].  The forward
- * statistics are recomputed here from the definition for exactly the query
- * rows that are needed (the dQ rows, plus every row that attends to one of
- * the selected keys).
+ * The backward of the problem with N query rows and Nk key rows (causal kept
+ * j <= i + Nk - N, the bottom-right rule, which is the top-left one when
+ * N = Nk); q_rows are global query rows bh * N + i, k_rows global key rows
+ * bh * Nk + j.
  */
-int fa_oracle_bwd_dropout(const double *q, const double *k, const double *v,
-                          const double *dout, int B, int H, int N, int d, double scale,
-                          int causal, const int32_t *kv_len, const uint8_t *block_mask, int blk,
-                          int p8, uint64_t seed, const int64_t *q_rows, int64_t nq,
-                          const int64_t *k_rows, int64_t nk, double *dq, double *dk,
-                          double *dv, int nthreads) {
-    if (!q || !k || !v || !dout || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+static int bwd_general(const double *q, const double *k, const double *v, const double *dout,
+                       int B, int H, int N, int Nk, int d, double scale, int causal,
+                       const int32_t *kv_len, const uint8_t *block_mask, int blk, int p8,
+                       uint64_t seed, const int64_t *q_rows, int64_t nq, const int64_t *k_rows,
+                       int64_t nk, double *dq, double *dk, double *dv, int nthreads) {
+    if (!q || !k || !v || !dout || B < 1 || H < 1 || N < 1 || Nk < 1 || d < 1) return -1;
     if (p8 < 0 || p8 > 255) return -1;
     if ((nq != 0 || !q_rows) && !dq) return -1;
     if ((nk != 0 || !k_rows) && (!dk || !dv)) return -1;
     problem p;
     problem_init(&p, q, k, v, dout, B, H, N, d, scale, causal, kv_len, block_mask, blk);
+    p.Nk = Nk;
+    p.causal_off = Nk - N;
     problem_dropout(&p, p8, seed);
-    const int64_t total = (int64_t)B * H * N;
+    const int64_t total = (int64_t)B * H * N, total_k = (int64_t)B * H * Nk;
     if (!q_rows) nq = total;
-    if (!k_rows) nk = total;
+    if (!k_rows) nk = total_k;
     for (int64_t r = 0; q_rows && r < nq; ++r)
         if (q_rows[r] < 0 || q_rows[r] >= total) return -1;
     for (int64_t r = 0; k_rows && r < nk; ++r)
-        if (k_rows[r] < 0 || k_rows[r] >= total) return -1;
+        if (k_rows[r] < 0 || k_rows[r] >= total_k) return -1;
 
     /* mark the query rows whose forward statistics are needed */
     uint8_t *need = (uint8_t *)calloc((size_t)total, 1);
@@ -596,16 +595,16 @@ int fa_oracle_bwd_dropout(const double *q, const double *k, const double *v,
     if (!need || !row_index) { free(need); free(row_index); return -3; }
     for (int64_t r = 0; r < nq; ++r) need[q_rows ? q_rows[r] : r] = 1;
     /* key-side needs: every query row of the head that attends to a selected key */
-    uint8_t *key_sel = (uint8_t *)calloc((size_t)total, 1);
+    uint8_t *key_sel = (uint8_t *)calloc((size_t)total_k, 1);
     if (!key_sel) { free(need); free(row_index); return -3; }
     for (int64_t r = 0; r < nk; ++r) key_sel[k_rows ? k_rows[r] : r] = 1;
-    int *sel = (int *)malloc((size_t)N * sizeof(int));
+    int *sel = (int *)malloc((size_t)Nk * sizeof(int));
     if (!sel) { free(need); free(row_index); free(key_sel); return -3; }
     for (int bh = 0; bh < B * H; ++bh) {
         const int b = bh / H;
         int nsel = 0;
-        for (int j = 0; j < N; ++j)
-            if (key_sel[(size_t)bh * N + j]) sel[nsel++] = j;
+        for (int j = 0; j < Nk; ++j)
+            if (key_sel[(size_t)bh * Nk + j]) sel[nsel++] = j;
         if (!nsel) continue;
         for (int i = 0; i < N; ++i) {
             if (need[(size_t)bh * N + i]) continue;
@@ -636,13 +635,46 @@ int fa_oracle_bwd_dropout(const double *q, const double *k, const double *v,
         c.fm = fm; c.fl = fl; c.fo = fo; c.fD = fD;
         c.q_rows = q_rows; c.dq = dq; c.k_rows = k_rows; c.dk = dk; c.dv = dv;
         c.row_index = row_index;
-        rc = parallel_for(nfwd, nthreads, (size_t)N, stats_item, &c);
+        rc = parallel_for(nfwd, nthreads, (size_t)Nk, stats_item, &c);
         if (rc == 0) rc = parallel_for(nq, nthreads, 0, dq_item, &c);
         if (rc == 0) rc = parallel_for(nk, nthreads, 0, dkdv_item, &c);
     }
 done:
     free(need); free(row_index); free(fwd_rows); free(fm); free(fl); free(fD); free(fo);
     return rc;
+}
+
+/*
+ * Backward on selected rows.  q_rows (global bh * N + i, NULL = all) select
+ * the dQ rows written to dq [nq, d]; k_rows (global bh * N + j, NULL = all)
+ * select the key rows whose dK, dV go to dk, dv [nk, d].  The forward
+ * statistics are recomputed here from the definition for exactly the query
+ * rows that are needed (the dQ rows, plus every row that attends to one of
+ * the selected keys).
+ */
+int fa_oracle_bwd_dropout(const double *q, const double *k, const double *v,
+                          const double *dout, int B, int H, int N, int d, double scale,
+                          int causal, const int32_t *kv_len, const uint8_t *block_mask, int blk,
+                          int p8, uint64_t seed, const int64_t *q_rows, int64_t nq,
+                          const int64_t *k_rows, int64_t nk, double *dq, double *dk,
+                          double *dv, int nthreads) {
+    return bwd_general(q, k, v, dout, B, H, N, N, d, scale, causal, kv_len, block_mask, blk, p8,
+                       seed, q_rows, nq, k_rows, nk, dq, dk, dv, nthreads);
+}
+
+/*
+ * Backward with Nq query rows and Nk key rows (no block mask, no dropout;
+ * causal aligned to the bottom right as in fa_oracle_fwd_qk): q, dout
+ * [B, H, Nq, d]; k, v [B, H, Nk, d]; q_rows are bh * Nq + i, k_rows
+ * bh * Nk + j.
+ */
+int fa_oracle_bwd_qk(const double *q, const double *k, const double *v, const double *dout,
+                     int B, int H, int Nq, int Nk, int d, double scale, int causal,
+                     const int32_t *kv_len, const int64_t *q_rows, int64_t nq,
+                     const int64_t *k_rows, int64_t nk, double *dq, double *dk, double *dv,
+                     int nthreads) {
+    return bwd_general(q, k, v, dout, B, H, Nq, Nk, d, scale, causal, kv_len, NULL, 128, 0, 0,
+                       q_rows, nq, k_rows, nk, dq, dk, dv, nthreads);
 }
 
 int fa_oracle_bwd(const double *q, const double *k, const double *v, const double *dout,

@@ -565,6 +565,85 @@ def test_bottom_right_causal_against_numpy_softmax(oracle_mod):
                                atol=1e-13)
 
 
+# ---------------------------------------------------------------- Nq != Nk backward
+
+
+def test_short_query_backward_square_case_is_the_square_backward(oracle_mod):
+    """Nq == Nk: backward_qk is the square backward (bottom-right causal is
+    then the top-left rule)."""
+    rng = np.random.default_rng(53)
+    B, H, N, d = 2, 2, 13, 4
+    q, k, vv, do = (_rand(rng, B, H, N, d) for _ in range(4))
+    kv_len = np.array([13, 6], np.int32)
+    for causal in (False, True):
+        a = oracle_mod.backward_qk(q, k, vv, do, 0.6, kv_len=kv_len, causal=causal)
+        b = oracle_mod.backward(q, k, vv, do, 0.6, kv_len=kv_len, causal=causal)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(3, 8, True), (8, 5, True), (4, 7, False)])
+def test_short_query_backward_matches_central_finite_differences(oracle_mod, Nq, Nk, causal):
+    """dQ, dK, dV of L = sum(dO o O) for the Nq x Nk forward, against
+    central differences of forward_qk (with key padding; with Nq > Nk the
+    first Nq - Nk causal rows have no key and give nothing)."""
+    rng = np.random.default_rng(54 + Nq)
+    B, H, d, scale, h = 2, 1, 3, 0.7, 1e-6
+    q, do = _rand(rng, B, H, Nq, d), _rand(rng, B, H, Nq, d)
+    k, vv = _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d)
+    kv_len = np.array([Nk, Nk - 2], np.int32)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle_mod.forward_qk(q_, k_, v_, scale, kv_len=kv_len, causal=causal)
+        return float(np.sum(do * o))
+
+    grads = oracle_mod.backward_qk(q, k, vv, do, scale, kv_len=kv_len, causal=causal)
+    base = {"q": q, "k": k, "v": vv}
+    for which, grad in zip(("q", "k", "v"), grads):
+        assert grad.shape == base[which].shape
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (loss(plus["q"], plus["k"], plus["v"])
+                        - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.linalg.norm(num - grad) / max(np.linalg.norm(grad), 1e-30)
+        assert err < 1e-6, (which, err)
+
+
+def test_short_query_backward_closed_form_at_zero_queries(oracle_mod):
+    """Q = 0 under bottom-right causal: P_ij = 1/n_i on the n_i = i + Nk - Nq + 1
+    allowed keys, so dV_j = sum over rows i that see j of dO_i / n_i, and
+    dK = scale * dS^T Q = 0."""
+    rng = np.random.default_rng(57)
+    B, H, Nq, Nk, d = 1, 2, 4, 9, 3
+    k, vv, do = _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nq, d)
+    _, dk, dv = oracle_mod.backward_qk(np.zeros((B, H, Nq, d)), k, vv, do, 0.9, causal=True)
+    want = np.zeros_like(dv)
+    for i in range(Nq):
+        n = i + Nk - Nq + 1
+        want[:, :, :n] += do[:, :, i:i + 1] / n
+    np.testing.assert_allclose(dv, want, rtol=0, atol=1e-14)
+    assert np.all(dk == 0.0)
+
+
+def test_short_query_backward_row_selection(oracle_mod):
+    rng = np.random.default_rng(58)
+    B, H, Nq, Nk, d = 2, 2, 5, 17, 3
+    q, do = _rand(rng, B, H, Nq, d), _rand(rng, B, H, Nq, d)
+    k, vv = _rand(rng, B, H, Nk, d), _rand(rng, B, H, Nk, d)
+    kw = dict(kv_len=np.array([17, 10], np.int32), causal=True)
+    dq, dk, dv = oracle_mod.backward_qk(q, k, vv, do, 0.5, **kw)
+    rows = np.array([0, 4, 7, 19], np.int64)
+    keys = np.array([0, 16, 20, 50, 67], np.int64)
+    dq_r, dk_r, dv_r = oracle_mod.backward_qk(q, k, vv, do, 0.5, q_rows=rows, k_rows=keys, **kw)
+    np.testing.assert_array_equal(dq_r, dq.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(dk_r, dk.reshape(-1, d)[keys])
+    np.testing.assert_array_equal(dv_r, dv.reshape(-1, d)[keys])
+
+
 # ---------------------------------------------------------------- row statistics (m, l)
 
 
