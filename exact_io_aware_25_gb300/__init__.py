@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_csr.restype = ci
             L.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, vp]
             L.fa_fwd_qk.restype = ci
+            L.fa_bwd_qk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf,
+                                    ci, vp, vp, sz, vp]
+            L.fa_bwd_qk.restype = ci
             L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
                                          ci, vp, vp, vp]
             L.fa_bwd_noalloc.restype = ci
@@ -240,6 +243,17 @@ def fa_fwd_qk(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal=0, kv_len=None,
     _check(lib().fa_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
                            int(Nq), int(Nk), int(d), float(scale), int(bool(causal)),
                            _ptr(kv_len), _stream(stream)), "fa_fwd_qk")
+
+
+def fa_bwd_qk(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal=0,
+              kv_len=None, workspace=None, workspace_bytes=0, stream=None) -> None:
+    """Backward of fa_fwd_qk (workspace: fa_bwd_workspace_size(B, H, Nq, d) bytes)."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fa_bwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                           _ptr(dk), _ptr(dv), int(B), int(H), int(Nq), int(Nk), int(d),
+                           float(scale), int(bool(causal)), _ptr(kv_len), _ptr(workspace),
+                           int(workspace_bytes), _stream(stream)), "fa_bwd_qk")
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=0,

@@ -220,18 +220,6 @@ fa_status validate_splitkv(int B, int H, int Nq, int Nk, int d, float scale, int
   return FA_OK;
 }
 
-}  // namespace
-}  // namespace fa
-
-using namespace fa;
-
-extern "C" {
-
-}  // extern "C"
-
-namespace fa {
-namespace {
-
 // Optional parts of a forward call beyond fa_fwd_dropout's arguments.
 struct FwdExtra {
   float *row_m = nullptr, *row_l = nullptr;             // row statistics
@@ -296,6 +284,8 @@ fa_status validate_csr(const int32_t *row_ptr, const int32_t *col_idx, int nnz) 
 }  // namespace
 }  // namespace fa
 
+using namespace fa;
+
 extern "C" {
 
 fa_status fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -353,14 +343,22 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return ws_layout(B, H, N, d).total;
 }
 
-fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
-                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
-                         int H, int N, int d, float scale, int causal, const int32_t *kv_len,
-                         const uint8_t *block_mask, float p, unsigned long long seed,
-                         void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// The backward of every entry point: N query rows, Nk key rows (Nk = N
+// except in fa_bwd_qk, which passes no block mask and no dropout).
+fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int Nk,
+                   int d, float scale, int causal, const int32_t *kv_len,
+                   const uint8_t *block_mask, float p, unsigned long long seed, void *workspace,
+                   size_t workspace_bytes, void *stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   fa_status st = validate_common(B, H, N, d, scale, block_mask);
   if (st != FA_OK) return st;
+  if (Nk < 1 || static_cast<long long>(B) * H * Nk >= (1LL << 31)) return FA_ERR_INVALID_ARG;
   const int p8 = drop_threshold(p);
   if (p8 < 0) return FA_ERR_INVALID_ARG;
   if (p8 > 0 && N > kMaxDropN) return FA_ERR_UNSUPPORTED;
@@ -376,14 +374,17 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
   // the d = 128 backward steps over 64 query rows at a time
   const int qrows = d == kHeadDimWide ? 64 : kTile;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!encode_bhnd(&tq, q, BH, N, d, qrows) || !encode_bhnd(&tk, k, BH, N, d) ||
-      !encode_bhnd(&tv, v, BH, N, d) || !encode_bhnd(&tdo, dout, BH, N, d, qrows) ||
-      !encode_bhnd(&tdk, dk, BH, N, d) || !encode_bhnd(&tdv, dv, BH, N, d))
+  if (!encode_bhnd(&tq, q, BH, N, d, qrows) || !encode_bhnd(&tk, k, BH, Nk, d) ||
+      !encode_bhnd(&tv, v, BH, Nk, d) || !encode_bhnd(&tdo, dout, BH, N, d, qrows) ||
+      !encode_bhnd(&tdk, dk, BH, Nk, d) || !encode_bhnd(&tdv, dv, BH, Nk, d))
     return FA_ERR_CUDA;
   BwdArgs a{};
   a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
   a.pr.d = d;
+  a.pr.Nk = Nk;
+  a.pr.causal_off = Nk - N;
   a.n_pad = static_cast<int>(align_up(static_cast<size_t>(N), kTile));
+  a.nkt = (Nk + kTile - 1) / kTile;
   a.o = static_cast<const uint16_t *>(o);
   a.dout = static_cast<const uint16_t *>(dout);
   a.lse = lse;
@@ -408,6 +409,28 @@ fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void
                  cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                         int H, int N, int d, float scale, int causal, const int32_t *kv_len,
+                         const uint8_t *block_mask, float p, unsigned long long seed,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, N, d, scale, causal, kv_len,
+                  block_mask, p, seed, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_bwd_qk(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                    const void *dout, void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk,
+                    int d, float scale, int causal, const int32_t *kv_len, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, kv_len,
+                  nullptr, 0.f, 0ull, workspace, workspace_bytes, stream);
 }
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {

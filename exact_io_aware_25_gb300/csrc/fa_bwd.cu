@@ -262,8 +262,8 @@ constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ
 constexpr uint32_t kTmemCols = 512;
 
 // One work item: key tile kt of head bh and the query tiles that attend to
-// it (i >= kt under causal, the block mask's column kt, none at all when the
-// tile lies past kv_len).
+// it (from causal_first_qtile under causal, the block mask's column kt, none
+// at all when the tile lies past kv_len).
 struct Item {
   int kt, bh, n, rot, i_begin;
   int kv_bound;
@@ -276,10 +276,10 @@ __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   it.kt = t / BH;
   it.bh = t - it.kt * BH;
   it.kv_bound = key_bound(pr, it.bh / pr.H);
-  it.i_begin = pr.causal ? it.kt : 0;
+  it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   if (it.kt * kTile >= it.kv_bound) it.n = 0;
   else if (pr.block_mask) it.n = __ldg(a.col_cnt + it.kt);
-  else it.n = pr.nt - it.i_begin;
+  else it.n = pr.nt > it.i_begin ? pr.nt - it.i_begin : 0;
   // the key tiles of one head start at different query tiles, so their
   // concurrent dQ reduce-adds land on different accumulator rows
   it.rot = it.n > 0 ? it.kt % it.n : 0;
@@ -296,8 +296,9 @@ __device__ __forceinline__ int qtile_of(const BwdArgs &a, const Item &it, int k)
 
 // Elementwise phase 1 for 32 query columns starting at qc: S^T values in
 // `v` are replaced, in place, by P^T = 2^(S^T * scale * log2(e) - lse2_q).
-// kMask selects the edge-tile body (keys past kv_len, causal diagonal); the
-// common body carries no masking work at all.
+// kMask selects the edge-tile body (keys past kv_len, causal diagonal: kr is
+// the key row less the tile pair's causal_delta); the common body carries no
+// masking work at all.
 template <bool kMask>
 __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int kr, bool key_ok,
                                            bool diag, float sl2, uint32_t lse2) {
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = pr.nt * pr.B * pr.H;
+  const int n_items = a.nkt * pr.B * pr.H;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -495,7 +496,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           break;
         }
         tc_fence_after();
-        const bool diag = pr.causal && (i == itm.kt);
+        // causal: this warp's block (keys kr0..kr0+31, queries half*64..+63)
+        // holds a masked element iff its largest kr - qc exceeds the pair's delta
+        const int delta = causal_delta(pr, i, itm.kt);
+        const bool diag = pr.causal && ((warp & 3) * 32 + 31 - half * 64 > delta);
+        const int kr_rel = kr - delta;
         const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
         const uint32_t t_s = tmem + lane_base + kColST + half * 64;
         const uint32_t t_dp = tmem + lane_base + kColDPT + half * 64;
@@ -507,12 +512,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_ld32(t_dp + 32, db);
         const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
         // phase 1: P^T, in place over the S^T registers
-        if (need_mask) p_from_s32<true>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
+        if (need_mask) p_from_s32<true>(sa, half * 64, kr_rel, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sa, half * 64, kr, key_ok, diag, sl2, lse2_a);
         tmem_wait_ld_tied32(sb, db);
         tc_fence_before();
         warp_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
-        if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
+        if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr_rel, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
         // the P^T columns are free once the previous step's dV has read them
         if (g > 0 && !w_wait(&s.bar_pt_free, (g - 1) & 1)) {
@@ -881,7 +886,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        a.pr.B * a.pr.H);
     return launch_pdl(fa_bwd_dq_kernel<kHeadDimWide>, dq_grid, dim3(256), 0, st, a);
   }
-  const int n_items = a.pr.nt * a.pr.B * a.pr.H;
+  const int n_items = a.nkt * a.pr.B * a.pr.H;
   const dim3 grid(n_items < num_sms ? n_items : num_sms);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
   e = a.pr.drop_p8 > 0

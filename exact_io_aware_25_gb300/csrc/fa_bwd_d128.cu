@@ -92,8 +92,8 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
 }
 
 // One work item: key tile kt of head bh and its query steps (two per query
-// tile that attends to the key tile: i >= kt under causal, the block mask's
-// column kt, none past kv_len).
+// tile that attends to the key tile: from causal_first_qtile under causal,
+// the block mask's column kt, none past kv_len).
 struct Item {
   int kt, bh, n, rot, i_begin;
   int kv_bound;
@@ -106,11 +106,11 @@ __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   it.kt = t / BH;
   it.bh = t - it.kt * BH;
   it.kv_bound = key_bound(pr, it.bh / pr.H);
-  it.i_begin = pr.causal ? it.kt : 0;
+  it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   int tiles;
   if (it.kt * kTile >= it.kv_bound) tiles = 0;
   else if (pr.block_mask) tiles = __ldg(a.col_cnt + it.kt);
-  else tiles = pr.nt - it.i_begin;
+  else tiles = pr.nt > it.i_begin ? pr.nt - it.i_begin : 0;
   it.n = 2 * tiles;
   // start the key tiles of one head at different query tiles, so that their
   // concurrent dQ reduce-adds land on different accumulator rows
@@ -131,7 +131,8 @@ __device__ __forceinline__ int qstep_of(const BwdArgs &a, const Item &it, int k)
 
 // P^T = 2^(S^T * scale * log2(e) - lse2_q) for this thread's 32 query
 // columns (qc: first column within the step, for lse2; qm: the same column
-// within its 128-query tile, for the causal diagonal), in place.
+// within its 128-query tile, for the causal diagonal, against kr = the key
+// row less the tile pair's causal_delta), in place.
 template <bool kMask>
 __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int qm, int kr, bool key_ok,
                                            bool diag, float sl2, uint32_t lse2) {
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = pr.nt * pr.B * pr.H;
+  const int n_items = a.nkt * pr.B * pr.H;
 
   if (tid == 0) {
     mbar_init(&s.bar_kv, 1);
@@ -320,8 +321,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           break;
         }
         tc_fence_after();
-        // the causal diagonal: query step i64 lies in query tile i64 / 2
-        const bool diag = pr.causal && ((i64 >> 1) == itm.kt);
+        // causal: query step i64 lies in query tile i64 / 2; this warp's block
+        // (keys kr0..kr0+31, tile columns qm..qm+31) holds a masked element iff
+        // its largest kr - qm exceeds the tile pair's delta
+        const int qm = (i64 & 1) * kQStep + qc;
+        const int delta = causal_delta(pr, i64 >> 1, itm.kt);
+        const bool diag = pr.causal && ((warp & 3) * 32 + 31 - qm > delta);
+        const int kr_rel = kr - delta;
         const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
         uint32_t sa[32], da[32];
         tmem_ld32(tmem + lane_base + kColST + qc, sa);
@@ -330,8 +336,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_fence_before();
         warp_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
         const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
-        const int qm = (i64 & 1) * kQStep + qc;
-        if (need_mask) p_from_s32<true>(sa, qc, qm, kr, key_ok, diag, sl2, lse2_a);
+        if (need_mask) p_from_s32<true>(sa, qc, qm, kr_rel, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sa, qc, qm, kr, key_ok, diag, sl2, lse2_a);
         // the P^T columns are free once the previous step's dV has read them
         if (g > 0 && !w_wait(&s.bar_pt_free, (g - 1) & 1)) {
@@ -676,7 +681,7 @@ cudaError_t launch_bwd_main_d128(const CUtensorMap &tq, const CUtensorMap &tk,
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  const int n_items = a.pr.nt * a.pr.B * a.pr.H;
+  const int n_items = a.nkt * a.pr.B * a.pr.H;
   const dim3 grid(n_items < num_sms ? n_items : num_sms);
   if (ev_start && ev_stop && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
   e = a.pr.drop_p8 > 0

@@ -78,6 +78,7 @@ struct FwdArgs {
 struct BwdArgs {
   Problem pr;
   int n_pad;              // N rounded up to a multiple of 128
+  int nkt;                // key tiles per head: ceil(Nk / 128) (work items per head)
   const uint16_t *o;      // [B, H, N, d] bf16
   const uint16_t *dout;   // [B, H, N, d] bf16
   const float *lse;       // [B, H, N]
@@ -89,6 +90,20 @@ struct BwdArgs {
   int *sched;             // workspace: work counter of the persistent main kernel
   uint16_t *dq;           // [B, H, N, d] bf16
 };
+
+// First query tile with a query that sees a key of key tile kt under the
+// causal rule (key j is kept for query i iff j <= i + causal_off): the tile
+// of query kt * 128 - causal_off, or tile 0.
+__device__ __forceinline__ int causal_first_qtile(const Problem &p, int kt) {
+  const int q0 = kt * kTile - p.causal_off;
+  return q0 <= 0 ? 0 : q0 / kTile;
+}
+
+// Causal offset of the tile pair (query tile i, key tile kt): the element of
+// tile rows (key kr, query qc) is masked iff kr > qc + causal_delta.
+__device__ __forceinline__ int causal_delta(const Problem &p, int i, int kt) {
+  return (i - kt) * kTile + p.causal_off;
+}
 
 // Key bound of batch b: kv_len[b] clamped to [0, Nk].
 __device__ __forceinline__ int key_bound(const Problem &p, int b) {

@@ -270,6 +270,24 @@ FA_API fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o,
                            const int32_t *kv_len, void *stream);
 
 /*
+ * Backward of fa_fwd_qk, by the same recomputation as fa_bwd with the same
+ * bottom-right causal rule; the gradient definitions are fa_bwd's with Nq
+ * query rows and Nk key rows.
+ *   q, o, dO in : bf16 [B, H, Nq, d];  k, v in : bf16 [B, H, Nk, d]
+ *   lse      in : fp32 [B, H, Nq], fa_fwd_qk's output for the same inputs
+ *   dq      out : bf16 [B, H, Nq, d];  dk, dv out : bf16 [B, H, Nk, d]
+ *   workspace   : >= fa_bwd_workspace_size(B, H, Nq, d) bytes (it scales
+ *                 with the query rows only)
+ * Query rows with no key give dQ = 0; keys that no query sees (past kv_len)
+ * give dK = dV = 0.  Errors as fa_bwd (FA_ERR_INVALID_ARG also for Nk < 1).
+ */
+FA_API fa_status fa_bwd_qk(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                           const int32_t *kv_len, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
  * Synchronises stream and reports the first device-side error recorded since
  * the previous fa_check: FA_ERR_TIMEOUT when a bounded wait inside a kernel
  * ran out (the kernel then returned early and its outputs are invalid),

@@ -208,6 +208,17 @@ def test_api_variant_validation_without_gpu(fa_lib):
     assert qk(Nk=0) == -1 and qk(Nq=0) == -1 and qk(d=32) == -2
     assert qk() == -3 and qk(d=128) == -3 and qk(Nq=300, Nk=5) == -3
 
+    def bqk(Nq=5, Nk=300, d=64, dk=FAKE, ws=FAKE, nbytes=None):
+        if nbytes is None:
+            nbytes = fa_lib.fa_bwd_workspace_size(2, 3, max(Nq, 1), 64)
+        return L.fa_bwd_qk(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dk, FAKE, 2, 3, Nq, Nk, d,
+                           0.125, 1, None, ws, nbytes, None)
+
+    assert bqk(Nk=0) == -1 and bqk(Nq=0) == -1 and bqk(d=32) == -2
+    assert bqk(dk=FAKE + 2) == -3 and bqk(d=128, dk=FAKE + 8) == -3
+    assert bqk(ws=None) == -6 and bqk(nbytes=1) == -6
+    assert bqk(Nq=300, Nk=5, ws=None) == -6
+
     up = lambda x: -(-x // 256) * 256
     for N in (1, 128, 1000, 65536):
         nt = -(-N // 128)

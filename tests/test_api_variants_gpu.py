@@ -3,7 +3,7 @@
 * fa_fwd_stats: the row statistics (m, l) next to O and lse;
 * fa_fwd_csr / fa_bwd_csr: the block mask given as CSR (unsorted, with
   repeated entries) equals the dense mask, and bad entries are reported;
-* fa_fwd_qk: Nq != Nk with the bottom-right causal mask.
+* fa_fwd_qk / fa_bwd_qk: Nq != Nk with the bottom-right causal mask.
 """
 import numpy as np
 import pytest
@@ -192,3 +192,84 @@ def test_fwd_qk_square_equals_fa_fwd(H):
     o1, l1 = H.run_fwd(x)
     o2, l2 = _qk(H, w.q, w.k, w.v, True, scale=w.spec.scale)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def _bwd_qk(H, q, k, v, do, o, lse, causal, kv_len=None, scale=0.125):
+    import exact_io_aware_25_gb300 as fa
+    B, Hh, Nq, d = q.shape
+    Nk = k.shape[2]
+    tq, tk, tv, tdo = (H.dev_bf16(t) for t in (q, k, v, do))
+    dq = H.nan_like_bf16((B, Hh, Nq, d))
+    dk, dv = H.nan_like_bf16((B, Hh, Nk, d)), H.nan_like_bf16((B, Hh, Nk, d))
+    kl = None if kv_len is None else torch.from_numpy(np.asarray(kv_len, np.int32)).cuda()
+    nbytes = fa.fa_bwd_workspace_size(B, Hh, Nq, d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    fa.fa_bwd_qk(tq, tk, tv, o, lse, tdo, dq, dk, dv, B, Hh, Nq, Nk, d, scale, causal, kl, ws,
+                 nbytes, st)
+    fa.fa_check(st)
+    return dq, dk, dv
+
+
+def _qk_inputs(rng, B, Hh, Nq, Nk, d):
+    import workloads as W
+    return tuple(W.f32_to_bf16_bits(rng.standard_normal((B, Hh, n, d), dtype=np.float32))
+                 for n in (Nq, Nk, Nk, Nq))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1000), (100, 1000), (300, 333), (500, 200), (200, 777),
+                                   (128, 4096)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_qk_bottom_right_causal(H, oracle_mod, d, Nq, Nk, causal):
+    """Every dQ, dK, dV of the Nq x Nk problem against the oracle's backward
+    (offsets Nk - Nq that are not multiples of the 128-row tile, Nq > Nk with
+    query rows that see no key, key padding)."""
+    import workloads as W
+    rng = np.random.default_rng(180 + Nq + Nk + d)
+    B, Hh = 2, 3
+    q, k, v, do = _qk_inputs(rng, B, Hh, Nq, Nk, d)
+    kv_len = np.array([Nk, max(1, (2 * Nk) // 3)], np.int32)
+    o, lse = _qk(H, q, k, v, causal, kv_len)
+    dq, dk, dv = _bwd_qk(H, q, k, v, do, o, lse, causal, kv_len)
+    f = W.bf16_bits_to_f64
+    refs = oracle_mod.backward_qk(f(q), f(k), f(v), f(do), 0.125, kv_len=kv_len, causal=causal)
+    for g, r, name in zip((dq, dk, dv), refs, ("dQ", "dK", "dV")):
+        H.assert_grad(H.host_f64(g), r, name)
+    if causal and Nq > Nk:   # rows i < Nq - Nk see no key
+        assert torch.all(dq[:, :, :Nq - Nk].float() == 0)
+
+
+def test_bwd_qk_square_equals_fa_bwd(H):
+    """Nq == Nk: the same kernels with the same (top-left) causal rule, so dK
+    and dV are bitwise those of fa_bwd; dQ, summed by reduce-adds in any
+    order, agrees to fp32 rounding."""
+    import workloads as W
+    w = W.make("gpt2", B=1, H=2)
+    x = H.Inputs(w)
+    o, lse = H.run_fwd(x)
+    a = H.run_bwd(x, o, lse)
+    b = _bwd_qk(H, w.q, w.k, w.v, w.do, o, lse, True, scale=w.spec.scale)
+    assert torch.equal(a[1].view(torch.int16), b[1].view(torch.int16))
+    assert torch.equal(a[2].view(torch.int16), b[2].view(torch.int16))
+    assert H.rel_fro(H.host_f64(a[0]), H.host_f64(b[0])) <= 1e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_qk_long_keys_sampled(H, oracle_mod, d):
+    """A 1000-query block at the end of 8192 keys (causal), checked on sampled
+    query rows (dQ) and sampled keys (dK, dV)."""
+    import workloads as W
+    rng = np.random.default_rng(190 + d)
+    B, Hh, Nq, Nk = 1, 2, 1000, 8192
+    q, k, v, do = _qk_inputs(rng, B, Hh, Nq, Nk, d)
+    o, lse = _qk(H, q, k, v, True)
+    dq, dk, dv = _bwd_qk(H, q, k, v, do, o, lse, True)
+    rows = np.sort(rng.choice(B * Hh * Nq, 96, replace=False)).astype(np.int64)
+    keys = np.sort(rng.choice(B * Hh * Nk, 96, replace=False)).astype(np.int64)
+    f = W.bf16_bits_to_f64
+    dq_r, dk_r, dv_r = oracle_mod.backward_qk(f(q), f(k), f(v), f(do), 0.125, q_rows=rows,
+                                              k_rows=keys, causal=True)
+    H.assert_grad(H.host_f64(dq).reshape(-1, d)[rows], dq_r, "dQ")
+    H.assert_grad(H.host_f64(dk).reshape(-1, d)[keys], dk_r, "dK")
+    H.assert_grad(H.host_f64(dv).reshape(-1, d)[keys], dv_r, "dV")
