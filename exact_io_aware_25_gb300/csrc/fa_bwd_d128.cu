@@ -33,7 +33,6 @@
 namespace fa {
 namespace {
 
-constexpr int kD = kHeadDimWide;
 constexpr int kQStep = 64;                          // queries per step
 constexpr int kStages = 3;
 constexpr uint32_t kKvHalf = kTile * 64 * 2;        // 128 rows x 64 bf16 = 16 KiB
@@ -42,7 +41,6 @@ constexpr uint32_t kQHalf = kQStep * 64 * 2;        // 64 rows x 64 bf16 = 8 KiB
 constexpr uint32_t kQBytes = 2 * kQHalf;            // Q_i or dO_i of one step
 constexpr uint32_t kDsBytes = kTile * kQStep * 2;   // dS^T: 128 keys x 64 queries bf16
 constexpr uint32_t kDqWarpStage = kQStep * 32 * 4;  // 64 queries x 32 d fp32 = 8 KiB
-constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kMainThreads = 512;
 constexpr uint32_t kRegsElementwise = 160, kRegsDq = 96, kRegsControl = 96;

@@ -273,3 +273,26 @@ def test_bwd_qk_long_keys_sampled(H, oracle_mod, d):
     H.assert_grad(H.host_f64(dq).reshape(-1, d)[rows], dq_r, "dQ")
     H.assert_grad(H.host_f64(dk).reshape(-1, d)[keys], dk_r, "dK")
     H.assert_grad(H.host_f64(dv).reshape(-1, d)[keys], dv_r, "dV")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(300, 1), (1, 1), (129, 2)])
+def test_bwd_qk_tiny_key_counts(H, oracle_mod, d, Nq, Nk):
+    """One or two keys under bottom-right causal: only the last Nk query rows
+    see any key; the others get dQ = 0.  The second batch has kv_len = 0: no
+    key at all, every gradient of it is 0."""
+    import workloads as W
+    rng = np.random.default_rng(200 + Nq + Nk + d)
+    B, Hh = 2, 2
+    q, k, v, do = _qk_inputs(rng, B, Hh, Nq, Nk, d)
+    kv_len = np.array([Nk, 0], np.int32)
+    o, lse = _qk(H, q, k, v, True, kv_len)
+    dq, dk, dv = _bwd_qk(H, q, k, v, do, o, lse, True, kv_len)
+    f = W.bf16_bits_to_f64
+    refs = oracle_mod.backward_qk(f(q), f(k), f(v), f(do), 0.125, kv_len=kv_len, causal=True)
+    for g, r, name in zip((dq, dk, dv), refs, ("dQ", "dK", "dV")):
+        H.assert_grad(H.host_f64(g)[0], r[0], name)
+    if Nq > Nk:
+        assert torch.all(dq[0, :, :Nq - Nk].float() == 0)
+    for g in (dq, dk, dv):
+        assert torch.all(g[1].float() == 0)
