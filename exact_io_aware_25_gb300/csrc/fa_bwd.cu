@@ -227,7 +227,7 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_st_read;    // elementwise warps hold S^T / dP^T in registers
   uint64_t bar_p_full;     // P^T of the step is in TMEM
   uint64_t bar_ds_full;    // dS^T of the step is in shared memory
-  uint64_t bar_pt_free;
+  uint64_t bar_pt_free;   // dropout only: dV has read P^T
   uint64_t bar_ds_free;
   uint64_t bar_dq_full;
   uint64_t bar_dq_free;
@@ -519,8 +519,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         warp_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
         if (need_mask) p_from_s32<true>(sb, half * 64 + 32, kr_rel, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sb, half * 64 + 32, kr, key_ok, diag, sl2, lse2_a);
-        // the P^T columns are free once the previous step's dV has read them
-        if (g > 0 && !w_wait(&s.bar_pt_free, (g - 1) & 1)) {
+        // The previous step's MMAs are done with the P^T columns (dV) and the
+        // dS^T tile (dK, dQ): without dropout one wait on the later of the two
+        // commits, which the MMA thread issues after both (an mbarrier
+        // operation costs about as much as the wait it saves); with dropout,
+        // whose longer step leaves dQ later, a wait for dV alone here.
+        if (g > 0 && !w_wait(kDrop ? &s.bar_pt_free : &s.bar_ds_free, (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -531,8 +535,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&s.bar_p_full);   // dV of this step may start
-        // phase 2: dS^T; the tile is free once the previous step's dK / dQ read it
-        if (g > 0 && !w_wait(&s.bar_ds_free, (g - 1) & 1)) {
+        // phase 2: dS^T (without dropout its tile was found free before the P^T store)
+        if (kDrop && g > 0 && !w_wait(&s.bar_ds_free, (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -779,7 +783,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_bf16_ts_w(tmem + kColDV, tmem + kColPT + kk * 8, d_do_mn + kk * 128, id_acc,
                           kk > 0 ? 1u : acc0);
-          mma_commit_w(&s.bar_pt_free);
+          if (kDrop) mma_commit_w(&s.bar_pt_free);
           // dS^T of this step is in shared memory.
           if (!mbar_wait_warp(&s.bar_ds_full, g & 1, pr.wait, &s.abort)) {
             ok = false;

@@ -63,7 +63,6 @@ struct __align__(1024) Bwd128Smem {
   uint64_t bar_st_read;
   uint64_t bar_p_full;
   uint64_t bar_ds_full;
-  uint64_t bar_pt_free;
   uint64_t bar_ds_free;
   uint64_t bar_dq_full;
   uint64_t bar_dq_free;
@@ -252,7 +251,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(&s.bar_st_read, kEwWarps);
     mbar_init(&s.bar_p_full, kEwWarps);
     mbar_init(&s.bar_ds_full, kEwWarps);
-    mbar_init(&s.bar_pt_free, 1);
     mbar_init(&s.bar_ds_free, 1);
     mbar_init(&s.bar_dq_full, 1);
     mbar_init(&s.bar_dq_free, kDqWarps);
@@ -336,8 +334,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const uint32_t lse2_a = smem_u32(s.lse2[st]), dsum_a = smem_u32(s.dsum[st]);
         if (need_mask) p_from_s32<true>(sa, qc, qm, kr_rel, key_ok, diag, sl2, lse2_a);
         else p_from_s32<false>(sa, qc, qm, kr, key_ok, diag, sl2, lse2_a);
-        // the P^T columns are free once the previous step's dV has read them
-        if (g > 0 && !w_wait(&s.bar_pt_free, (g - 1) & 1)) {
+        // The previous step's MMAs are done with the P^T columns (dV) and the
+        // dS^T tile (dK, dQ^T): one wait on the later of the two commits, which
+        // the MMA thread issues after both.
+        if (g > 0 && !w_wait(&s.bar_ds_free, (g - 1) & 1)) {
           ok = false;
           break;
         }
@@ -346,11 +346,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(&s.bar_p_full);   // dV of this step may start
-        // the dS^T tile is free once the previous step's dK and dQ^T read it
-        if (g > 0 && !w_wait(&s.bar_ds_free, (g - 1) & 1)) {
-          ok = false;
-          break;
-        }
         ds_store32<kDrop>(sa, da, qc, kr, dsum_a, smem_u32(s.dst) + kr * 128, keep,
                           pr.keep_scale);
         fence_proxy_async_smem();
@@ -593,7 +588,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           for (int kk = 0; kk < kQStep / 16; ++kk)
             mma_bf16_ts_w(tmem + kColDV, tmem + kColPT + kk * 8, d_do_mn + kk * 128, id_acc,
                           kk > 0 ? 1u : acc0);
-          mma_commit_w(&s.bar_pt_free);
           if (!mbar_wait_warp(&s.bar_ds_full, g & 1, pr.wait, &s.abort)) {
             ok = false;
             break;
