@@ -66,12 +66,38 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_text(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to one
+    space: what the compiler sees, so that editing a comment does not mark a
+    capture stale.  String and character literals are kept as written."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def _sources_hash(names):
     import hashlib
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "exact_io_aware_25_gb300", "csrc", n)) as f:
+            h.update(_code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,12 +13,15 @@
 //   fa_bwd_pre_kernel   D_i, lse_i * log2(e) (+inf on padding / empty rows)
 //                       into the workspace, and zeroes the fp32 dQ
 //                       accumulators.  HBM-bound.
-//   fa_bwd_main_kernel  one CTA per (key tile j, b*h); K_j, V_j stay in shared
-//                       memory while the allowed query tiles stream past:
+//   fa_bwd_main_kernel  persistent, one CTA per SM claiming work items (key
+//                       tile j, b*h) from a counter in the workspace; per item
+//                       K_j, V_j stay in shared memory while the allowed query
+//                       tiles stream past:
 //                         S^T = K_j Q_i^T, dP^T = V_j dO_i^T  (tcgen05, TMEM)
 //                         P^T = 2^(S^T scale log2e - lse2_i), dS^T = P^T o (dP^T - D_i)
 //                         dV += P^T dO_i, dK += dS^T Q_i      (TMEM accumulators)
-//                         dQ_i partial = dS K_j -> fp32 atomics into the workspace
+//                         dQ_i partial = dS K_j -> TMA reduce-add (fp32) into
+//                         the workspace accumulators
 //   fa_bwd_dq_kernel    dQ = scale * accumulator -> bf16.
 #include "fa_kernels.cuh"
 

@@ -78,3 +78,16 @@ def test_reference_arm_prints_one_json_line(fa_lib, oracle_mod):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["higher_is_better"] is True and d["steps"] == 1
+
+
+def test_traffic_hash_ignores_comments_but_not_code():
+    """The staleness check hashes what the compiler sees: comments and
+    whitespace may change, code and string literals may not."""
+    a = 'int x = 1; // note\n/* block */ asm("add.f32 %0, %1; // not a comment");\n'
+    b = 'int x = 1;   /* reworded note */\n\n asm("add.f32 %0, %1; // not a comment");'
+    c = 'int x = 2; asm("add.f32 %0, %1; // not a comment");'
+    d = 'int x = 1; asm("add.f32 %0, %1; // changed");'
+    assert bench._code_text(a) == bench._code_text(b)
+    assert bench._code_text(a) != bench._code_text(c)
+    assert bench._code_text(a) != bench._code_text(d)
+    assert bench._code_text("char q = '\\''; // x") == "char q = '\\'';"
