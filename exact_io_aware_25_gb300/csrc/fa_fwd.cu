@@ -11,7 +11,7 @@
 // then only O and the per-row statistic (lse = m + ln l) are written.
 //
 // GB300 mapping (one CTA per (query tile, b*h); 6 warps; two CTAs share an SM:
-// 256 TMEM columns and ~99 KB of shared memory each):
+// 256 TMEM columns and 100 KiB of shared memory each):
 //   warp 4   TMA producer: Q once, then K_j (3-stage ring, one tile ahead) and
 //            V_j (2-stage ring).
 //   warp 5   TMEM owner and MMA issuer: S = Q K_j^T (M=128, N=128, K=64)

@@ -6,7 +6,7 @@
 // "Method": S_ij on chip, running max and exponential sum, rescaled partial
 // output, only O and lse written), with a layout for the wider head:
 //
-// One CTA per (query tile, b*h) and per SM (195 KiB of shared memory, all
+// One CTA per (query tile, b*h) and per SM (199 KiB of shared memory, all
 // 512 TMEM columns); 10 warps:
 //   warp 8   TMA producer: Q once, K_j (3-stage ring, two tiles ahead) and
 //            V_j (2-stage ring).  Each 128 x 128 bf16 tile is two 128 x 64
