@@ -63,6 +63,10 @@ def _allowed_np(B, N, causal=False, kv_len=None, block_mask=None, block=128):
 
 def _evalnum(x):
     if isinstance(x, str):
+        if x == "-inf":
+            return -math.inf
+        if "+" in x:
+            return sum(_evalnum(t) for t in x.split("+"))
         if "*" in x:
             a, b = x.split("*")
             return float(a) * _evalnum(b)
@@ -95,6 +99,31 @@ def test_closed_form_golden(oracle_mod, case):
     np.testing.assert_allclose(dq.reshape(N, d), _arr(case["dq"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dk.reshape(N, d), _arr(case["dk"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv.reshape(N, d), _arr(case["dv"]), rtol=0, atol=1e-12)
+
+
+GOLDEN_QK = os.path.join(os.path.dirname(GOLDEN), "closed_form_qk.json")
+
+
+@pytest.mark.parametrize("case", json.load(open(GOLDEN_QK))["cases"], ids=lambda c: c["name"])
+def test_closed_form_golden_short_queries(oracle_mod, case):
+    """Nq != Nk with bottom-right causal: forward_qk and backward_qk against
+    hand-derived values (tests/golden/closed_form_qk.json)."""
+    B, H, Nq, Nk, d = case["B"], case["H"], case["Nq"], case["Nk"], case["d"]
+    q = _arr(case["q"]).reshape(B, H, Nq, d)
+    k = _arr(case["k"]).reshape(B, H, Nk, d)
+    v = _arr(case["v"]).reshape(B, H, Nk, d)
+    do = _arr(case["do"]).reshape(B, H, Nq, d)
+    o, lse = oracle_mod.forward_qk(q, k, v, case["scale"], causal=True)
+    np.testing.assert_allclose(o.reshape(Nq, d), _arr(case["o"]), rtol=0, atol=1e-12)
+    want = np.array([_evalnum(x) for x in case["lse"]])
+    got = lse.reshape(Nq)
+    assert np.array_equal(np.isneginf(got), np.isneginf(want))
+    fin = np.isfinite(want)
+    np.testing.assert_allclose(got[fin], want[fin], rtol=0, atol=1e-12)
+    dq, dk, dv = oracle_mod.backward_qk(q, k, v, do, case["scale"], causal=True)
+    np.testing.assert_allclose(dq.reshape(Nq, d), _arr(case["dq"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.reshape(Nk, d), _arr(case["dk"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv.reshape(Nk, d), _arr(case["dv"]), rtol=0, atol=1e-12)
 
 
 # ---------------------------------------------------------------- invariants
