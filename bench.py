@@ -2,17 +2,21 @@
 """Benchmark: exact attention forward + backward on one GB300 (or N replicas).
 
 One step = one pass of the whole hot path over one batch: fa_fwd (forward
-kernel) then fa_bwd (D preprocess, dK/dV/dQ kernel, dQ convert), on the
-BERT-large-shaped encoder workload B=16 H=16 N=512 d=64 with per-sequence key
-padding (kv_len uniform in [256, 512]), bf16 storage, fp32 accumulation.
-Inputs are synthetic (seeded normals, see workloads.py).
+kernel) then fa_bwd (D preprocess, block-sparse column lists, dK/dV/dQ
+kernel, dQ convert), by default on the block-sparse long-sequence workload
+B=1 H=8 N=65536 d=64 with a 512x512 mask of 128x128 blocks (a diagonal band
+of width 3 plus uniformly random blocks, 5% nonzero), bf16 storage, fp32
+accumulation: the largest of the five configurations and one inside the
+N >= 4K, d = 64 regime.  Inputs are synthetic (seeded normals, see
+workloads.py); --workload selects the others.
 
 Timing: W warm-up steps, then exactly K steps, each bracketed by CUDA events
 on the launching stream; L2 is flushed (a 256 MiB buffer is rewritten)
 between steps, outside the events.  A barrier and a device synchronise
 bracket the timed loop; the per-rank time is the sum of the step events and
 the job time is the maximum over ranks.  value = counted FLOPs of all ranks
-/ job time.  FLOPs: 4*N*kv_len*d per (b, h) forward, 2.5x that backward.
+/ job time.  FLOPs: 4*N*L*d per (b, h) forward (L = key bound, x0.5 causal,
+x nonzero-block fraction), 2.5x that backward.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch one process per GPU with torch.distributed.run; every rank
@@ -30,13 +34,15 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
 UNIT = "TFLOP/s"
-WORKLOAD = "bert"
+WORKLOAD = "sparse64k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
 # forward, D preprocess, dK/dV/dQ, dQ convert; plus the column-list kernel
@@ -116,6 +122,15 @@ def load_traffic(kernel: str, workload: str):
     if entry.get("sources") != _sources_hash(KERNEL_SOURCES[kernel]):
         return None
     return entry.get("bytes")
+
+
+def step_stats(ms):
+    """Per-step spread of CUDA-event times (ms): mean, min, median, p90, max."""
+    xs = sorted(ms)
+    n = len(xs)
+    pick = lambda f: xs[min(n - 1, max(0, int(math.ceil(f * n)) - 1))]
+    return {"mean": statistics.mean(xs), "min": xs[0], "p50": statistics.median(xs),
+            "p90": pick(0.9), "max": xs[-1], "n": n}
 
 
 def counted_flops(spec, kv_len, block_mask=None):
@@ -299,30 +314,97 @@ def time_oracle(w, budget_s: float, max_units=None, dropout=0.0, seed=0):
 # ---------------------------------------------------------------- arms
 
 
+def allowed_keys(spec, kv_len, block_mask, b, i):
+    """Number of keys query row i of batch b attends to (for FLOP counting)."""
+    N = spec.N
+    L = N if kv_len is None else max(0, min(int(kv_len[b]), N))
+    lim = min(L, i + 1) if spec.causal else L
+    if block_mask is None:
+        return lim
+    row = block_mask[i // 128]
+    full_tiles = lim // 128
+    n = 128 * int(np.count_nonzero(row[:full_tiles]))
+    if lim % 128 and row[full_tiles]:
+        n += lim % 128
+    return n
+
+
+def time_oracle_rows(w, rows, dropout=0.0, seed=0):
+    """Times the oracle's forward and the dQ side of its backward on the given
+    global query rows (bh * N + i); returns (flops counted, seconds, threads).
+    Counted per row: 4*L*d forward plus 6*L*d backward (S, dP and dQ, the
+    part of the 10*L*d backward convention that belongs to the row's dQ);
+    the key-side dK / dV work is not part of this sample."""
+    import oracle
+    spec = w.spec
+    threads = os.cpu_count() or 1
+    p8 = oracle.drop_p8(dropout) if dropout > 0 else 0
+    q, k, v, do = (w.f64(n) for n in ("q", "k", "v", "do"))
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, spec.scale, causal=spec.causal, kv_len=w.kv_len,
+                   block_mask=w.block_mask, rows=rows, nthreads=threads, p8=p8, seed=seed)
+    oracle.backward(q, k, v, do, spec.scale, causal=spec.causal, kv_len=w.kv_len,
+                    block_mask=w.block_mask, q_rows=rows, k_rows=np.zeros(0, np.int64),
+                    nthreads=threads, p8=p8, seed=seed)
+    t = time.perf_counter() - t0
+    flops = 0.0
+    for g in rows:
+        bh, i = divmod(int(g), spec.N)
+        flops += 10.0 * allowed_keys(spec, w.kv_len, w.block_mask, bh // spec.H, i) * spec.d
+    return flops, t, threads
+
+
 def run_reference(args, rank, world):
-    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    """The oracle as it stands, timed on the host cores (rank 0 only).  Each
+    step is a bounded sample of the workload: whole (b, h) heads (forward +
+    backward) when one head fits the per-step budget, else seeded query rows
+    spread over the heads (forward + the dQ side of the backward)."""
     if rank != 0:
         return 0
     import workloads as W
     w = W.make(args.workload) if args.head_dim == 64 else W.make(args.workload, d=args.head_dim)
-    # calibrate one head, then size each step to keep the whole run to ~2 minutes
-    f1, t1, _, threads = time_oracle(w, 0.0, max_units=1, dropout=args.dropout, seed=args.seed)
+    spec = w.spec
     per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
-    heads_per_step = max(1, min(w.spec.B * w.spec.H, int(per_step_budget / max(t1, 1e-6))))
+    rng = np.random.default_rng(4242)
+    total_rows = spec.B * spec.H * spec.N
+    # per-row cost from a small probe, to decide between whole heads and rows
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, 64), replace=False))
+    f_p, t_p, threads = time_oracle_rows(w, probe, dropout=args.dropout, seed=args.seed)
+    head_est = t_p / len(probe) * spec.N * 1.4
+    if head_est <= per_step_budget:
+        f1, t1, _, threads = time_oracle(w, 0.0, max_units=1, dropout=args.dropout,
+                                         seed=args.seed)
+        heads_per_step = max(1, min(spec.B * spec.H, int(per_step_budget / max(t1, 1e-6))))
+        run = lambda: time_oracle(w, float("inf"), max_units=heads_per_step,
+                                  dropout=args.dropout, seed=args.seed)[:2]
+        sample = (f"{heads_per_step} of {spec.B * spec.H} (b, h) heads per step "
+                  f"(forward + backward, full rows)")
+    else:
+        # blocks of 64 consecutive query rows (half a tile: rows that share
+        # their allowed key tiles), drawn uniformly over all heads
+        blk = 64
+        n_blocks = total_rows // blk
+        per_blk = max(t_p / len(probe), 1e-9) * blk
+        nb = max(1, min(n_blocks, int(per_step_budget / per_blk)))
+        steps_rows = [(np.sort(rng.choice(n_blocks, size=nb, replace=False))[:, None] * blk
+                       + np.arange(blk)[None, :]).ravel() for _ in range(args.steps)]
+        it = iter(steps_rows)
+        run = lambda: time_oracle_rows(w, next(it), dropout=args.dropout, seed=args.seed)[:2]
+        sample = (f"{nb * blk} of {total_rows} query rows per step ({nb} blocks of {blk} "
+                  f"consecutive rows drawn uniformly over the (b, h) heads, seed 4242): forward "
+                  f"+ the dQ side of the backward, counted at 10*L*d per row (one whole head, "
+                  f"forward + backward, takes about {head_est:.0f} s here)")
     for _ in range(args.warmup):
-        time_oracle(w, 0.0, max_units=heads_per_step, dropout=args.dropout, seed=args.seed)
+        time_oracle_rows(w, probe, dropout=args.dropout, seed=args.seed)
     tot_f, tot_t = 0.0, 0.0
     for _ in range(args.steps):
-        f, t, _, _ = time_oracle(w, float("inf"), max_units=heads_per_step,
-                                 dropout=args.dropout, seed=args.seed)
+        f, t = run()
         tot_f += f
         tot_t += t
     value = tot_f / tot_t / 1e12
-    sample = (f"{heads_per_step} of {w.spec.B * w.spec.H} (b, h) heads per step "
-              f"(forward + backward, full rows)")
     line = {
         "impl": "reference",
-        "metric": METRIC if w.spec.d == 64 else METRIC.replace("(bf16,", f"(bf16, d={w.spec.d},"),
+        "metric": METRIC if spec.d == 64 else METRIC.replace("(bf16,", f"(bf16, d={spec.d},"),
         "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
@@ -387,12 +469,21 @@ def run_ours(args, rank, world, local):
     kv_len = torch.from_numpy(w.kv_len).to(device) if w.kv_len is not None else None
     mask = (torch.from_numpy(w.block_mask).to(device) if w.block_mask is not None else None)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    stream = torch.cuda.current_stream(device)
+    # Auxiliary memory, measured: everything allocated beyond the inputs
+    # (Q, K, V, dO, masks) and the outputs O, dQ, dK, dV from here until one
+    # forward + backward has finished -- the lse the forward leaves for the
+    # backward and the backward's workspace -- as the allocator's peak, and
+    # the device's free memory before and after (the library itself
+    # allocates nothing).
+    torch.cuda.synchronize(device)
+    base_alloc = torch.cuda.memory_allocated(device)
+    torch.cuda.reset_peak_memory_stats(device)
+    free0 = torch.cuda.mem_get_info(device)[0]
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
 
     p_drop, seed = args.dropout, args.seed
 
@@ -414,6 +505,22 @@ def run_ours(args, rank, world, local):
     def step():
         fwd_call()
         bwd_call()
+
+    step()
+    torch.cuda.synchronize(device)
+    fa.fa_check(stream)
+    aux_peak = torch.cuda.max_memory_allocated(device) - base_alloc
+    aux_free_delta = free0 - torch.cuda.mem_get_info(device)[0]
+    materialised = 2 * B * H * N * N * 2
+    aux = {"measured_peak_bytes": int(aux_peak),
+           "lse_bytes": int(lse.numel() * 4), "workspace_bytes": int(ws_bytes),
+           "device_free_delta_bytes": int(aux_free_delta),
+           "materialised_s_p_bf16_bytes": int(materialised),
+           "ratio_materialised_over_measured": materialised / max(1, aux_peak),
+           "how": "torch allocator peak above the inputs and outputs over one fa_fwd + fa_bwd "
+                  "(lse + backward workspace); device free-memory delta over the same span "
+                  "(allocator rounding included); baseline = S and P in bf16 for every (b, h)"}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1)
@@ -450,6 +557,8 @@ def run_ours(args, rank, world, local):
     step_ms = [ev_step0[i].elapsed_time(ev_step1[i]) for i in range(K)]
     fwd_ms = [ev_step0[i].elapsed_time(ev_fwd1[i]) for i in range(K)]
     bwd_main_ms = [bm0[i].elapsed_time(bm1[i]) for i in range(K)]
+    spread = {"step": step_stats(step_ms), "fwd": step_stats(fwd_ms),
+              "bwd_main": step_stats(bwd_main_ms)}
     t_rank = sum(step_ms) / 1e3
     t_job = max_over_ranks(t_rank, world, device)
     value = fl["step"] * K * world / t_job / 1e12
@@ -521,10 +630,14 @@ def run_ours(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, t, heads, threads = time_oracle(w, args.cpu_budget, dropout=p_drop, seed=seed)
+        est = t * fl["step"] / f   # the same rate over the whole workload
         cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{heads} of {B * H} (b, h) heads, forward + backward, full rows; "
                          f"{t:.1f} s of fp64 C oracle work",
-               "seconds": t}
+               "seconds": t,
+               "extrapolated_full_workload_s": est,
+               "extrapolation": f"the sampled heads' time scaled by counted FLOPs to all "
+                                f"{B * H} heads (labelled estimate, not measured)"}
 
     if rank == 0:
         line = {
@@ -540,9 +653,9 @@ def run_ours(args, rank, world, local):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": (KERNELS_PER_STEP + (w.block_mask is not None)) * K,
             "clocks": sampler.summary(),
+            "step_ms_stats": spread,
             "wall_s_timed_region": wall,
-            "peak_aux_bytes": ws_bytes,
-            "materialised_s_p_bytes": 2 * B * H * N * N * 2,
+            "aux_memory": aux,
         }
         print(json.dumps(line), flush=True)
     return 0
@@ -813,7 +926,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="workload name from workloads.py (the reported line uses bert), or "
+                    help="workload name from workloads.py (the reported line uses sparse64k), or "
                          "'decode' for the split-KV forward on a decode-shaped problem")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=12.0)

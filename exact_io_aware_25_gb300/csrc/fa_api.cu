@@ -14,6 +14,35 @@ namespace fa {
 // Device error word written by kernels whose bounded waits ran out.
 __device__ int g_dev_error;
 
+// The two driver calls are resolved through the runtime's entry-point query,
+// like cuTensorMapEncodeTiled, so that the library loads (for its host-side
+// checks) on a machine without the driver.
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c) return 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -23,7 +52,10 @@ std::mutex g_mu;
 long long g_timeout_ns = kDefaultTimeoutNs;
 int g_starve_next = 0;
 cudaEvent_t g_bwd_ev_start = nullptr, g_bwd_ev_stop = nullptr;
+// Device address of the error word, per device, with the identifier of the
+// context it was looked up in (the address is only valid in that context).
 int *g_err_ptr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -58,10 +90,14 @@ fa_status device_setup(int *dev_out, int **err_out) {
     g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
-  if (!g_err_ptr[dev]) {
+  // looked up again whenever the current context is not the one the cached
+  // address came from (another context made current, or the device reset)
+  const unsigned long long ctx = current_context_id();
+  if (!g_err_ptr[dev] || ctx == 0 || ctx != g_err_ctx[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess || !p) return FA_ERR_CUDA;
     g_err_ptr[dev] = static_cast<int *>(p);
+    g_err_ctx[dev] = current_context_id();  // the lookup creates the primary context if needed
   }
   *dev_out = dev;
   *err_out = g_err_ptr[dev];

@@ -299,8 +299,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
         const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
-        if (edge) exp_half<0, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);  // exact zeros where masked
-        else exp_half<kPolyPer8, kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);
+        exp_half<kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);  // exact zeros where masked
         if (half == 0 && it > 0) {
           if (!mbar_wait_warp_fast(&s.bar_o_done, (it - 1) & 1, pr.wait, &s.abort)) {
             ok = false;

@@ -16,45 +16,6 @@ namespace fa {
 // Exact: O / l and lse use the same reference.
 constexpr float kLazyRescale = 8.f;
 
-// Coefficients of 2^f on [-1/2, 1/2]: Chebyshev interpolation at 5 nodes
-// (gen_exp2_poly.py), relative error below 4e-6.
-constexpr float kExp2C0 = 1.000000000e+00f, kExp2C1 = 6.931210160e-01f,
-                kExp2C2 = 2.402234972e-01f, kExp2C3 = 5.592197552e-02f,
-                kExp2C4 = 9.666368365e-03f;
-
-// 2^x for x in [-126, 9) without the MUFU unit: n = round(x) from the
-// 1.5 * 2^23 rounding trick, f = x - n in [-1/2, 1/2], 2^f by the degree-4
-// polynomial above, and n added to the exponent field.  Inputs below -126
-// are clamped (result ~1e-38, never used where an exact 0 is required: edge
-// tiles take the MUFU path).
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;
-  const float n = t - 12582912.f;
-  const float r = x - n;
-  const float q =
-      fmaf(fmaf(fmaf(fmaf(kExp2C4, r, kExp2C3), r, kExp2C2), r, kExp2C1), r, kExp2C0);
-  const int ni = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(q) + (ni << 23));
-}
-
-// exp2_poly on two values at once with the packed fp32 pair instructions
-// (the same operations, each rounded as in the scalar version).
-__device__ __forceinline__ void exp2_poly2(float &y0, float &y1, float x0, float x1) {
-  x0 = fmaxf(x0, -126.f);
-  x1 = fmaxf(x1, -126.f);
-  float t0, t1, n0, n1, r0, r1, q0, q1;
-  add2(t0, t1, x0, x1, 12582912.f, 12582912.f);
-  sub2(n0, n1, t0, t1, 12582912.f, 12582912.f);
-  sub2(r0, r1, x0, x1, n0, n1);
-  fma2(q0, q1, kExp2C4, kExp2C4, r0, r1, kExp2C3, kExp2C3);
-  fma2(q0, q1, q0, q1, r0, r1, kExp2C2, kExp2C2);
-  fma2(q0, q1, q0, q1, r0, r1, kExp2C1, kExp2C1);
-  fma2(q0, q1, q0, q1, r0, r1, kExp2C0, kExp2C0);
-  y0 = __int_as_float(__float_as_int(q0) + ((__float_as_int(t0) - 0x4B400000) << 23));
-  y1 = __int_as_float(__float_as_int(q1) + ((__float_as_int(t1) - 0x4B400000) << 23));
-}
-
 // Dropout state of one query row: hash key with the row pair folded in, the
 // bit offset of the row's two bytes in each block word, the threshold.
 struct RowDrop {
@@ -66,13 +27,10 @@ struct RowDrop {
 // Exponentials of 64 consecutive S columns sv[0..64) of a row: sv[c] <-
 // 2^(sv[c]*sl2 - m), accumulated into the eight partial sums (before
 // dropout) and packed to bf16 pairs in pk, with dropped elements packed as 0
-// when kDrop (jp0 = key pair index of sv[0]).  In every group of eight
-// columns the first kPoly (even) use exp2_poly2 (FMA pipe), the rest the MUFU
-// unit.
-template <int kPoly, bool kDrop>
+// when kDrop (jp0 = key pair index of sv[0]).
+template <bool kDrop>
 __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8)[8],
                                       uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
-  static_assert(kPoly % 2 == 0 && kPoly <= 8, "polynomial exponentials go in pairs");
 #pragma unroll
   for (int c = 0; c < 64; c += 8) {
     float x[8];
@@ -80,14 +38,7 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
     for (int u = 0; u < 8; u += 2)
       fma2(x[u], x[u + 1], sv[c + u], sv[c + u + 1], sl2, sl2, -m, -m);
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      if (u < kPoly) {
-        exp2_poly2(sv[c + u], sv[c + u + 1], x[u], x[u + 1]);
-      } else {
-        sv[c + u] = ex2_approx(x[u]);
-        sv[c + u + 1] = ex2_approx(x[u + 1]);
-      }
-    }
+    for (int u = 0; u < 8; ++u) sv[c + u] = ex2_approx(x[u]);
 #pragma unroll
     for (int u = 0; u < 8; u += 2)
       add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
@@ -107,17 +58,12 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
 
 // exp64 on the 64-column half `half` of a 128-column row (jp0: the tile's
 // first key pair).
-template <int kPoly, bool kDrop>
+template <bool kDrop>
 __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
                                          float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
                                          uint32_t jp0) {
-  exp64<kPoly, kDrop>(sv + half * 64, sl2, m, rs8, pk, rd, jp0 + static_cast<uint32_t>(half * 32));
+  exp64<kDrop>(sv + half * 64, sl2, m, rs8, pk, rd, jp0 + static_cast<uint32_t>(half * 32));
 }
-
-#ifndef FA_FWD_POLY_PER8
-#define FA_FWD_POLY_PER8 0
-#endif
-constexpr int kPolyPer8 = FA_FWD_POLY_PER8;
 
 
 // Masks of C consecutive S columns of a row on an edge tile: columns at or

@@ -319,8 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t pk[32];
         const uint32_t jp0 = static_cast<uint32_t>(kc0 >> 1);
-        if (edge) exp64<0, kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
-        else exp64<kPolyPer8, kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
+        exp64<kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
         tmem_st32(tmem + lane_base + kColP + static_cast<uint32_t>(bf) * 64 + ch * 32, pk);
       }
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));

@@ -142,6 +142,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 size_t fwd_smem_bytes();
 size_t bwd_smem_bytes();
 
+// Unique identifier of the CUDA context current on the calling host thread
+// (cuCtxGetId), 0 when there is none yet.  A device address looked up with
+// cudaGetSymbolAddress is valid only in the context it was looked up in; the
+// host code caches such addresses together with this identifier.
+unsigned long long current_context_id();
+
 // Expands a CSR block mask (row_ptr [nb + 1], col_idx [nnz]) into the dense
 // nb x nb uint8 form (fa_bwd.cu); bad entries are skipped and recorded as
 // kDevBadArg in *err.

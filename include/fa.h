@@ -182,19 +182,27 @@ FA_API fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, voi
  * device memory when they run the backward pass (for instance a plugin whose
  * host application owns every device allocation, or a latency-critical loop
  * that must not allocate).  The paper has no counterpart: this is a
- * deployment variant of fa_bwd with identical arguments, results and rules
- * apart from the workspace.
+ * deployment variant of fa_bwd with identical arguments, results and status
+ * codes apart from the workspace (it runs fa_bwd's own argument checks
+ * first, so an argument fa_bwd rejects is rejected here with the same code).
  *   Scratch comes from a fixed array inside the library's device image of
- *   fa_bwd_noalloc_max_scratch_bytes() bytes (64 MiB), held on every GPU that
- *   loads the library until the process exits.  A problem whose
+ *   fa_bwd_noalloc_max_scratch_bytes() bytes (64 MiB).  A problem whose
  *   fa_bwd_workspace_size() exceeds it is rejected with FA_ERR_WORKSPACE
  *   before anything is launched.
- *   The first call on a device looks the array's device address up (with
- *   that device current); make that first call before any stream capture.
+ *   The array is reserved in device memory when the module holding it is
+ *   loaded into a context: under CUDA's default lazy module loading that is
+ *   the first call on each device, which therefore allocates those 64 MiB
+ *   implicitly, can fail with FA_ERR_CUDA when the device lacks the memory,
+ *   and may synchronise; it stays reserved until the context is destroyed.
+ *   Make the first call on a device outside latency-critical code and before
+ *   any stream capture.  The array's device address is cached per device and
+ *   per context (a call in another context, or after a device reset, looks
+ *   it up again).
  *   All calls share the one array: calls that overlap on the GPU race and
  *   must be ordered by the caller.  Nothing needs clearing between calls;
  *   each call rewrites the scratch it reads.
- *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   After its first call on a device it allocates nothing: no cudaMalloc,
+ *   cudaFree or allocating library call.
  */
 FA_API fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                 const float *lse, const void *dout, void *dq, void *dk,

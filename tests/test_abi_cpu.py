@@ -235,3 +235,26 @@ def test_api_variant_validation_without_gpu(fa_lib):
     assert bcsr(rp=None) == -1
     assert bcsr(nbytes=need - 1) == -6 and bcsr(ws=None) == -6
     assert bcsr(dq=FAKE + 2) == -3
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dq=None), dict(B=0), dict(scale=-1.0), dict(d=96), dict(dq=FAKE + 2),
+    dict(N=65535 * 128 + 1),                     # too many query tiles: unsupported
+    dict(N=1024 * 128 + 1, block_mask=FAKE),     # block mask wider than 1024 tiles: unsupported
+    dict(B=1 << 16, H=1 << 16, N=1),
+    dict(H=8, N=65536),                          # valid, but beyond the fixed scratch
+])
+def test_noalloc_status_equals_fa_bwd_status_without_gpu(fa_lib, kw):
+    """fa_bwd_noalloc gives every argument set fa_bwd rejects the code fa_bwd
+    gives it; arguments fa_bwd accepts but whose workspace exceeds the fixed
+    scratch get FA_ERR_WORKSPACE.  No call here reaches a device."""
+    L = fa_lib.lib()
+    a = dict(dq=FAKE, B=1, H=1, N=128, d=64, scale=0.125, block_mask=None)
+    a.update(kw)
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["dq"], FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+            a["scale"], 0, None, a["block_mask"])
+    want = L.fa_bwd(*args, None, 0, None)
+    got = L.fa_bwd_noalloc(*args, None)
+    assert got == want
+    if kw.get("N") == 65536:
+        assert want == -6 and got == -6

@@ -91,3 +91,32 @@ def test_traffic_hash_ignores_comments_but_not_code():
     assert bench._code_text(a) != bench._code_text(c)
     assert bench._code_text(a) != bench._code_text(d)
     assert bench._code_text("char q = '\\''; // x") == "char q = '\\'';"
+
+
+def test_allowed_keys_is_the_support_of_the_oracles_probabilities(oracle_mod):
+    """The reference arm's row sample counts 10*L*d per row with L from
+    bench.allowed_keys: L must be the number of keys with nonzero P in the
+    oracle, for every mask kind (ragged N, causal, key padding, block mask)."""
+    rng = np.random.default_rng(5)
+    mask = (rng.random((3, 3)) < 0.5).astype(np.uint8)
+    mask[2, 0] = 1
+    for causal, kv, bm in [(False, None, None), (True, None, None),
+                           (False, np.array([300, 137], np.int32), None),
+                           (True, np.array([251, 300], np.int32), mask),
+                           (False, None, mask)]:
+        w = W.make("tiny", seed=8, B=2, H=1, N=300, causal=causal)
+        q, k = w.f64("q"), w.f64("k")
+        for b in range(2):
+            P = oracle_mod.probs(q, k, w.spec.scale, bh=b, causal=causal, kv_len=kv,
+                                 block_mask=bm)
+            for i in range(300):
+                want = int(np.count_nonzero(P[i]))
+                assert bench.allowed_keys(w.spec, kv, bm, b, i) == want, (causal, b, i)
+
+
+def test_reference_row_sample_counts_its_rows(oracle_mod):
+    w = W.make("tiny", seed=9, B=1, H=2, N=256, causal=True)
+    rows = np.array([0, 5, 255, 256 + 17], np.int64)
+    f, t, threads = bench.time_oracle_rows(w, rows)
+    assert t > 0 and threads >= 1
+    assert f == 10.0 * 64 * sum([1, 6, 256, 18])

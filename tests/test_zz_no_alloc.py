@@ -48,6 +48,31 @@ def test_noalloc_backward_matches_workspace_backward_twice(fa_lib):
             assert torch.equal(got[2].view(torch.int16), ref[2].view(torch.int16))
 
 
+def test_noalloc_block_mask_matches_workspace_backward(fa_lib):
+    """A block-sparse mask through the fixed scratch: the per-key-tile query
+    lists the backward builds live in that array too.  A 4 x 4 mask with an
+    empty key column (its dK, dV must be 0) and an empty query row."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_io_aware_25_gb300 as fa
+    import gpu_harness as H
+    import workloads as W
+    mask = np.array([[1, 0, 1, 0],
+                     [0, 1, 1, 0],
+                     [0, 0, 0, 0],
+                     [1, 1, 0, 0]], np.uint8)
+    x = H.Inputs(W.make("tiny", seed=97, B=2, H=3, N=512), block_mask=mask)
+    o, lse = H.run_fwd(x)
+    ref = _run(fa, W, H, False, x, o, lse)
+    for _ in range(2):
+        got = _run(fa, W, H, True, x, o, lse)
+        H.assert_grad(H.host_f64(got[0]), H.host_f64(ref[0]), "dQ")
+        assert torch.equal(got[1].view(torch.int16), ref[1].view(torch.int16))
+        assert torch.equal(got[2].view(torch.int16), ref[2].view(torch.int16))
+        # key tile 3 is attended by no query tile
+        assert torch.all(got[1][:, :, 384:].float() == 0) and torch.all(got[2][:, :, 384:].float() == 0)
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(fa_lib):
     import exact_io_aware_25_gb300 as fa
     limit = fa.fa_bwd_noalloc_max_scratch_bytes()
