@@ -185,7 +185,19 @@ Problem make_problem(int B, int H, int N, float scale, int causal, const int32_t
   p.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
   p.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.keep_scale = 256.f / static_cast<float>(256 - p8);
+  p.head_group = B * H;
   return p;
+}
+
+// Heads per scheduling group (Problem::head_group): as many as fit their
+// re-read rows, per_head_bytes each, into about half of the 129 MB L2.
+int heads_per_group(int B, int H, size_t per_head_bytes) {
+  constexpr size_t kL2Budget = size_t(64) << 20;
+  const size_t bh = static_cast<size_t>(B) * H;
+  size_t g = per_head_bytes > 0 ? kL2Budget / per_head_bytes : bh;
+  if (g < 1) g = 1;
+  if (g > bh) g = bh;
+  return static_cast<int>(g);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -294,6 +306,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   a.pr.d = d;
   a.pr.Nk = Nk;
   a.pr.causal_off = Nk - N;
+  // the rows every query tile re-reads: K and V of its head
+  a.pr.head_group = heads_per_group(B, H, 4 * static_cast<size_t>(Nk) * d);
   a.lse = lse;
   a.row_m = x.row_m;
   a.row_l = x.row_l;
@@ -419,6 +433,9 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.pr.d = d;
   a.pr.Nk = Nk;
   a.pr.causal_off = Nk - N;
+  // the rows every key tile re-reads: Q and dO (bf16) and the fp32 dQ
+  // accumulators of its head
+  a.pr.head_group = heads_per_group(B, H, 8 * static_cast<size_t>(N) * d);
   a.n_pad = static_cast<int>(align_up(static_cast<size_t>(N), kTile));
   a.nkt = (Nk + kTile - 1) / kTile;
   a.o = static_cast<const uint16_t *>(o);

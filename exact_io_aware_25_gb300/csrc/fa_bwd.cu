@@ -192,8 +192,12 @@ __global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
 // Its first item is t = blockIdx.x; later ones are claimed from a global
 // counter by the producer warp and handed to the other roles through a small
 // ring in shared memory, so CTAs that drew short items take more of them.
-// Items are numbered key-tile major: under a causal mask the longest items
-// (small kt) are handed out first.
+// Items are numbered by work_order: groups of heads whose Q, dO and fp32 dQ
+// accumulators fit in L2 together, and within a group key tile by key tile
+// (the longest causal items, small kt, first) with the group's heads
+// fastest.  On long sequences a group is one or two heads, so the dQ
+// reduce-adds and the Q / dO re-reads stay in L2; on short ones it is every
+// head, which keeps one global longest-first order.
 // K_j and V_j are double-buffered across items and every ring runs on one
 // step counter for the whole CTA, so the next item's loads and first
 // S^T / dP^T overlap the current item's last step and epilogue.
@@ -274,10 +278,8 @@ struct Item {
 
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
-  const int BH = pr.B * pr.H;
   Item it;
-  it.kt = t / BH;
-  it.bh = t - it.kt * BH;
+  work_order(pr, t, a.nkt, it.bh, it.kt);
   it.kv_bound = key_bound(pr, it.bh / pr.H);
   it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   if (it.kt * kTile >= it.kv_bound) it.n = 0;
@@ -826,8 +828,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!mbar_wait_warp(&s.bar_epi_full[kb], (u >> 1) & 1, pr.wait, &s.abort)) break;
         const int t = s.epi_item[kb];
         if (t < 0) break;
-        const int BH = pr.B * pr.H;
-        const int kt = t / BH, bh = t - (t / BH) * BH;
+        int bh, kt;
+        work_order(pr, t, a.nkt, bh, kt);
         if (lane == 0) {
           tma_store_3d(&tm_dv, s.kv[kb][1], 0, kt * kTile, bh);
           tma_store_3d(&tm_dk, s.kv[kb][0], 0, kt * kTile, bh);

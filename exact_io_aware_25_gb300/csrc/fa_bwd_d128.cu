@@ -10,8 +10,8 @@
 // dQ partial is produced transposed, dQ^T = K^T dS^T (M = d = 128, N = 64
 // queries), so it needs 64 TMEM columns instead of 128.
 //
-// Persistent, one CTA per SM walking the work items (key tile kt, head b*h)
-// from a global counter like the d = 64 kernel; K_j and V_j (32 KiB each)
+// Persistent, one CTA per SM walking the work items (key tile kt, head b*h),
+// numbered by work_order, from a global counter like the d = 64 kernel; K_j and V_j (32 KiB each)
 // have a single buffer, which also stages dK / dV for the store.
 //
 // Warp roles (16 warps):
@@ -98,10 +98,8 @@ struct Item {
 
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
-  const int BH = pr.B * pr.H;
   Item it;
-  it.kt = t / BH;
-  it.bh = t - it.kt * BH;
+  work_order(pr, t, a.nkt, it.bh, it.kt);
   it.kv_bound = key_bound(pr, it.bh / pr.H);
   it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   int tiles;
@@ -624,8 +622,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (!mbar_wait_warp(&s.bar_epi_full, u & 1, pr.wait, &s.abort)) break;
         const int t = s.epi_item;
         if (t < 0) break;
-        const int BH = pr.B * pr.H;
-        const int kt = t / BH, bh = t - (t / BH) * BH;
+        int bh, kt;
+        work_order(pr, t, a.nkt, bh, kt);
         if (lane == 0) {
           tma_store_3d(&tm_dv, s.kv[1], 0, kt * kTile, bh);
           tma_store_3d(&tm_dv, s.kv[1] + kKvHalf, 64, kt * kTile, bh);

@@ -69,7 +69,7 @@ __device__ __forceinline__ int tile_at(const FwdSmem &s, bool sparse, int it) {
 
 constexpr uint32_t kSoftmaxWarps = 4;
 
-// kDrop: fused dropout; kSplit: split-KV partial (key range per blockIdx.z,
+// kDrop: fused dropout; kSplit: split-KV partial (key range per blockIdx.y,
 // fp32 partial outputs for the merge kernel).
 template <bool kDrop, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -83,10 +83,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = args.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // blockIdx.x (the head) varies fastest in launch order, so every head's last
-  // query tile, the heaviest under a causal mask, is dispatched first.
-  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.y);
-  const int bh = blockIdx.x;
+  // Launch order (work_order): groups of heads whose K and V fit in L2
+  // together, and within a group the last query tile of every head first,
+  // so that the heaviest causal tiles start first while the CTAs resident at
+  // one time re-read only a few heads' K and V.
+  int bh, qrank;
+  work_order(pr, static_cast<int>(blockIdx.x), pr.nt, bh, qrank);
+  const int qt = pr.nt - 1 - qrank;
   const int b = bh / pr.H;
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (kSplit) {
     // split-KV (no causal, no block mask): this CTA's contiguous range of key tiles
     const int per = (n_kv + args.n_split - 1) / args.n_split;
-    j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
+    j_begin = min(n_kv, static_cast<int>(blockIdx.y) * per);
     j_end = min(n_kv, j_begin + per);
   }
   const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (kSplit) {
           // split-KV partial: O_s = O / l_s (fp32) and lse_s of this row, for the merge
           if (qrow < pr.N) {
-            const size_t prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
+            const size_t prow = (static_cast<size_t>(blockIdx.y) * (pr.B * pr.H) + bh) *
                                     static_cast<size_t>(args.nq_pad) + qrow;
             float4 *dst = reinterpret_cast<float4 *>(args.part_o + prow * kHeadDim);
 #pragma unroll
@@ -389,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!kSplit && tid == 0 && ok && !s.abort) {
       tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
       bulk_commit();
-      bulk_wait_all();
+      // the CTA may leave once the store has read shared memory; the grid's
+      // completion covers the global writes
+      bulk_wait_read_all();
     }
   }
   tc_fence_before();
@@ -431,7 +436,7 @@ cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   cudaError_t e = launch_fwd_config();
   if (e != cudaSuccess) return e;
   const size_t smem = fwd_smem_bytes();
-  dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
+  dim3 grid(a.pr.nt * a.pr.B * a.pr.H);
   if (a.pr.drop_p8 > 0)
     return launch_pdl(fa_fwd_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to,
                       a);
@@ -442,7 +447,7 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st) {
   cudaError_t e = launch_fwd_config();
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt, a.n_split);
+  const dim3 grid(a.pr.nt * a.pr.B * a.pr.H, a.n_split);
   // the O tensor map is not used in split mode (the merge kernel writes O)
   e = launch_pdl(fa_fwd_kernel<false, true>, grid, dim3(kThreads), fwd_smem_bytes(), st, tq, tk, tv,
                  tq, a);

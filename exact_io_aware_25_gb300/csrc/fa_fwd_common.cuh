@@ -98,18 +98,39 @@ __device__ __forceinline__ float max_cols(const float (&sv)[C]) {
 __device__ __forceinline__ float row_max(const float (&sv)[kTile]) { return max_cols<kTile>(sv); }
 
 // Block-sparse: writes the key tiles j < j_end whose mask byte in `row` is
-// nonzero to tiles[], ascending, and returns their count (one warp).
+// nonzero to tiles[], ascending, and returns their count (one warp; j_end <=
+// kMaxMaskTiles).  Lane l takes the contiguous bytes [l * per, (l + 1) * per)
+// and issues all its loads before using any, so the row costs one memory
+// latency; a warp prefix sum of the per-lane counts places each lane's tiles.
 __device__ __forceinline__ int compact_mask_row(const uint8_t *row, int j_end, int16_t *tiles,
                                                 int lane) {
-  int count = 0;
-  for (int base = 0; base < j_end; base += 32) {
-    const int j = base + lane;
-    const bool keep = j < j_end && __ldg(row + j) != 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (keep) tiles[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(j);
-    count += __popc(bal);
+  const int per = (j_end + 31) >> 5;  // at most 32 bytes per lane
+  const int j0 = lane * per;
+  uint32_t bits = 0u;
+  // 16 loads in flight at a time (one round up to 512 tiles, two beyond)
+  for (int r = 0; r < per; r += 16) {
+    uint32_t v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      v[e] = (r + e < per && j0 + r + e < j_end) ? static_cast<uint32_t>(__ldg(row + j0 + r + e))
+                                                 : 0u;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) bits |= (v[e] != 0u ? 1u : 0u) << (r + e);
   }
-  return count;
+  const int cnt = __popc(bits);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int off = incl - cnt;
+  while (bits) {
+    const int e = __ffs(static_cast<int>(bits)) - 1;
+    bits &= bits - 1u;
+    tiles[off++] = static_cast<int16_t>(j0 + e);
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 

@@ -86,16 +86,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Problem &pr = args.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heads vary fastest in launch order; the heaviest (last) query tiles go first
-  const int qt = pr.nt - 1 - static_cast<int>(blockIdx.y);
-  const int bh = blockIdx.x;
+  // launch order (work_order): groups of heads whose K and V fit in L2,
+  // within a group the last (heaviest causal) query tiles first
+  int bh, qrank;
+  work_order(pr, static_cast<int>(blockIdx.x), pr.nt, bh, qrank);
+  const int qt = pr.nt - 1 - qrank;
   const int b = bh / pr.H;
   const int kv_bound = key_bound(pr, b);
   const int n_kv = (kv_bound + kTile - 1) / kTile;
   int j_begin = 0, j_end = pr.causal ? causal_tile_end(qt, pr.causal_off, n_kv) : n_kv;
   if (kSplit) {
     const int per = (n_kv + args.n_split - 1) / args.n_split;
-    j_begin = min(n_kv, static_cast<int>(blockIdx.z) * per);
+    j_begin = min(n_kv, static_cast<int>(blockIdx.y) * per);
     j_end = min(n_kv, j_begin + per);
   }
   const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = (n > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       size_t prow = 0;
       if (kSplit)
-        prow = (static_cast<size_t>(blockIdx.z) * (pr.B * pr.H) + bh) *
+        prow = (static_cast<size_t>(blockIdx.y) * (pr.B * pr.H) + bh) *
                    static_cast<size_t>(args.nq_pad) + qrow;
       float ov[64];
       if (n > 0) {
@@ -418,7 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_3d(&tm_o, s.q, 0, qt * kTile, bh);
       tma_store_3d(&tm_o, s.q + kHalfBytes, 64, qt * kTile, bh);
       bulk_commit();
-      bulk_wait_all();
+      // the CTA may leave once the stores have read shared memory; the grid's
+      // completion covers the global writes
+      bulk_wait_read_all();
     }
   }
   tc_fence_before();
@@ -461,7 +465,7 @@ cudaError_t launch_fwd_d128(const CUtensorMap &tq, const CUtensorMap &tk, const 
   cudaError_t e = launch_fwd_d128_config();
   if (e != cudaSuccess) return e;
   const size_t smem = fwd_d128_smem_bytes();
-  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt);
+  const dim3 grid(a.pr.nt * a.pr.B * a.pr.H);
   if (a.pr.drop_p8 > 0)
     return launch_pdl(fa_fwd_d128_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv,
                       to, a);
@@ -473,7 +477,7 @@ cudaError_t launch_fwd_splitkv_d128(const CUtensorMap &tq, const CUtensorMap &tk
                                     const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st) {
   cudaError_t e = launch_fwd_d128_config();
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.pr.B * a.pr.H, a.pr.nt, a.n_split);
+  const dim3 grid(a.pr.nt * a.pr.B * a.pr.H, a.n_split);
   e = launch_pdl(fa_fwd_d128_kernel<false, true>, grid, dim3(kThreads), fwd_d128_smem_bytes(), st,
                  tq, tk, tv, tq, a);
   if (e != cudaSuccess) return e;

@@ -14,7 +14,7 @@ constexpr int kTile = 128;      // B_r = B_c = 128 query / key rows per tile
 constexpr int kHeadDim = 64;    // d of the main kernels; the forward also has a d = 128 kernel
 constexpr int kHeadDimWide = 128;
 constexpr int kMaxMaskTiles = 1024;  // block-sparse: at most 1024 tiles per row (N <= 131072)
-// Query tiles per head are a grid dimension of the forward launch (y, at most 65535).
+// Query tiles per head: the limit the host checks (at most 65535 tiles, 8M rows).
 constexpr int kMaxGridTiles = 65535;
 
 struct Problem {
@@ -34,7 +34,30 @@ struct Problem {
   uint32_t drop_p8;
   uint32_t seed_lo, seed_hi;
   float keep_scale;
+  // Work order (see work_order): heads are taken in groups of head_group
+  // whose re-read rows fit in L2 together (1 <= head_group <= B * H).
+  int head_group;
 };
+
+// The order in which the forward's CTAs and the backward's work items are
+// handed out: heads in groups of p.head_group, and within a group by rank
+// (query tile from the last, or key tile from the first: the longest first
+// under causal) with the group's heads varying fastest.  Unit u in
+// [0, B*H*per_head) maps to head bh and rank.  head_group = B*H gives one
+// global longest-first order; smaller groups keep the rows that the
+// resident CTAs re-read (K, V in the forward; Q, dO and the fp32 dQ
+// accumulators in the backward) to a few heads, so that they stay in L2.
+__device__ __forceinline__ void work_order(const Problem &p, int u, int per_head, int &bh,
+                                           int &rank) {
+  const int BH = p.B * p.H;
+  const int span = p.head_group * per_head;
+  const int gi = u / span;
+  const int g0 = gi * p.head_group;
+  const int gs = min(p.head_group, BH - g0);
+  const int rem = u - gi * span;
+  rank = rem / gs;
+  bh = g0 + (rem - rank * gs);
+}
 
 // The 32-bit PCG hash (Jarzynski and Olano, "Hash Functions for GPU
 // Rendering", JCGT 9(3), 2020): an LCG step followed by the RXS-M-XS output
