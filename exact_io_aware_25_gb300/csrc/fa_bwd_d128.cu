@@ -154,13 +154,23 @@ __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int qm, in
 // Dropout keep bits of 32 query columns of this thread's key row (bit e is
 // Z(q0 + e, key)); the hash and byte layout of include/fa.h.
 __device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32_t p8, int q0) {
+  // keys 2m and 2m + 1 sit in adjacent lanes and draw on the same hash word
+  // of each 2x2 block: each lane of the pair hashes half of the 16 query
+  // pairs (the even lane pairs 0-7, the odd lane 8-15) and the two swap their
+  // words with one shuffle (the warp is converged here)
+  const uint32_t odd = threadIdx.x & 1u;
   uint32_t bits = 0u;
-#pragma unroll 4
-  for (int e = 0; e < 32; e += 2) {
-    const uint32_t qp = static_cast<uint32_t>((q0 + e) >> 1);
-    const uint32_t r = pcg_hash(kk ^ (qp << 16)) >> sh;
-    bits |= static_cast<uint32_t>((r & 0xffu) >= p8) << e;
-    bits |= static_cast<uint32_t>(((r >> 16) & 0xffu) >= p8) << (e + 1);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t qp = static_cast<uint32_t>((q0 + 2 * k + 16 * static_cast<int>(odd)) >> 1);
+    const uint32_t w = pcg_hash(kk ^ (qp << 16));
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, 1);
+    const uint32_t ra = (odd ? o : w) >> sh;   // queries q0 + 2k, q0 + 2k + 1
+    const uint32_t rb = (odd ? w : o) >> sh;   // queries q0 + 16 + 2k, + 1
+    bits |= static_cast<uint32_t>((ra & 0xffu) >= p8) << (2 * k);
+    bits |= static_cast<uint32_t>(((ra >> 16) & 0xffu) >= p8) << (2 * k + 1);
+    bits |= static_cast<uint32_t>((rb & 0xffu) >= p8) << (2 * k + 16);
+    bits |= static_cast<uint32_t>(((rb >> 16) & 0xffu) >= p8) << (2 * k + 17);
   }
   return bits;
 }
@@ -307,9 +317,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       for (int k = 0; k < itm.n; ++k, ++g) {
         const int st = g % kStages;
-        const int i64 = qstep_of(a, itm, k);
+        // the step's query block: a global load under a block mask, so looked
+        // up only where it is used (the causal diagonal, the dropout keep bits)
+        const int i64 = (pr.causal || kDrop) ? qstep_of(a, itm, k) : 0;
         uint32_t keep = 0u;
-        if (kDrop) keep = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i64 * kQStep + qc);
+        if (kDrop) {
+          keep = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i64 * kQStep + qc);
+          asm volatile("" : "+r"(keep));  // evaluated here, before the step's registers fill
+        }
         if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1) || !w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
@@ -421,6 +436,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (t >= n_items) break;
       const Item itm = item_at(a, t);
       for (int k = 0; k < itm.n; ++k, ++g) {
+        // the accumulator rows of this step (looked up before the wait)
+        const int row0 = itm.bh * a.n_pad + qstep_of(a, itm, k) * kQStep;
         if (!mbar_wait_warp(&s.bar_dq_full, g & 1, pr.wait, &s.abort)) {
           ok = false;
           break;
@@ -446,7 +463,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int row0 = itm.bh * a.n_pad + qstep_of(a, itm, k) * kQStep;
           tma_reduce_add_2d(&tm_dq_acc, s.dq_stage[dw], dw * 32, row0);
           bulk_commit();
         }
@@ -492,11 +508,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int k = 0; k < itm.n; ++k, ++g) {
           const int st = g % kStages;
           const uint32_t use = g / kStages;
+          const int i64 = qstep_of(a, itm, k);  // (a global load under a block mask: before the wait)
           if (use > 0 && !mbar_wait_warp(&s.bar_q_empty[st], (use - 1) & 1, pr.wait, &s.abort)) {
             ok = false;
             break;
           }
-          const int i64 = qstep_of(a, itm, k);
           const size_t stat = static_cast<size_t>(itm.bh) * a.n_pad + static_cast<size_t>(i64) * kQStep;
           mbar_arrive_expect_tx_w(&s.bar_q_full[st], 2 * kQBytes + 2 * kQStep * 4);
           tma_load_3d_w(s.q[st], &tm_q, &s.bar_q_full[st], 0, i64 * kQStep, itm.bh);
