@@ -309,6 +309,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   // the rows every query tile re-reads: K and V of its head
   a.pr.head_group = heads_per_group(B, H, 4 * static_cast<size_t>(Nk) * d);
   a.lse = lse;
+  a.o = static_cast<uint16_t *>(o);
   a.row_m = x.row_m;
   a.row_l = x.row_l;
   a.csr_ptr = x.csr_ptr;

@@ -85,7 +85,8 @@ struct FwdArgs {
   int nq_pad;             // query rows per head in the partial arrays (N rounded up to 128)
   float *part_o;          // [n_split, B*H, nq_pad, d] fp32
   float *part_lse;        // [n_split, B*H, nq_pad] fp32, natural log
-  uint16_t *o;            // [B, H, N, d] bf16, written by the merge kernel
+  uint16_t *o;            // [B, H, N, d] bf16: written by the d = 64 forward's softmax warps,
+                          // or by the merge kernel in split-KV mode
   // Optional row statistics (plain forward): row max m_i of S and the
   // exponential sum l_i = sum_j exp(s_ij - m_i), fp32 [B, H, N].
   float *row_m;
