@@ -105,3 +105,39 @@ def test_two_streams_with_their_own_workspaces(H, oracle_mod):
         fa.fa_check(st)
     for x, (o, lse, grads, _) in zip(xs, outs):
         _check_all(H, oracle_mod, x, o, lse, grads)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_forwards_on_concurrent_streams_match_serial_runs(H, d):
+    """The d = 64 forward hands out its units by cancelling the launch of CTAs
+    of its own grid; with three forwards (hundreds of units each, more than
+    the CTAs that run) enqueued on three streams at once, every unit of every
+    call must still run exactly once: O and lse equal, bit for bit, those of
+    the same calls run one at a time."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    specs = [dict(seed=130, B=2, H=8, N=4096, causal=True),
+             dict(seed=131, B=4, H=8, N=2048, causal=False),
+             dict(seed=132, B=1, H=16, N=3000, causal=True)]
+    xs = [H.Inputs(W.make("tiny", d=d, **sp)) for sp in specs]
+
+    def run(streams):
+        outs = []
+        for x in xs:
+            shape = (x.B, x.H, x.N, x.d)
+            outs.append((H.nan_like_bf16(shape),
+                         torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda")))
+        torch.cuda.synchronize()
+        for x, st, (o, lse) in zip(xs, streams, outs):
+            fa.fa_fwd(x.q, x.k, x.v, o, lse, x.B, x.H, x.N, x.d, x.scale, x.causal, None, None, st)
+        for st in set(streams):
+            fa.fa_check(st)
+        torch.cuda.synchronize()
+        return outs
+
+    ref = run([torch.cuda.current_stream()] * len(xs))
+    for _ in range(3):
+        got = run([torch.cuda.Stream() for _ in xs])
+        for (o, lse), (o_r, lse_r) in zip(got, ref):
+            assert torch.equal(o.view(torch.int16), o_r.view(torch.int16))
+            assert torch.equal(lse, lse_r)
