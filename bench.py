@@ -586,12 +586,22 @@ def run_ours(args, rank, world, local):
     e2e_steps = max(3, min(args.e2e_steps, K))
     hq, hk, hv, hdo = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (w.q, w.k, w.v, w.do))
     hkv = torch.from_numpy(w.kv_len).pin_memory() if w.kv_len is not None else None
+    hmask = torch.from_numpy(w.block_mask).pin_memory() if w.block_mask is not None else None
     ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=torch.int16).pin_memory() for _ in range(4))
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     dq_i, dk_i, dv_i, do_i = (t.view(torch.int16) for t in (dq, dk, dv, do))
     qi, ki, vi, oi = (t.view(torch.int16) for t in (q, k, v, o))
+    arena_bytes = fa.fa_host_arena_size(B, H, N, d)
+    arena = torch.empty(arena_bytes, dtype=torch.uint8, device=device) if p_drop == 0 else None
 
-    def e2e_step():
+    def e2e_host_api():
+        # one call: the library copies each head group in, runs it and copies
+        # its results out, overlapping the three across groups
+        fa.fa_fwd_bwd_host(hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv, B, H, N, d, s.scale,
+                           s.causal, hkv, hmask, 0, arena, arena_bytes, stream)
+
+    def e2e_serial():
+        # the device entry points between plain copies on one stream
         qi.copy_(hq, non_blocking=True)
         ki.copy_(hk, non_blocking=True)
         vi.copy_(hv, non_blocking=True)
@@ -605,27 +615,44 @@ def run_ours(args, rank, world, local):
         hdk.copy_(dk_i, non_blocking=True)
         hdv.copy_(dv_i, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(device)
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    barrier(world, device)
-    for i in range(e2e_steps):
-        flush.fill_(i & 0xFF)
-        e0[i].record(stream)
-        e2e_step()
-        e1[i].record(stream)
-    torch.cuda.synchronize(device)
-    fa.fa_check(stream)
-    e2e_t = max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
-                           world, device)
+    def time_e2e(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(device)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        barrier(world, device)
+        for i in range(e2e_steps):
+            flush.fill_(i & 0xFF)
+            e0[i].record(stream)
+            fn()
+            e1[i].record(stream)
+        torch.cuda.synchronize(device)
+        fa.fa_check(stream)
+        return max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
+                              world, device)
+
     t_bytes = q.numel() * 2
     h2d = 4 * t_bytes + (hkv.numel() * 4 if hkv is not None else 0)
     d2h = 4 * t_bytes + hlse.numel() * 4
-    e2e = {"value": fl["step"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "ms_per_step": 1e3 * e2e_t / e2e_steps}
+    t_serial = time_e2e(e2e_serial)
+    serial = {"value": fl["step"] * e2e_steps * world / t_serial / 1e12,
+              "ms_per_step": 1e3 * t_serial / e2e_steps,
+              "api": "fa_fwd / fa_bwd on device buffers between plain copies on one stream"}
+    if p_drop == 0:
+        e2e_t = time_e2e(e2e_host_api)
+        h2d += hmask.numel() if hmask is not None else 0   # the host call copies the mask too
+        e2e = {"value": fl["step"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": 1e3 * e2e_t / e2e_steps,
+               "api": "fa_fwd_bwd_host: pinned host buffers, copies of each head group "
+                      "overlapped with the kernels of the previous one",
+               "serial_copies": serial}
+    else:
+        # the host-buffer entry points have no dropout
+        e2e = {"value": serial["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": serial["ms_per_step"], "api": serial["api"]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -728,17 +755,16 @@ def run_fwd_only(args, rank, world, local):
 
     e2e_steps = max(3, min(args.e2e_steps, K))
     hq, hk, hv = (torch.from_numpy(x.view(np.int16)).pin_memory() for x in (w.q, w.k, w.v))
+    hkv = torch.from_numpy(w.kv_len).pin_memory() if w.kv_len is not None else None
+    hmask = torch.from_numpy(w.block_mask).pin_memory() if w.block_mask is not None else None
     ho = torch.empty(q.shape, dtype=torch.int16).pin_memory()
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    qi, ki, vi, oi = (t.view(torch.int16) for t in (q, k, v, o))
+    arena_bytes = fa.fa_host_arena_size(B, H, N, d)
+    arena = torch.empty(arena_bytes, dtype=torch.uint8, device=device)
 
     def e2e_step():
-        qi.copy_(hq, non_blocking=True)
-        ki.copy_(hk, non_blocking=True)
-        vi.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(oi, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
+        fa.fa_fwd_host(hq, hk, hv, ho, hlse, B, H, N, d, s.scale, s.causal, hkv, hmask, 0, arena,
+                       arena_bytes, stream)
 
     for _ in range(2):
         e2e_step()
@@ -755,9 +781,13 @@ def run_fwd_only(args, rank, world, local):
     e2e_t = max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
                            world, device)
     t_bytes = q.numel() * 2
+    h2d = 3 * t_bytes + (hkv.numel() * 4 if hkv is not None else 0) + (
+        hmask.numel() if hmask is not None else 0)
     e2e = {"value": fl["fwd"] * e2e_steps * world / e2e_t / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": 3 * t_bytes, "d2h_bytes_per_step": t_bytes + hlse.numel() * 4,
-           "steps": e2e_steps}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": t_bytes + hlse.numel() * 4,
+           "steps": e2e_steps, "ms_per_step": 1e3 * e2e_t / e2e_steps,
+           "api": "fa_fwd_host: pinned host buffers, copies of each head group overlapped "
+                  "with the kernels of the previous one"}
     if rank == 0:
         cfg = workload_config(w)
         cfg["workload"] = cfg["workload"].replace("fwd+bwd", f"forward only, d={d}")

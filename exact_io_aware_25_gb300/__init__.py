@@ -22,6 +22,7 @@ __all__ = [
     "FaError", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_check",
     "fa_status_string", "fa_set_wait_timeout_ns", "fa_debug_starve_next_fwd",
     "fa_set_bwd_main_events", "fa_bwd_noalloc", "fa_bwd_noalloc_max_scratch_bytes",
+    "fa_host_arena_size", "fa_fwd_host", "fa_fwd_bwd_host",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA",
     "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE", "LIB_PATH",
 ]
@@ -97,6 +98,14 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_noalloc.restype = ci
             L.fa_bwd_noalloc_max_scratch_bytes.argtypes = []
             L.fa_bwd_noalloc_max_scratch_bytes.restype = sz
+            L.fa_host_arena_size.argtypes = [ci, ci, ci, ci]
+            L.fa_host_arena_size.restype = sz
+            L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, cf, ci, vp, vp, ci, vp,
+                                      sz, vp]
+            L.fa_fwd_host.restype = ci
+            L.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, cf,
+                                          ci, vp, vp, ci, vp, sz, vp]
+            L.fa_fwd_bwd_host.restype = ci
             L.fa_check.argtypes = [vp]
             L.fa_check.restype = ci
             L.fa_status_string.argtypes = [ci]
@@ -269,6 +278,39 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal=
 
 def fa_bwd_noalloc_max_scratch_bytes() -> int:
     return int(lib().fa_bwd_noalloc_max_scratch_bytes())
+
+
+def fa_host_arena_size(B, H, N, d) -> int:
+    return int(lib().fa_host_arena_size(int(B), int(H), int(N), int(d)))
+
+
+def _nbytes(t, given):
+    if t is not None and not isinstance(t, int) and not given:
+        return t.numel() * t.element_size()
+    return int(given)
+
+
+def fa_fwd_host(q, k, v, o, lse, B, H, N, d, scale, causal=0, kv_len=None, block_mask=None,
+                n_chunks=0, arena=None, arena_bytes=0, stream=None) -> None:
+    """Forward of tensors in (pinned) HOST memory, with the copies overlapped
+    with the kernels; ``arena`` is device scratch of >= fa_host_arena_size
+    bytes.  The outputs are ready once ``stream`` has completed."""
+    _check(lib().fa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                             int(N), int(d), float(scale), int(bool(causal)), _ptr(kv_len),
+                             _ptr(block_mask), int(n_chunks), _ptr(arena),
+                             _nbytes(arena, arena_bytes), _stream(stream)), "fa_fwd_host")
+
+
+def fa_fwd_bwd_host(q, k, v, dout, o, lse, dq, dk, dv, B, H, N, d, scale, causal=0,
+                    kv_len=None, block_mask=None, n_chunks=0, arena=None, arena_bytes=0,
+                    stream=None) -> None:
+    """Forward and backward of tensors in (pinned) HOST memory (see
+    fa_fwd_host and include/fa.h)."""
+    _check(lib().fa_fwd_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d),
+                                 float(scale), int(bool(causal)), _ptr(kv_len), _ptr(block_mask),
+                                 int(n_chunks), _ptr(arena), _nbytes(arena, arena_bytes),
+                                 _stream(stream)), "fa_fwd_bwd_host")
 
 
 def fa_check(stream=None) -> None:

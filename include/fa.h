@@ -178,6 +178,53 @@ FA_API fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, voi
                                 size_t workspace_bytes, void *stream);
 
 /*
+ * Host-buffer entry points: the forward (fa_fwd_host) or the forward and the
+ * backward (fa_fwd_bwd_host) of the tensors above held in HOST memory.  Every
+ * (b, h) is an independent N x d problem ([EXPL] "Method"), so the heads are
+ * cut into contiguous groups and the host-to-device copies of one group, the
+ * kernels of the previous one and the device-to-host copies of the one before
+ * overlap on the GPU (two copy streams of the library plus `stream`, joined
+ * by events).  Each group runs fa_fwd (and fa_bwd) on its heads, so the
+ * results are those entry points' results for the same inputs.
+ *   q, k, v, dout  in : HOST bf16 [B, H, N, d]; page-locked (pinned) memory
+ *                       is needed for the copies to overlap anything
+ *   o              out: HOST bf16 [B, H, N, d]
+ *   lse            out: HOST fp32 [B, H, N]
+ *   dq, dk, dv     out: HOST bf16 [B, H, N, d] (fa_fwd_bwd_host only)
+ *   kv_len         in : NULL or HOST int32 [B]
+ *   block_mask     in : NULL or HOST uint8 [nb * nb], as in fa_fwd
+ *   n_chunks       in : head groups; 0 = about 256 query tiles per group,
+ *                       2 to 8 groups; at most 64; capped at B * H
+ *   arena          in : DEVICE scratch of >= fa_host_arena_size() bytes,
+ *                       256-byte aligned, caller-owned: device copies of the
+ *                       tensors, the backward's workspace and small slack
+ *   stream         in : the kernels run on it, and it completes only after the
+ *                       last copy back: synchronise it (or fa_check) before
+ *                       reading the outputs or reusing the inputs
+ * No dropout: the keep mask depends on the head's index in the whole problem;
+ * use fa_fwd_dropout / fa_bwd_dropout on device tensors.  Errors: fa_fwd's
+ * and fa_bwd's codes for the same arguments; FA_ERR_WORKSPACE for a missing,
+ * misaligned or short arena; FA_ERR_INVALID_ARG for n_chunks outside
+ * [0, 64]; FA_ERR_CUDA when a copy or a stream / event call fails.  The
+ * library cannot tell host from device pointers here: pass host memory.
+ * Calls on one device share
+ * the copy streams: they are enqueued one at a time and their copies run in
+ * call order.
+ */
+FA_API size_t fa_host_arena_size(int B, int H, int N, int d);
+
+FA_API fa_status fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             const int32_t *kv_len, const uint8_t *block_mask, int n_chunks,
+                             void *arena, size_t arena_bytes, void *stream);
+
+FA_API fa_status fa_fwd_bwd_host(const void *q, const void *k, const void *v, const void *dout,
+                                 void *o, float *lse, void *dq, void *dk, void *dv, int B, int H,
+                                 int N, int d, float scale, int causal, const int32_t *kv_len,
+                                 const uint8_t *block_mask, int n_chunks, void *arena,
+                                 size_t arena_bytes, void *stream);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory when they run the backward pass (for instance a plugin whose
  * host application owns every device allocation, or a latency-critical loop

@@ -258,3 +258,49 @@ def test_noalloc_status_equals_fa_bwd_status_without_gpu(fa_lib, kw):
     assert got == want
     if kw.get("N") == 65536:
         assert want == -6 and got == -6
+
+
+def test_host_arena_size_formula(fa_lib):
+    # device copies of q, k, v, dout, o, dq, dk, dv; the lse region with one
+    # 256-byte boundary of slack per head group (at most 64); kv_len; the
+    # block mask (when it may exist); the backward workspace of the whole problem
+    L = fa_lib.lib()
+    up = lambda x: -(-x // 256) * 256
+    for B, H, N, d in [(1, 1, 1, 64), (2, 3, 301, 128), (1, 8, 65536, 64), (1, 1, 1 << 18, 64)]:
+        nb = -(-N // 128)
+        want = 8 * up(B * H * N * d * 2) + up(B * H * N * 4) + 256 * 64 + up(B * 4)
+        want += up(nb * nb) if nb <= 1024 else 0
+        want += fa_lib.fa_bwd_workspace_size(B, H, N, d)
+        assert L.fa_host_arena_size(B, H, N, d) == want
+    assert L.fa_host_arena_size(1, 1, 128, 96) == 0
+    assert L.fa_host_arena_size(0, 1, 128, 64) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), -1), (dict(dout=None), -1), (dict(n_chunks=-1), -1), (dict(n_chunks=65), -1),
+    (dict(B=0), -1), (dict(scale=float("nan")), -1), (dict(d=96), -2),
+    (dict(N=1024 * 128 + 1, mask=FAKE), -2), (dict(N=65535 * 128 + 1), -2),
+    (dict(arena=None), -6), (dict(arena=FAKE + 16), -6), (dict(short=1), -6),
+])
+def test_host_api_validation_without_gpu(fa_lib, kw, status):
+    """Both host-buffer entry points reject bad arguments before any CUDA
+    call, with fa_fwd's code for the arguments they share."""
+    L = fa_lib.lib()
+    a = dict(q=FAKE, dout=FAKE, B=1, H=1, N=128, d=64, scale=0.125, mask=None, n_chunks=0,
+             arena=FAKE, short=0)
+    a.update(kw)
+    need = L.fa_host_arena_size(a["B"], a["H"], a["N"], a["d"])
+    nbytes = max(need - a["short"], 0) if need else 1 << 40
+    got = L.fa_fwd_bwd_host(a["q"], FAKE, FAKE, a["dout"], FAKE, FAKE, FAKE, FAKE, FAKE, a["B"],
+                            a["H"], a["N"], a["d"], a["scale"], 0, None, a["mask"],
+                            a["n_chunks"], a["arena"], nbytes, None)
+    assert got == status
+    if "dout" not in kw:
+        got_f = L.fa_fwd_host(a["q"], FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+                              a["scale"], 0, None, a["mask"], a["n_chunks"], a["arena"], nbytes,
+                              None)
+        assert got_f == status
+    if status in (-1, -2) and not {"n_chunks", "dout"} & set(kw):
+        want = L.fa_fwd(a["q"], FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+                        a["scale"], 0, None, a["mask"], None)
+        assert got == want
