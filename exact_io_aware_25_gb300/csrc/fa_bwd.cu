@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           keep_b = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i * kTile + half * 64 + 32);
           asm volatile("" : "+r"(keep_a), "+r"(keep_b));  // evaluated here, before S^T / dP^T
         }
-        if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1) || !w_wait(&s.bar_s_full, g & 1)) {
+        if (!w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
         }
@@ -526,6 +526,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t sa[32], da[32], sb[32], db[32];
         tmem_ld32(t_s, sa);
         tmem_ld32(t_dp, da);
+        // the step's lse2 and D (the Q / dO stage; the S^T MMA already waited
+        // for its Q), checked while the TMEM loads are in flight
+        if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1)) {
+          tmem_wait_ld_tied32(sa, da);
+          ok = false;
+          break;
+        }
         tmem_wait_ld_tied32(sa, da);
         tmem_ld32(t_s + 32, sb);   // second half in flight while the first is computed
         tmem_ld32(t_dp + 32, db);

@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           keep = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i64 * kQStep + qc);
           asm volatile("" : "+r"(keep));  // evaluated here, before the step's registers fill
         }
-        if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1) || !w_wait(&s.bar_s_full, g & 1)) {
+        if (!w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
         }
@@ -341,6 +341,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         uint32_t sa[32], da[32];
         tmem_ld32(tmem + lane_base + kColST + qc, sa);
         tmem_ld32(tmem + lane_base + kColDPT + qc, da);
+        // the step's lse2 and D (the Q / dO stage; the S^T MMA already waited
+        // for its Q), checked while the TMEM loads are in flight
+        if (!w_wait(&s.bar_q_full[st], (g / kStages) & 1)) {
+          tmem_wait_ld_tied32(sa, da);
+          ok = false;
+          break;
+        }
         tmem_wait_ld_tied32(sa, da);
         tc_fence_before();
         warp_arrive(&s.bar_st_read);  // S^T / dP^T TMEM columns may be overwritten
