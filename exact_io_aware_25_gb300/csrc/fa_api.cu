@@ -203,13 +203,14 @@ int heads_per_group(int B, int H, size_t per_head_bytes) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t dsum, lse2, dq_acc, col_cnt, col_idx, sched, total;
+  size_t dsum, lse2, dq_acc, col_cnt, col_idx, kt_order, sched, total;
 };
 
 // Workspace: D and base-2 lse [B*H, n_pad] fp32, dQ accumulators
-// [B*H, n_pad, 64] fp32, and the block-sparse column lists (key tile ->
-// ascending query tiles): counts int32 [nt] and indices int16 [nt, nt]; one
-// int32 work counter for the persistent main kernel.
+// [B*H, n_pad, d] fp32, and the block-sparse column lists (key tile ->
+// ascending query tiles): counts int32 [nt], indices int16 [nt, nt] and the
+// key tiles by descending count int16 [nt]; one int32 work counter for the
+// persistent main kernel.
 WsLayout ws_layout(int B, int H, int N, int d) {
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t n_pad = align_up(static_cast<size_t>(N), kTile);
@@ -222,7 +223,8 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   const size_t nl = nt < static_cast<size_t>(kMaxMaskTiles) ? nt : kMaxMaskTiles;
   w.col_cnt = align_up(w.dq_acc + bh * n_pad * static_cast<size_t>(d) * sizeof(float), 256);
   w.col_idx = align_up(w.col_cnt + nl * sizeof(int), 256);
-  w.sched = align_up(w.col_idx + nl * nl * sizeof(int16_t), 256);
+  w.kt_order = align_up(w.col_idx + nl * nl * sizeof(int16_t), 256);
+  w.sched = align_up(w.kt_order + nl * sizeof(int16_t), 256);
   w.total = align_up(w.sched + sizeof(int), 256);
   return w;
 }
@@ -448,6 +450,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
   a.dq_acc = reinterpret_cast<float *>(ws + wl.dq_acc);
   a.col_cnt = reinterpret_cast<int *>(ws + wl.col_cnt);
   a.col_idx = reinterpret_cast<int16_t *>(ws + wl.col_idx);
+  a.kt_order = reinterpret_cast<int16_t *>(ws + wl.kt_order);
   a.sched = reinterpret_cast<int *>(ws + wl.sched);
   a.dq = static_cast<uint16_t *>(dq);
   CUtensorMap tdq_acc;

@@ -52,6 +52,28 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
   const int sub = threadIdx.x & 7;
   const int r0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.sched = 0;
+  if (pr.block_mask && blockIdx.x == 0 && blockIdx.y == 0) {
+    // the key tiles by descending number of query tiles (counting sort; ties
+    // in any order): the main kernel hands out each head group's items
+    // longest first, so that the ones left for the end are the shortest
+    __shared__ int bins[kMaxMaskTiles + 1];
+    const int nt = pr.nt;
+    for (int c = threadIdx.x; c <= nt; c += blockDim.x) bins[c] = 0;
+    __syncthreads();
+    for (int kt = threadIdx.x; kt < nt; kt += blockDim.x) atomicAdd(&bins[a.col_cnt[kt]], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int pos = 0;
+      for (int c = nt; c >= 0; --c) {
+        const int k = bins[c];
+        bins[c] = pos;
+        pos += k;
+      }
+    }
+    __syncthreads();
+    for (int kt = threadIdx.x; kt < nt; kt += blockDim.x)
+      a.kt_order[atomicAdd(&bins[a.col_cnt[kt]], 1)] = static_cast<int16_t>(kt);
+  }
   const uint16_t *o_head = a.o + static_cast<size_t>(bh) * pr.N * D;
   const uint16_t *do_head = a.dout + static_cast<size_t>(bh) * pr.N * D;
   const size_t ws_row0 = static_cast<size_t>(bh) * a.n_pad;
@@ -279,7 +301,7 @@ struct Item {
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
   Item it;
-  work_order(pr, t, a.nkt, it.bh, it.kt);
+  bwd_item(a, t, it.bh, it.kt);
   it.kv_bound = key_bound(pr, it.bh / pr.H);
   it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   if (it.kt * kTile >= it.kv_bound) it.n = 0;
@@ -851,7 +873,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int t = s.epi_item[kb];
         if (t < 0) break;
         int bh, kt;
-        work_order(pr, t, a.nkt, bh, kt);
+        bwd_item(a, t, bh, kt);
         if (lane == 0) {
           tma_store_3d(&tm_dv, s.kv[kb][1], 0, kt * kTile, bh);
           tma_store_3d(&tm_dk, s.kv[kb][0], 0, kt * kTile, bh);

@@ -99,7 +99,7 @@ struct Item {
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
   Item it;
-  work_order(pr, t, a.nkt, it.bh, it.kt);
+  bwd_item(a, t, it.bh, it.kt);
   it.kv_bound = key_bound(pr, it.bh / pr.H);
   it.i_begin = pr.causal ? causal_first_qtile(pr, it.kt) : 0;
   int tiles;
@@ -646,7 +646,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int t = s.epi_item;
         if (t < 0) break;
         int bh, kt;
-        work_order(pr, t, a.nkt, bh, kt);
+        bwd_item(a, t, bh, kt);
         if (lane == 0) {
           tma_store_3d(&tm_dv, s.kv[1], 0, kt * kTile, bh);
           tma_store_3d(&tm_dv, s.kv[1] + kKvHalf, 64, kt * kTile, bh);

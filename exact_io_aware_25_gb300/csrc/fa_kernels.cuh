@@ -111,9 +111,20 @@ struct BwdArgs {
   float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, d]
   int *col_cnt;           // workspace, block mask only: query tiles per key tile [nt]
   int16_t *col_idx;       // workspace, block mask only: their indices [nt][nt], ascending
+  int16_t *kt_order;      // workspace, block mask only: key tiles by descending count [nt]
   int *sched;             // workspace: work counter of the persistent main kernel
   uint16_t *dq;           // [B, H, N, d] bf16
 };
+
+// Item t of a backward main kernel: head bh and key tile kt.  work_order
+// gives the key tile's rank; under a block mask the rank indexes the key
+// tiles sorted by their number of query tiles, largest first (written by the
+// preprocess), so that the items handed out last are the shortest.
+__device__ __forceinline__ void bwd_item(const BwdArgs &a, int t, int &bh, int &kt) {
+  int rank;
+  work_order(a.pr, t, a.nkt, bh, rank);
+  kt = a.pr.block_mask ? static_cast<int>(__ldg(a.kt_order + rank)) : rank;
+}
 
 // First query tile with a query that sees a key of key tile kt under the
 // causal rule (key j is kept for query i iff j <= i + causal_off): the tile

@@ -83,9 +83,10 @@ FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, fl
  * query row (padded to a multiple of 128) one fp32 D_i = <dO_i, O_i>, one
  * fp32 base-2 log-sum-exp, and d fp32 dQ accumulators; O(N) per head
  * ([EXPL] "Complexity analysis": O(N) extra memory).  Plus, for the
- * block-sparse schedule, one int32 count and up to nt int16 query-tile indices
- * per key tile (nt = ceil(N / 128), capped at 1024), and one int32 work
- * counter.  Returns 0 for invalid sizes.
+ * block-sparse schedule, one int32 count, up to nt int16 query-tile indices
+ * and one int16 place in the longest-first order per key tile (nt =
+ * ceil(N / 128), capped at 1024), and one int32 work counter.  Returns 0 for
+ * invalid sizes.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 

@@ -42,9 +42,9 @@ def test_status_strings(fa_lib):
 
 def test_workspace_size_formula(fa_lib):
     # per (b, h) and padded row: D (4 B) + base-2 lse (4 B) + d fp32 dQ accumulators;
-    # plus the block-sparse column lists: nl int32 counts and nl*nl int16 indices
-    # (nl = min(nt, 1024), the most tiles a block mask may have), and one int32
-    # work counter
+    # plus the block-sparse column lists: nl int32 counts, nl*nl int16 indices and
+    # nl int16 key tiles by count (nl = min(nt, 1024), the most tiles a block mask
+    # may have), and one int32 work counter
     up = lambda x: -(-x // 256) * 256
     for B, H, N in [(1, 1, 1), (2, 3, 129), (16, 16, 512), (1, 8, 65536), (1, 1, 1 << 20)]:
         for d in (64, 128):
@@ -56,6 +56,7 @@ def test_workspace_size_formula(fa_lib):
             want = up(want + bh * n_pad * d * 4)
             want = up(want + nl * 4)
             want = up(want + nl * nl * 2)
+            want = up(want + nl * 2)
             want = up(want + 4)
             assert fa_lib.fa_bwd_workspace_size(B, H, N, d) == want
     assert fa_lib.fa_bwd_workspace_size(1, 1, 128, 96) == 0
