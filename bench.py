@@ -372,7 +372,8 @@ def run_reference(args, rank, world):
     f_p, t_p, threads = time_oracle_rows(w, probe, dropout=args.dropout, seed=args.seed)
     head_est = t_p / len(probe) * spec.N * 1.4
     if head_est <= per_step_budget:
-        f1, t1, _, threads = time_oracle(w, 0.0, max_units=1, dropout=args.dropout,
+        # one whole head, timed (max_units bounds it; the budget must not stop it first)
+        f1, t1, _, threads = time_oracle(w, float("inf"), max_units=1, dropout=args.dropout,
                                          seed=args.seed)
         heads_per_step = max(1, min(spec.B * spec.H, int(per_step_budget / max(t1, 1e-6))))
         run = lambda: time_oracle(w, float("inf"), max_units=heads_per_step,

@@ -120,3 +120,15 @@ def test_reference_row_sample_counts_its_rows(oracle_mod):
     f, t, threads = bench.time_oracle_rows(w, rows)
     assert t > 0 and threads >= 1
     assert f == 10.0 * 64 * sum([1, 6, 256, 18])
+
+
+def test_oracle_head_timer_runs_the_heads_it_is_asked_for(oracle_mod):
+    """time_oracle with max_units bounds the heads, and an unlimited budget
+    does not stop it before the first one (the reference arm sizes its steps
+    from one timed head)."""
+    w = W.make("tiny", B=1, H=3, N=64)
+    f, t, heads, _ = bench.time_oracle(w, float("inf"), max_units=1)
+    assert heads == 1 and t > 0 and f > 0
+    f2, _, heads2, _ = bench.time_oracle(w, float("inf"), max_units=2)
+    assert heads2 == 2 and f2 == pytest.approx(2 * f)
+    assert bench.time_oracle(w, 0.0)[2] == 0
