@@ -206,7 +206,10 @@ FA_API fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, voi
  * use fa_fwd_dropout / fa_bwd_dropout on device tensors.  Errors: fa_fwd's
  * and fa_bwd's codes for the same arguments; FA_ERR_WORKSPACE for a missing,
  * misaligned or short arena; FA_ERR_INVALID_ARG for n_chunks outside
- * [0, 64]; FA_ERR_CUDA when a copy or a stream / event call fails.  The
+ * [0, 64]; FA_ERR_CUDA when a copy or a stream / event call fails.  Every
+ * argument is checked before anything is enqueued; a CUDA failure part-way
+ * leaves the groups enqueued before it running, so after FA_ERR_CUDA the
+ * outputs are undefined until the device has been synchronised.  The
  * library cannot tell host from device pointers here: pass host memory.
  * Calls on one device share
  * the copy streams: they are enqueued one at a time and their copies run in
