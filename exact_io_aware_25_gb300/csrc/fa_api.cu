@@ -301,7 +301,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
   if (!encode_bhnd(&tq, q, BH, N, d) || !encode_bhnd(&tk, k, BH, Nk, d) ||
-      !encode_bhnd(&tv, v, BH, Nk, d) || !encode_bhnd(&to, o, BH, N, d))
+      !encode_bhnd(&tv, v, BH, Nk, d) ||
+      (d == kHeadDimWide && !encode_bhnd(&to, o, BH, N, d)))   // the d = 128 forward stores O by TMA
     return FA_ERR_CUDA;
   FwdArgs a{};
   a.pr = make_problem(B, H, N, scale, causal, kv_len, block_mask, err, p8, seed);
@@ -324,7 +325,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
   }
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d == kHeadDimWide ? launch_fwd_d128(tq, tk, tv, to, a, cs)
-                                          : launch_fwd(tq, tk, tv, to, a, cs);
+                                          : launch_fwd(tq, tk, tv, a, cs);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -349,31 +349,6 @@ __device__ __forceinline__ void p_from_s32(uint32_t (&v)[32], int qc, int kr, bo
   }
 }
 
-// Dropout keep bits of 32 query columns of this thread's key row: bit e is
-// Z(q0 + e, key).  kk = head key ^ (key >> 1); sh = 8 * (key & 1) selects the
-// key's byte among each 2x2 block word (even queries: bytes 0-1, odd: 2-3).
-__device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32_t p8, int q0) {
-  // keys 2m and 2m + 1 sit in adjacent lanes and draw on the same hash word
-  // of each 2x2 block: each lane of the pair hashes half of the 16 query
-  // pairs (the even lane pairs 0-7, the odd lane 8-15) and the two swap their
-  // words with one shuffle (the warp is converged here)
-  const uint32_t odd = threadIdx.x & 1u;
-  uint32_t bits = 0u;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t qp = static_cast<uint32_t>((q0 + 2 * k + 16 * static_cast<int>(odd)) >> 1);
-    const uint32_t w = pcg_hash(kk ^ (qp << 16));
-    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, 1);
-    const uint32_t ra = (odd ? o : w) >> sh;   // queries q0 + 2k, q0 + 2k + 1
-    const uint32_t rb = (odd ? w : o) >> sh;   // queries q0 + 16 + 2k, + 1
-    bits |= static_cast<uint32_t>((ra & 0xffu) >= p8) << (2 * k);
-    bits |= static_cast<uint32_t>(((ra >> 16) & 0xffu) >= p8) << (2 * k + 1);
-    bits |= static_cast<uint32_t>((rb & 0xffu) >= p8) << (2 * k + 16);
-    bits |= static_cast<uint32_t>(((rb >> 16) & 0xffu) >= p8) << (2 * k + 17);
-  }
-  return bits;
-}
-
 // P^T of 32 columns as bf16 pairs into the TMEM P^T columns; with dropout,
 // the dropped columns as 0 (the keep scale is applied to dV at the end).
 template <bool kDrop>

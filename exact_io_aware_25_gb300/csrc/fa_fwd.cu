@@ -23,7 +23,7 @@
 //            applies the masks, keeps (m, l) in base-2 units, writes
 //            P~ = 2^(S*scale*log2e - m) as packed bf16 pairs back into TMEM,
 //            rescales its O row in TMEM when m grew, and runs the epilogue
-//            (O / l -> bf16 -> TMA store, lse).
+//            (O / l -> bf16 -> its row of O in global memory, lse).
 // Division by l is deferred to the epilogue; the result equals the pages'
 // per-step normalised update because both use the same running max.
 #include "fa_kernels.cuh"
@@ -144,8 +144,7 @@ __device__ __forceinline__ int clc_cancelled_x(const uint4 *resp) {
 template <bool kDrop, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdArgs args) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -155,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool sparse = pr.block_mask != nullptr || args.csr_ptr != nullptr;
   const bool persist = !kSplit && !args.starve;
-  (void)tm_o;
 
   // The producer warp initialises the barriers and, for a first unit without
   // a block mask, issues its first loads (Q, K_0, V_0) at once, so that their
@@ -575,15 +573,14 @@ cudaError_t launch_fwd_config() {
 }
 
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st) {
+                       const FwdArgs &a, cudaStream_t st) {
   cudaError_t e = launch_fwd_config();
   if (e != cudaSuccess) return e;
   const size_t smem = fwd_smem_bytes();
   dim3 grid(a.pr.nt * a.pr.B * a.pr.H);
   if (a.pr.drop_p8 > 0)
-    return launch_pdl(fa_fwd_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to,
-                      a);
-  return launch_pdl(fa_fwd_kernel<false, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, to, a);
+    return launch_pdl(fa_fwd_kernel<true, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, a);
+  return launch_pdl(fa_fwd_kernel<false, false>, grid, dim3(kThreads), smem, st, tq, tk, tv, a);
 }
 
 cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
@@ -591,9 +588,8 @@ cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
   cudaError_t e = launch_fwd_config();
   if (e != cudaSuccess) return e;
   const dim3 grid(a.pr.nt * a.pr.B * a.pr.H, a.n_split);
-  // the O tensor map is not used in split mode (the merge kernel writes O)
   e = launch_pdl(fa_fwd_kernel<false, true>, grid, dim3(kThreads), fwd_smem_bytes(), st, tq, tk, tv,
-                 tq, a);
+                 a);
   if (e != cudaSuccess) return e;
   const dim3 mgrid((a.pr.N + 31) / 32, a.pr.B * a.pr.H);
   return launch_pdl(fa_fwd_merge_kernel<kHeadDim>, mgrid, dim3(256), 0, st, a);

@@ -74,6 +74,32 @@ __device__ __forceinline__ uint32_t drop_head_key(const Problem &pr, int bh) {
   return pcg_hash(pcg_hash(pcg_hash(pr.seed_lo) ^ pr.seed_hi) ^ static_cast<uint32_t>(bh));
 }
 
+// Dropout keep bits of 32 query columns of one key row in the backward
+// (thread = key row): bit e is Z(q0 + e, key).  kk = head key ^ (key >> 1);
+// sh = 8 * (key & 1) selects the key's byte among each 2x2 block word (even
+// queries: bytes 0-1, odd: 2-3).  Called by a converged warp.
+__device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32_t p8, int q0) {
+  // keys 2m and 2m + 1 sit in adjacent lanes and draw on the same hash word
+  // of each 2x2 block: each lane of the pair hashes half of the 16 query
+  // pairs (the even lane pairs 0-7, the odd lane 8-15) and the two swap their
+  // words with one shuffle (the warp is converged here)
+  const uint32_t odd = threadIdx.x & 1u;
+  uint32_t bits = 0u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t qp = static_cast<uint32_t>((q0 + 2 * k + 16 * static_cast<int>(odd)) >> 1);
+    const uint32_t w = pcg_hash(kk ^ (qp << 16));
+    const uint32_t o = __shfl_xor_sync(0xffffffffu, w, 1);
+    const uint32_t ra = (odd ? o : w) >> sh;   // queries q0 + 2k, q0 + 2k + 1
+    const uint32_t rb = (odd ? w : o) >> sh;   // queries q0 + 16 + 2k, + 1
+    bits |= static_cast<uint32_t>((ra & 0xffu) >= p8) << (2 * k);
+    bits |= static_cast<uint32_t>(((ra >> 16) & 0xffu) >= p8) << (2 * k + 1);
+    bits |= static_cast<uint32_t>((rb & 0xffu) >= p8) << (2 * k + 16);
+    bits |= static_cast<uint32_t>(((rb >> 16) & 0xffu) >= p8) << (2 * k + 17);
+  }
+  return bits;
+}
+
 struct FwdArgs {
   Problem pr;
   float *lse;             // [B, H, N]
@@ -189,8 +215,9 @@ unsigned long long current_context_id();
 cudaError_t launch_csr_to_dense(const int32_t *row_ptr, const int32_t *col_idx, int nnz, int nb,
                                 uint8_t *dense, int *err, cudaStream_t st);
 
+// (the d = 64 forward writes O from registers: no O tensor map)
 cudaError_t launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &to, const FwdArgs &a, cudaStream_t st);
+                       const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_splitkv(const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const FwdArgs &a, cudaStream_t st);
 // The same two entry points for d = 128 (fa_fwd_d128.cu); the tensor maps
