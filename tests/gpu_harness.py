@@ -86,11 +86,15 @@ def rel_fro(got: np.ndarray, want: np.ndarray) -> float:
     return float(num / den) if den > 0 else float(num)
 
 
-def assert_o(got, want, what="O"):
+def assert_o(got, want, what="O", maxabs_scale=1.0):
+    """O within the parity tolerances; maxabs_scale widens the absolute bound
+    for outputs scaled up on purpose (dropout's 1/(1-p'): every kept term of
+    O, and its bf16 rounding, is multiplied by it; the relative bound holds as is)."""
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     ma = float(np.max(np.abs(got - want))) if got.size else 0.0
     rf = rel_fro(got, want)
-    assert ma <= TOL_O_MAXABS and rf <= TOL_O_RELFRO, f"{what}: max-abs {ma:.3e}, rel-fro {rf:.3e}"
+    assert ma <= TOL_O_MAXABS * maxabs_scale and rf <= TOL_O_RELFRO, \
+        f"{what}: max-abs {ma:.3e}, rel-fro {rf:.3e}"
     return ma, rf
 
 
