@@ -835,6 +835,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_commit_w(&s.bar_dq_full);
           mma_commit_w(&s.bar_ds_free);
         }
+        // after the item's last dQ, not its last dK: dQ reads K_j from the
+        // buffer the epilogue then overwrites with the dK / dV staging
         if (ok) mma_commit_w(&s.bar_done);
       }
       mma_commit_w(&s.bar_final);
