@@ -240,6 +240,14 @@ __global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
 constexpr int kMainThreads = 512;
 constexpr uint32_t kRegsElementwise = 160, kRegsDq = 96, kRegsControl = 96;
 
+// One work item: key tile kt of head bh and the query tiles that attend to
+// it (from causal_first_qtile under causal, the block mask's column kt, none
+// at all when the tile lies past kv_len).
+struct Item {
+  int kt, bh, n, rot, i_begin;
+  int kv_bound;
+};
+
 struct __align__(1024) BwdSmem {
   uint8_t kv[2][2][kTileBytes];          // [item parity][K_j | V_j]; later dK / dV staging
   uint8_t q[kStages][kTileBytes];
@@ -267,6 +275,7 @@ struct __align__(1024) BwdSmem {
   uint64_t bar_item_full[4];
   uint64_t bar_item_empty[4];
   int item_ring[4];
+  Item item_info[4];   // the items, as the producer computed them (the others read them here)
   uint32_t tmem_base;
   int abort;
 };
@@ -290,13 +299,6 @@ constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ
                    kColPT = 448;
 constexpr uint32_t kTmemCols = 512;
 
-// One work item: key tile kt of head bh and the query tiles that attend to
-// it (from causal_first_qtile under causal, the block mask's column kt, none
-// at all when the tile lies past kv_len).
-struct Item {
-  int kt, bh, n, rot, i_begin;
-  int kv_bound;
-};
 
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
@@ -484,9 +486,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int v = 0; ok; ++v) {
       if (!wg_wait(&s.bar_item_full[v & 3], (v >> 2) & 1)) break;
       const int t = s.item_ring[v & 3];
+      const Item itm = s.item_info[v & 3];
       warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
-      const Item itm = item_at(a, t);
       const bool key_ok = itm.kt * kTile + kr < itm.kv_bound;
       uint32_t drop_kk = 0u, drop_sh = 0u;
       if (kDrop) {
@@ -641,9 +643,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                                                 &s.abort)))
         break;
       const int t = s.item_ring[v & 3];
+      const Item itm = s.item_info[v & 3];
       warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
-      const Item itm = item_at(a, t);
       for (int k = 0; k < itm.n; ++k, ++g) {
         // the accumulator rows of this step (looked up before the wait)
         const int row0 = itm.bh * a.n_pad + qtile_of(a, itm, k) * kTile;
@@ -708,13 +710,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // barrier (item v's own store) can complete before this wait looks.
         if (v >= 2 && !mbar_wait_warp(&s.bar_kv_free[kb], ((v - 2) >> 1) & 1, pr.wait, &s.abort))
           break;
+        // the item's schedule, computed once here (its global lookups: the
+        // longest-first order, the column count, kv_len) and handed over with it
+        Item itm{};
+        if (t < n_items) itm = item_at(a, t);
         if (lane == 0) {
           s.item_ring[slot] = t;
+          s.item_info[slot] = itm;
           mbar_arrive(&s.bar_item_full[slot]);
         }
         __syncwarp();
         if (t >= n_items) break;
-        const Item itm = item_at(a, t);
         if (itm.n == 0) continue;
         mbar_arrive_expect_tx_w(&s.bar_kv[kb], 2 * kTileBytes);
         tma_load_3d_w(s.kv[kb][0], &tm_k, &s.bar_kv[kb], 0, itm.kt * kTile, itm.bh);
@@ -750,11 +756,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int v = 0; ok; ++v) {
         if (!mbar_wait_warp(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
         const int t = s.item_ring[v & 3];
+        const Item itm = s.item_info[v & 3];
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.bar_item_empty[v & 3]);
         __syncwarp();
         if (t >= n_items) break;
-        const Item itm = item_at(a, t);
         if (itm.n == 0) continue;
         const int kb = v & 1;
         const uint32_t k_addr = smem_u32(s.kv[kb][0]), v_addr = smem_u32(s.kv[kb][1]);

@@ -47,6 +47,14 @@ constexpr uint32_t kRegsElementwise = 160, kRegsDq = 96, kRegsControl = 96;
 constexpr uint32_t kEwWarps = 8, kDqWarps = 4;
 constexpr uint32_t kItemConsumers = 1 + kEwWarps + kDqWarps;
 
+// One work item: key tile kt of head bh and its query steps (two per query
+// tile that attends to the key tile: from causal_first_qtile under causal,
+// the block mask's column kt, none past kv_len).
+struct Item {
+  int kt, bh, n, rot, i_begin;
+  int kv_bound;
+};
+
 struct __align__(1024) Bwd128Smem {
   uint8_t kv[2][kKvBytes];                // K_j | V_j; later dK | dV staging
   uint8_t q[kStages][kQBytes];
@@ -73,6 +81,7 @@ struct __align__(1024) Bwd128Smem {
   uint64_t bar_item_full[4];
   uint64_t bar_item_empty[4];
   int item_ring[4];
+  Item item_info[4];   // the items, as the producer computed them (the others read them here)
   uint32_t tmem_base;
   int abort;
 };
@@ -88,13 +97,6 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// One work item: key tile kt of head bh and its query steps (two per query
-// tile that attends to the key tile: from causal_first_qtile under causal,
-// the block mask's column kt, none past kv_len).
-struct Item {
-  int kt, bh, n, rot, i_begin;
-  int kv_bound;
-};
 
 __device__ __forceinline__ Item item_at(const BwdArgs &a, int t) {
   const Problem &pr = a.pr;
@@ -281,9 +283,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int v = 0; ok; ++v) {
       if (!wg_wait(&s.bar_item_full[v & 3], (v >> 2) & 1)) break;
       const int t = s.item_ring[v & 3];
+      const Item itm = s.item_info[v & 3];
       warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
-      const Item itm = item_at(a, t);
       const bool key_ok = itm.kt * kTile + kr < itm.kv_bound;
       uint32_t drop_kk = 0u, drop_sh = 0u;
       if (kDrop) {
@@ -415,9 +417,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int v = 0; ok; ++v) {
       if (!mbar_wait_warp(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
       const int t = s.item_ring[v & 3];
+      const Item itm = s.item_info[v & 3];
       warp_arrive(&s.bar_item_empty[v & 3]);
       if (t >= n_items) break;
-      const Item itm = item_at(a, t);
       for (int k = 0; k < itm.n; ++k, ++g) {
         // the accumulator rows of this step (looked up before the wait)
         const int row0 = itm.bh * a.n_pad + qstep_of(a, itm, k) * kQStep;
@@ -475,13 +477,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // Waited before item v is published, so that no later phase of the
         // barrier (item v's own store) can complete before this wait looks.
         if (v >= 1 && !mbar_wait_warp(&s.bar_kv_free, (v - 1) & 1, pr.wait, &s.abort)) break;
+        // the item's schedule, computed once here (its global lookups: the
+        // longest-first order, the column count, kv_len) and handed over with it
+        Item itm{};
+        if (t < n_items) itm = item_at(a, t);
         if (lane == 0) {
           s.item_ring[slot] = t;
+          s.item_info[slot] = itm;
           mbar_arrive(&s.bar_item_full[slot]);
         }
         __syncwarp();
         if (t >= n_items) break;
-        const Item itm = item_at(a, t);
         if (itm.n == 0) continue;
         mbar_arrive_expect_tx_w(&s.bar_kv, 2 * kKvBytes);
         tma_load_3d_w(s.kv[0], &tm_k, &s.bar_kv, 0, itm.kt * kTile, itm.bh);
@@ -526,11 +532,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int v = 0; ok; ++v) {
         if (!mbar_wait_warp(&s.bar_item_full[v & 3], (v >> 2) & 1, pr.wait, &s.abort)) break;
         const int t = s.item_ring[v & 3];
+        const Item itm = s.item_info[v & 3];
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.bar_item_empty[v & 3]);
         __syncwarp();
         if (t >= n_items) break;
-        const Item itm = item_at(a, t);
         if (itm.n == 0) continue;
         if (!mbar_wait_warp(&s.bar_kv, kv_use & 1, pr.wait, &s.abort)) break;
         ++kv_use;
