@@ -38,6 +38,12 @@ constexpr int kKStages = 3, kVStages = 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // 16 KiB bf16 tile
 
+// One unit of work: query tile qt of head bh and its key-tile range.  id is
+// the CTA index it was launched as (blockIdx.x), mapped by work_order.
+struct Unit {
+  int qt, bh, kv_bound, j_begin, j_end;
+};
+
 struct __align__(1024) FwdSmem {
   uint8_t q[kTileBytes];              // Q_i of the current unit
   uint8_t k[kKStages][kTileBytes];
@@ -60,6 +66,7 @@ struct __align__(1024) FwdSmem {
   uint4 clc_resp;                     // its 16-byte response
   int unit_id[2];                     // CTA index of the unit in the slot, -1: no more units
   int unit_n[2];                      // its number of key tiles
+  Unit unit_info[2];                  // the unit as the producer computed it
   uint32_t tmem_base;
   int abort;
   int16_t tiles[2][kMaxMaskTiles];    // block-sparse: the unit's key tiles, per ring slot
@@ -73,11 +80,6 @@ constexpr uint32_t kSoftmaxWarps = 4;
 // Consumers of the unit ring: the MMA warp and the four softmax warps.
 constexpr uint32_t kUnitConsumers = 1 + kSoftmaxWarps;
 
-// One unit of work: query tile qt of head bh and its key-tile range.  id is
-// the CTA index it was launched as (blockIdx.x), mapped by work_order.
-struct Unit {
-  int qt, bh, kv_bound, j_begin, j_end;
-};
 
 template <bool kSplit>
 __device__ __forceinline__ Unit unit_at(const FwdArgs &args, int id) {
@@ -234,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) {
         s.unit_id[slot] = id;
         s.unit_n[slot] = n;
+        s.unit_info[slot] = u;   // (its kv_len lookup is not repeated by the softmax warps)
       }
       __threadfence_block();
       __syncwarp();
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!mbar_wait_warp(&s.bar_unit_full[slot], (v >> 1) & 1, pr.wait, &s.abort)) break;
       const int id = s.unit_id[slot], n = s.unit_n[slot];
       if (id < 0) break;
-      const Unit u = unit_at<kSplit>(args, id);
+      const Unit u = s.unit_info[slot];
       const int qt = u.qt, bh = u.bh, kv_bound = u.kv_bound;
       const int qrow = qt * kTile + row;
       float m = -INFINITY;     // running max of S*scale*log2e
