@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import json
 import math
 import os
@@ -538,6 +539,10 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local)
     barrier(world, device)
     torch.cuda.synchronize(device)
+    # no collector pause while the host enqueues the timed steps (a pause longer
+    # than the queue the host has built up would show as GPU idle time)
+    gc.collect()
+    gc.disable()
     sampler.start()
     wall0 = time.perf_counter()
     for i in range(K):
@@ -551,6 +556,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - wall0
     sampler.stop()
+    gc.enable()
     fa.fa_set_bwd_main_events(None, None)
     barrier(world, device)
     fa.fa_check(stream)
@@ -620,6 +626,8 @@ def run_ours(args, rank, world, local):
         for _ in range(2):
             fn()
         torch.cuda.synchronize(device)
+        gc.collect()
+        gc.disable()
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
         barrier(world, device)
@@ -629,6 +637,7 @@ def run_ours(args, rank, world, local):
             fn()
             e1[i].record(stream)
         torch.cuda.synchronize(device)
+        gc.enable()
         fa.fa_check(stream)
         return max_over_ranks(sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / 1e3,
                               world, device)
@@ -733,6 +742,10 @@ def run_fwd_only(args, rank, world, local):
     sampler = ClockSampler(local)
     barrier(world, device)
     torch.cuda.synchronize(device)
+    # no collector pause while the host enqueues the timed steps (a pause longer
+    # than the queue the host has built up would show as GPU idle time)
+    gc.collect()
+    gc.disable()
     sampler.start()
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -741,6 +754,7 @@ def run_fwd_only(args, rank, world, local):
         ev1[i].record(stream)
     torch.cuda.synchronize(device)
     sampler.stop()
+    gc.enable()
     barrier(world, device)
     fa.fa_check(stream)
     t_job = max_over_ranks(sum(ev0[i].elapsed_time(ev1[i]) for i in range(K)) / 1e3, world,
@@ -863,6 +877,10 @@ def run_decode(args, rank, world, local):
     sampler = ClockSampler(local)
     barrier(world, device)
     torch.cuda.synchronize(device)
+    # no collector pause while the host enqueues the timed steps (a pause longer
+    # than the queue the host has built up would show as GPU idle time)
+    gc.collect()
+    gc.disable()
     sampler.start()
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -871,6 +889,7 @@ def run_decode(args, rank, world, local):
         e1[i].record(stream)
     torch.cuda.synchronize(device)
     sampler.stop()
+    gc.enable()
     fa.fa_check(stream)
     t_rank = sum(e0[i].elapsed_time(e1[i]) for i in range(K)) / 1e3
     t_job = max_over_ranks(t_rank, world, device)
