@@ -904,7 +904,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     configured_dev = dev;
   }
   if (a.pr.block_mask &&
-      (e = launch_pdl(fa_bwd_cols_kernel, dim3(a.pr.nt), dim3(256), 0, st, a)) != cudaSuccess)
+      (e = launch_ordered(fa_bwd_cols_kernel, dim3(a.pr.nt), dim3(256), 0, st, a)) != cudaSuccess)
     return e;
   // preprocess: n_pad / (32 rows x 4) blocks per head cover the padded rows exactly
   const dim3 pre_grid(a.n_pad / (kRowsPerBlock * kRowsPerThread), a.pr.B * a.pr.H);

@@ -1,7 +1,7 @@
 """More GPU edge cases against the fp64 oracle: masks combined with dropout
 at d = 128, an empty CSR mask, many tiny heads (the persistent backward's
 scheduler with hundreds of items per CTA), concurrent calls on two streams
-with their own workspaces."""
+with their own workspaces, back-to-back backward calls sharing one workspace."""
 import numpy as np
 import pytest
 
@@ -141,3 +141,48 @@ def test_forwards_on_concurrent_streams_match_serial_runs(H, d):
         for (o, lse), (o_r, lse_r) in zip(got, ref):
             assert torch.equal(o.view(torch.int16), o_r.view(torch.int16))
             assert torch.equal(lse, lse_r)
+
+
+@pytest.mark.parametrize("d,masked", [(64, False), (64, True), (128, False), (128, True)])
+def test_backwards_back_to_back_share_a_workspace(H, d, masked):
+    """Three backward calls on different inputs enqueued back to back on one
+    stream, with no forward and no synchronisation between them, all sharing
+    one workspace.  Each call's zeroing of the dQ accumulators starts without
+    waiting for the previous kernel, so it must not overtake the previous
+    call's dQ conversion (or its main kernel): every call's dK and dV equal,
+    bit for bit, and its dQ matches (within the gradient tolerance) the same
+    call run on its own: element by element within two bf16 ulps (the fp32
+    partial sums are added in hardware order) plus 1e-3 of the largest
+    magnitude, so that even one row with a lost or stale partial fails."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    B, Hh, N = 2, 8, 4096 if d == 64 else 2048
+    nb = -(-N // 128)
+    xs = []
+    for i in range(3):
+        mask = None
+        if masked:
+            m = np.random.default_rng(140 + i).random((nb, nb)) < 0.3
+            mask = (m | np.eye(nb, dtype=bool)).astype(np.uint8)
+        xs.append(H.Inputs(W.make("tiny", seed=140 + i, d=d, B=B, H=Hh, N=N), block_mask=mask))
+    fwd = [H.run_fwd(x) for x in xs]
+    solo = [H.run_bwd(x, o, lse) for x, (o, lse) in zip(xs, fwd)]
+    shape = (B, Hh, N, d)
+    nbytes = fa.fa_bwd_workspace_size(B, Hh, N, d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    outs = [tuple(H.nan_like_bf16(shape) for _ in range(3)) for _ in xs]
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    for x, (o, lse), (dq, dk, dv) in zip(xs, fwd, outs):
+        fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hh, N, d, x.scale, x.causal,
+                  x.kv_len, x.mask, ws, nbytes, st)
+    fa.fa_check(st)
+    for (dq, dk, dv), (dq_s, dk_s, dv_s) in zip(outs, solo):
+        assert torch.equal(dk.view(torch.int16), dk_s.view(torch.int16))
+        assert torch.equal(dv.view(torch.int16), dv_s.view(torch.int16))
+        got, want = H.host_f64(dq), H.host_f64(dq_s)
+        assert np.all(np.isfinite(got))
+        bound = 2.0 ** -6 * np.abs(want) + 1e-3 * np.abs(want).max()
+        bad = np.abs(got - want) > bound
+        assert not bad.any(), f"dQ: {int(bad.sum())} elements differ from the call on its own"
+
