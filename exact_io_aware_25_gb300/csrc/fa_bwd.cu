@@ -34,25 +34,48 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
 
-// Preprocess, one (b, h) per blockIdx.y: 8 threads per row, each reading 8
-// bf16 of O and dO (16 bytes each) and zeroing 8 fp32 accumulators.  Each
-// thread takes kRowsPerThread rows, spaced one block-row apart, and issues all
-// their loads before using any, so enough requests are in flight.  Rows past
-// N (up to the 128-row padding) get D = 0 and lse2 = +inf.
+// Preprocess.  The fp32 dQ accumulators are zeroed either by its first
+// n_zero blocks (kZeroPerThread float4 per thread, 64 KiB per block), or, when
+// n_zero is 0, row by row by the blocks below.  Nothing in the zeroing depends
+// on the previous kernel on the stream, so the zeroing blocks store without
+// waiting for it, on whatever SMs that kernel's tail leaves idle, and exit.
+// (The accumulators' previous reader, the dQ conversion of an earlier call,
+// lets its successors launch only after its reads.)  The other blocks wait,
+// then take one (b, h) per n_pad / 128 blocks: 8 threads per row, each
+// reading 8 bf16 of O and dO (16 bytes each).  Each thread takes
+// kRowsPerThread rows, spaced one block-row apart, and issues all their loads
+// before using any, so enough requests are in flight.  Rows past N (up to
+// the 128-row padding) get D = 0 and lse2 = +inf.
 constexpr int kRowsPerThread = 4;
 constexpr int kRowsPerBlock = 256 / 8;  // rows one pass of a block covers
+constexpr int kZeroPerThread = 16;
+constexpr size_t kZeroPerBlock = 256 * kZeroPerThread;  // float4 per zeroing block
+constexpr int kZeroAheadMaxN = 2048;
 
 template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
-  pdl_wait();
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, unsigned n_zero,
+                                                         size_t n4) {
   pdl_trigger();
+  if (blockIdx.x < n_zero) {
+    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc);
+    const size_t base = blockIdx.x * kZeroPerBlock + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kZeroPerThread; ++u) {
+      const size_t i = base + static_cast<size_t>(u) * 256;
+      if (i < n4) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  pdl_wait();
   constexpr int kV = D / 64;  // 16-byte words of O (and of dO) per thread and row
   const Problem &pr = a.pr;
-  const int bh = blockIdx.y;
+  const int blocks_per_head = a.n_pad / (kRowsPerBlock * kRowsPerThread);
+  const int blk = static_cast<int>(blockIdx.x - n_zero);
+  const int bh = blk / blocks_per_head, bx = blk - bh * blocks_per_head;
   const int sub = threadIdx.x & 7;
-  const int r0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.sched = 0;
-  if (pr.block_mask && blockIdx.x == 0 && blockIdx.y == 0) {
+  const int r0 = bx * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 3);
+  if (blk == 0 && threadIdx.x == 0) *a.sched = 0;
+  if (pr.block_mask && blk == 0) {
     // the key tiles by descending number of query tiles (counting sort; ties
     // in any order): the main kernel hands out each head group's items
     // longest first, so that the ones left for the end are the shortest
@@ -112,9 +135,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
     dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
     const size_t g = ws_row0 + i;
-    float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + g * D + sub * (D / 8));
+    if (n_zero == 0) {
+      float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + g * D + sub * (D / 8));
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) acc[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w = 0; w < D / 32; ++w) acc[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (sub == 0) {
       a.dsum[g] = dsum;
       float l2 = INFINITY;  // padding rows and rows with no allowed key: P = 0
@@ -131,11 +156,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a) {
 
 // dQ = scale * accumulator -> bf16, one (b, h) per blockIdx.y; a thread
 // converts 8 consecutive values of a row (chunk c: row c / 8, part c % 8) for
-// kRowsPerThread chunks spaced one block apart.
+// kRowsPerThread chunks spaced one block apart.  Its successors may launch
+// only once every block is past its reads of the accumulators (the next
+// call's zeroing writes them without waiting).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
   pdl_wait();
-  pdl_trigger();
   const Problem &pr = a.pr;
   const int bh = blockIdx.y;
   const int chunks = pr.N * (D / 8);
@@ -166,6 +192,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
     out.w = pack_bf16(y[u].z * s, y[u].w * s);
     *reinterpret_cast<uint4 *>(dq_head + static_cast<size_t>(c) * 8) = out;
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- main kernel
@@ -906,12 +933,22 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (a.pr.block_mask &&
       (e = launch_ordered(fa_bwd_cols_kernel, dim3(a.pr.nt), dim3(256), 0, st, a)) != cudaSuccess)
     return e;
-  // preprocess: n_pad / (32 rows x 4) blocks per head cover the padded rows exactly
-  const dim3 pre_grid(a.n_pad / (kRowsPerBlock * kRowsPerThread), a.pr.B * a.pr.H);
+  // preprocess: n_pad / (32 rows x 4) blocks per head, which cover the padded
+  // rows exactly, after the zeroing blocks (every padded row of every head)
+  // on sequences of up to kZeroAheadMaxN: the zeroing is O(N) work against an
+  // O(N^2) step, worth taking off the step's path only while N is short (on
+  // long sequences its stores mostly slow the previous kernel's last work)
+  const size_t n4 = static_cast<size_t>(a.pr.B) * a.pr.H * a.n_pad * (a.pr.d / 4);
+  const unsigned n_zero = a.pr.N <= kZeroAheadMaxN
+                              ? static_cast<unsigned>((n4 + kZeroPerBlock - 1) / kZeroPerBlock)
+                              : 0u;
+  const dim3 pre_grid(n_zero + static_cast<unsigned>(a.n_pad / (kRowsPerBlock * kRowsPerThread)) *
+                                   static_cast<unsigned>(a.pr.B * a.pr.H));
   if ((e = a.pr.d == kHeadDimWide
-               ? launch_pdl(fa_bwd_pre_kernel<kHeadDimWide>, pre_grid, dim3(256), 0, st, a)
-               : launch_pdl(fa_bwd_pre_kernel<kHeadDim>, pre_grid, dim3(256), 0, st, a)) !=
-      cudaSuccess)
+               ? launch_pdl(fa_bwd_pre_kernel<kHeadDimWide>, pre_grid, dim3(256), 0, st, a, n_zero,
+                            n4)
+               : launch_pdl(fa_bwd_pre_kernel<kHeadDim>, pre_grid, dim3(256), 0, st, a, n_zero,
+                            n4)) != cudaSuccess)
     return e;
   if (a.pr.d == kHeadDimWide) {
     if ((e = launch_bwd_main_d128(tq, tk, tv, tdo, tdk, tdv, tdq_acc, a, st, ev_start, ev_stop)) !=
