@@ -30,6 +30,10 @@
  *   - stream is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call is asynchronous on it; outputs are fully overwritten, never
  *     accumulated.
+ *   - The library's kernels let the next kernel on the stream begin
+ *     launching while they finish (programmatic dependent launch); each reads
+ *     its inputs only once the previous kernel has completed.  The one
+ *     exception is fa_bwd's workspace (see there).
  *   - Every argument is validated before anything is launched; a failed call
  *     launches nothing.  There is no CPU fallback and no other backend.
  */
@@ -104,6 +108,14 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace      in : device scratch of >= fa_bwd_workspace_size() bytes,
  *                       16-byte aligned, owned by the caller; its contents
  *                       on entry do not matter and are garbage on return.
+ *                       For N <= 2048 and no block mask, fa_bwd starts
+ *                       zeroing part of it while the previous kernel on the
+ *                       stream, if it is one of this library's, may still be
+ *                       running: the workspace must not share memory with
+ *                       anything that call's kernels read or write (a
+ *                       buffer released to a stream-ordered allocator after
+ *                       that call and handed back as the workspace does).
+ *                       Successive fa_bwd calls may share one workspace.
  * Masks and scale must be the ones given to fa_fwd.
  */
 FA_API fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
