@@ -188,3 +188,29 @@ def test_backwards_back_to_back_share_a_workspace(H, d, masked, N):
         bad = np.abs(got - want) > bound
         assert not bad.any(), f"dQ: {int(bad.sum())} elements differ from the call on its own"
 
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [2048, 2049])
+@pytest.mark.parametrize("variant", ["causal", "kv_len"])
+def test_either_side_of_the_ahead_zeroing_length(H, oracle_mod, d, N, variant):
+    """The backward zeroes its dQ accumulators ahead of its wait for the
+    previous kernel up to N = 2048 and in the preprocess beyond: both sides
+    against the oracle (fwd and bwd run back to back, without a host
+    synchronisation between them)."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    kw = {"causal": True} if variant == "causal" else {"kv_len": np.array([N - 300], np.int32)}
+    x = H.Inputs(W.make("tiny", seed=160 + N + d, d=d, B=1, H=2, N=N), **kw)
+    shape = (x.B, x.H, x.N, x.d)
+    o = H.nan_like_bf16(shape)
+    lse = torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    grads = tuple(H.nan_like_bf16(shape) for _ in range(3))
+    nbytes = fa.fa_bwd_workspace_size(x.B, x.H, x.N, x.d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    fa.fa_fwd(x.q, x.k, x.v, o, lse, x.B, x.H, x.N, x.d, x.scale, x.causal, x.kv_len, None, st)
+    fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, *grads, x.B, x.H, x.N, x.d, x.scale, x.causal,
+              x.kv_len, None, ws, nbytes, st)
+    fa.fa_check(st)
+    _check_all(H, oracle_mod, x, o, lse, grads)
