@@ -27,7 +27,8 @@ struct RowDrop {
 // Exponentials of 64 consecutive S columns sv[0..64) of a row: sv[c] <-
 // 2^(sv[c]*sl2 - m), accumulated into the eight partial sums (before
 // dropout) and packed to bf16 pairs in pk, with dropped elements packed as 0
-// when kDrop (jp0 = key pair index of sv[0]).
+// when kDrop (jp0 = key pair index of sv[0]).  Called by a converged warp
+// whose lanes hold consecutive rows, even rows in even lanes.
 template <bool kDrop>
 __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8)[8],
                                       uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
@@ -42,12 +43,27 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
 #pragma unroll
     for (int u = 0; u < 8; u += 2)
       add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
+    // the block words of key pairs (c >> 1) + 0..3 (keys c + u and c + u + 1
+    // share one): rows 2i and 2i + 1 sit in adjacent lanes and draw on the
+    // same words, so each lane of the pair hashes two of the four and the two
+    // swap them with one shuffle each
+    uint32_t wd[4] = {0u, 0u, 0u, 0u};
+    if (kDrop) {
+      const uint32_t odd = threadIdx.x & 1u;
+      const uint32_t p = jp0 + static_cast<uint32_t>(c >> 1) + 2u * odd;
+      const uint32_t w0 = pcg_hash(rd.key ^ p), w1 = pcg_hash(rd.key ^ (p + 1u));
+      const uint32_t o0 = __shfl_xor_sync(0xffffffffu, w0, 1);
+      const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w1, 1);
+      wd[0] = odd ? o0 : w0;
+      wd[1] = odd ? o1 : w1;
+      wd[2] = odd ? w0 : o0;
+      wd[3] = odd ? w1 : o1;
+    }
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
       float a = sv[c + u], b = sv[c + u + 1];
       if (kDrop) {
-        // keys c + u (even) and c + u + 1 share one block word
-        const uint32_t r = pcg_hash(rd.key ^ (jp0 + static_cast<uint32_t>((c + u) >> 1))) >> rd.shift;
+        const uint32_t r = wd[u >> 1] >> rd.shift;
         a = (r & 0xffu) >= rd.p8 ? a : 0.f;
         b = ((r >> 8) & 0xffu) >= rd.p8 ? b : 0.f;
       }
