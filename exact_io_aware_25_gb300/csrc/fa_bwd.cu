@@ -391,8 +391,8 @@ __device__ __forceinline__ void store_p32(const uint32_t (&v)[32], int qc, uint3
       const int e = 16 * c + 2 * t;
       float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
       if (kDrop) {
-        x0 = (keep >> e) & 1u ? x0 : 0.f;
-        x1 = (keep >> (e + 1)) & 1u ? x1 : 0.f;
+        x0 = keep_bit(keep, e) ? x0 : 0.f;
+        x1 = keep_bit(keep, e + 1) ? x1 : 0.f;
       }
       pw[t] = pack_bf16(x0, x1);
     }
@@ -418,7 +418,7 @@ __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint3
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         dp[u] = __uint_as_float(dv[e0 + u]);
-        if (kDrop) dp[u] = (keep >> (e0 + u)) & 1u ? dp[u] * keep_scale : 0.f;
+        if (kDrop) dp[u] = keep_bit(keep, e0 + u) ? dp[u] * keep_scale : 0.f;
       }
       sub2(dp[0], dp[1], dp[0], dp[1], d4.x, d4.y);
       sub2(dp[2], dp[3], dp[2], dp[3], d4.z, d4.w);

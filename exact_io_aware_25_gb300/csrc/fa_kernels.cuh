@@ -75,29 +75,45 @@ __device__ __forceinline__ uint32_t drop_head_key(const Problem &pr, int bh) {
 }
 
 // Dropout keep bits of 32 query columns of one key row in the backward
-// (thread = key row): bit e is Z(q0 + e, key).  kk = head key ^ (key >> 1);
-// sh = 8 * (key & 1) selects the key's byte among each 2x2 block word (even
-// queries: bytes 0-1, odd: 2-3).  Called by a converged warp.
+// (thread = key row): column e is kept iff keep_bit(bits, e), i.e. Z(q0 + e,
+// key) = 1.  kk = head key ^ (key >> 1); sh = 8 * (key & 1) selects the key's
+// byte among each 2x2 block word (even queries: bytes 0-1, odd: 2-3); p8 is
+// 1..255.  Called by a converged warp.
 __device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32_t p8, int q0) {
   // keys 2m and 2m + 1 sit in adjacent lanes and draw on the same hash word
   // of each 2x2 block: each lane of the pair hashes half of the 16 query
   // pairs (the even lane pairs 0-7, the odd lane 8-15) and the two swap their
   // words with one shuffle (the warp is converged here)
   const uint32_t odd = threadIdx.x & 1u;
+  // byte x >= p8 iff x + (256 - p8) carries out of the byte: the low seven
+  // bits of each byte are added without crossing bytes, and the carry out of
+  // bit 7 is the majority of the two top bits and the carry into it
+  const uint32_t qq = (256u - p8) * 0x01010101u;
   uint32_t bits = 0u;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t qp = static_cast<uint32_t>((q0 + 2 * k + 16 * static_cast<int>(odd)) >> 1);
     const uint32_t w = pcg_hash(kk ^ (qp << 16));
     const uint32_t o = __shfl_xor_sync(0xffffffffu, w, 1);
-    const uint32_t ra = (odd ? o : w) >> sh;   // queries q0 + 2k, q0 + 2k + 1
-    const uint32_t rb = (odd ? w : o) >> sh;   // queries q0 + 16 + 2k, + 1
-    bits |= static_cast<uint32_t>((ra & 0xffu) >= p8) << (2 * k);
-    bits |= static_cast<uint32_t>(((ra >> 16) & 0xffu) >= p8) << (2 * k + 1);
-    bits |= static_cast<uint32_t>((rb & 0xffu) >= p8) << (2 * k + 16);
-    bits |= static_cast<uint32_t>(((rb >> 16) & 0xffu) >= p8) << (2 * k + 17);
+    const uint32_t ra = (odd ? o : w) >> sh;   // bytes 0, 2: queries q0 + 2k, q0 + 2k + 1
+    const uint32_t rb = (odd ? w : o) >> sh;   // bytes 0, 2: queries q0 + 16 + 2k, + 1
+    // the four keep bytes of this key: [2k, 2k + 16, 2k + 1, 2k + 17]
+    const uint32_t x = (ra & 0x00ff00ffu) | ((rb << 8) & 0xff00ff00u);
+    const uint32_t sum7 = (x & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
+    const uint32_t carry = (x & qq) | ((x | qq) & sum7);
+    // their carries (bit 7 of each byte) to bits k, 8 + k, 16 + k, 24 + k
+    bits |= (carry & 0x80808080u) >> (7 - k);
   }
   return bits;
+}
+
+// Bit of keep_bits32's word that holds column e (0..31): columns 2k and
+// 2k + 1 at bits k and 16 + k, columns 16 + 2k and 17 + 2k at 8 + k and 24 + k.
+__device__ __forceinline__ constexpr int keep_pos(int e) {
+  return ((e >> 4) << 3) + ((e & 1) << 4) + ((e & 15) >> 1);
+}
+__device__ __forceinline__ bool keep_bit(uint32_t bits, int e) {
+  return (bits >> keep_pos(e)) & 1u;
 }
 
 struct FwdArgs {
