@@ -32,6 +32,10 @@ struct RowDrop {
 template <bool kDrop>
 __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8)[8],
                                       uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
+  // byte x >= p8 (1..255) iff x + (256 - p8) carries out of the byte
+  const uint32_t qq = kDrop ? (256u - rd.p8) * 0x01010101u : 0u;
+  // this row's keep bytes in each block word: bytes 0-1 (even row), 2-3 (odd)
+  const uint32_t sel = rd.shift ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int c = 0; c < 64; c += 8) {
     float x[8];
@@ -47,28 +51,31 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
     // share one): rows 2i and 2i + 1 sit in adjacent lanes and draw on the
     // same words, so each lane of the pair hashes two of the four and the two
     // swap them with one shuffle each
-    uint32_t wd[4] = {0u, 0u, 0u, 0u};
+    uint32_t km[4] = {~0u, ~0u, ~0u, ~0u};  // per bf16 pair: 0xffff over each kept column
     if (kDrop) {
       const uint32_t odd = threadIdx.x & 1u;
       const uint32_t p = jp0 + static_cast<uint32_t>(c >> 1) + 2u * odd;
       const uint32_t w0 = pcg_hash(rd.key ^ p), w1 = pcg_hash(rd.key ^ (p + 1u));
       const uint32_t o0 = __shfl_xor_sync(0xffffffffu, w0, 1);
       const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w1, 1);
-      wd[0] = odd ? o0 : w0;
-      wd[1] = odd ? o1 : w1;
-      wd[2] = odd ? w0 : o0;
-      wd[3] = odd ? w1 : o1;
+      const uint32_t wd0 = odd ? o0 : w0, wd1 = odd ? o1 : w1;
+      const uint32_t wd2 = odd ? w0 : o0, wd3 = odd ? w1 : o1;
+      // the keep bytes of columns c .. c + 3 and c + 4 .. c + 7, four per
+      // word, compared with p8 at once: bit 7 of each byte is the carry
+      const uint32_t x0 = prmt(wd0, wd1, sel), x1 = prmt(wd2, wd3, sel);
+      const uint32_t s0 = (x0 & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
+      const uint32_t s1 = (x1 & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
+      const uint32_t k0 = (x0 & qq) | ((x0 | qq) & s0);
+      const uint32_t k1 = (x1 & qq) | ((x1 | qq) & s1);
+      // each column's carry replicated over its half of the bf16 pair
+      km[0] = prmt(k0, 0u, 0x9988u);
+      km[1] = prmt(k0, 0u, 0xbbaau);
+      km[2] = prmt(k1, 0u, 0x9988u);
+      km[3] = prmt(k1, 0u, 0xbbaau);
     }
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      float a = sv[c + u], b = sv[c + u + 1];
-      if (kDrop) {
-        const uint32_t r = wd[u >> 1] >> rd.shift;
-        a = (r & 0xffu) >= rd.p8 ? a : 0.f;
-        b = ((r >> 8) & 0xffu) >= rd.p8 ? b : 0.f;
-      }
-      pk[(c + u) >> 1] = pack_bf16(a, b);
-    }
+    for (int u = 0; u < 8; u += 2)
+      pk[(c + u) >> 1] = pack_bf16(sv[c + u], sv[c + u + 1]) & km[u >> 1];
   }
 }
 

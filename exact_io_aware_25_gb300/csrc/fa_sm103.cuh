@@ -558,6 +558,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.
+// Byte permute (PTX prmt, default mode): result byte n is byte (s >> 4n) & 7
+// of {b, a} (a = bytes 0-3); when bit 3 of that nibble is set, it is the
+// selected byte's top bit replicated over all eight bits instead.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(s));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
