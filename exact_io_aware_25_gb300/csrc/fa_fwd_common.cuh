@@ -34,8 +34,10 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
                                       uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
   // byte x >= p8 (1..255) iff x + (256 - p8) carries out of the byte
   const uint32_t qq = kDrop ? (256u - rd.p8) * 0x01010101u : 0u;
-  // this row's keep bytes in each block word: bytes 0-1 (even row), 2-3 (odd)
+  // a row's keep bytes in each block word: bytes 0-1 (even row), 2-3 (odd);
+  // this row's, and its partner's in the adjacent lane
   const uint32_t sel = rd.shift ? 0x7632u : 0x5410u;
+  const uint32_t sel_partner = rd.shift ? 0x5410u : 0x7632u;
 #pragma unroll
   for (int c = 0; c < 64; c += 8) {
     float x[8];
@@ -49,20 +51,19 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
       add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
     // the block words of key pairs (c >> 1) + 0..3 (keys c + u and c + u + 1
     // share one): rows 2i and 2i + 1 sit in adjacent lanes and draw on the
-    // same words, so each lane of the pair hashes two of the four and the two
-    // swap them with one shuffle each
+    // same words, so each lane of the pair hashes two of the four (the even
+    // lane pairs 0-1, the odd lane 2-3), keeps its own row's bytes of them
+    // and hands its partner the partner's with one shuffle
     uint32_t km[4] = {~0u, ~0u, ~0u, ~0u};  // per bf16 pair: 0xffff over each kept column
     if (kDrop) {
       const uint32_t odd = threadIdx.x & 1u;
       const uint32_t p = jp0 + static_cast<uint32_t>(c >> 1) + 2u * odd;
       const uint32_t w0 = pcg_hash(rd.key ^ p), w1 = pcg_hash(rd.key ^ (p + 1u));
-      const uint32_t o0 = __shfl_xor_sync(0xffffffffu, w0, 1);
-      const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w1, 1);
-      const uint32_t wd0 = odd ? o0 : w0, wd1 = odd ? o1 : w1;
-      const uint32_t wd2 = odd ? w0 : o0, wd3 = odd ? w1 : o1;
+      const uint32_t own = prmt(w0, w1, sel);
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, prmt(w0, w1, sel_partner), 1);
       // the keep bytes of columns c .. c + 3 and c + 4 .. c + 7, four per
       // word, compared with p8 at once: bit 7 of each byte is the carry
-      const uint32_t x0 = prmt(wd0, wd1, sel), x1 = prmt(wd2, wd3, sel);
+      const uint32_t x0 = odd ? got : own, x1 = odd ? own : got;
       const uint32_t s0 = (x0 & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
       const uint32_t s1 = (x1 & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
       const uint32_t k0 = (x0 & qq) | ((x0 | qq) & s0);

@@ -89,16 +89,20 @@ __device__ __forceinline__ uint32_t keep_bits32(uint32_t kk, uint32_t sh, uint32
   // bits of each byte are added without crossing bytes, and the carry out of
   // bit 7 is the majority of the two top bits and the carry into it
   const uint32_t qq = (256u - p8) * 0x01010101u;
+  // the four keep bytes of this key for query columns [2k, 2k + 16, 2k + 1,
+  // 2k + 17], picked in one byte permute from {own word, partner's word}:
+  // columns 2k, 2k + 1 are in the word of query pair k (the even lane's),
+  // 16 + 2k, 17 + 2k in that of pair 8 + k (the odd lane's); the key's byte
+  // in a word is sh / 8 (even query) and 2 + sh / 8 (odd query)
+  const uint32_t b = sh >> 3, lo = odd ? 4u : 0u, hi = odd ? 0u : 4u;
+  const uint32_t sel = (lo + b) | ((hi + b) << 4) | ((lo + 2u + b) << 8) | ((hi + 2u + b) << 12);
   uint32_t bits = 0u;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t qp = static_cast<uint32_t>((q0 + 2 * k + 16 * static_cast<int>(odd)) >> 1);
     const uint32_t w = pcg_hash(kk ^ (qp << 16));
     const uint32_t o = __shfl_xor_sync(0xffffffffu, w, 1);
-    const uint32_t ra = (odd ? o : w) >> sh;   // bytes 0, 2: queries q0 + 2k, q0 + 2k + 1
-    const uint32_t rb = (odd ? w : o) >> sh;   // bytes 0, 2: queries q0 + 16 + 2k, + 1
-    // the four keep bytes of this key: [2k, 2k + 16, 2k + 1, 2k + 17]
-    const uint32_t x = (ra & 0x00ff00ffu) | ((rb << 8) & 0xff00ff00u);
+    const uint32_t x = prmt(w, o, sel);
     const uint32_t sum7 = (x & 0x7f7f7f7fu) + (qq & 0x7f7f7f7fu);
     const uint32_t carry = (x & qq) | ((x | qq) & sum7);
     // their carries (bit 7 of each byte) to bits k, 8 + k, 16 + k, 24 + k
