@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdArgs a, unsign
       for (int w = 0; w < D / 32; ++w) acc[w] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (sub == 0) {
-      a.dsum[g] = dsum;
+      a.dsum[g] = -dsum;   // stored negated: the main kernels add it
       float l2 = INFINITY;  // padding rows and rows with no allowed key: P = 0
       if (i < pr.N) {
         const float lse = a.lse[static_cast<size_t>(bh) * pr.N + i];
@@ -416,12 +416,18 @@ __device__ __forceinline__ void ds_store32(const uint32_t (&pv)[32], const uint3
       const float4 d4 = ld_shared_f4(dsum + (qc + e0) * 4);
       float dp[4], ds[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        dp[u] = __uint_as_float(dv[e0 + u]);
-        if (kDrop) dp[u] = keep_bit(keep, e0 + u) ? dp[u] * keep_scale : 0.f;
+      for (int u = 0; u < 4; ++u) dp[u] = __uint_as_float(dv[e0 + u]);
+      if (kDrop) {
+        // dP^T * Z * keep_scale - D in one packed multiply-add per pair
+        float zs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) zs[u] = keep_bit(keep, e0 + u) ? keep_scale : 0.f;
+        fma2(dp[0], dp[1], dp[0], dp[1], zs[0], zs[1], d4.x, d4.y);
+        fma2(dp[2], dp[3], dp[2], dp[3], zs[2], zs[3], d4.z, d4.w);
+      } else {
+        add2(dp[0], dp[1], dp[0], dp[1], d4.x, d4.y);   // (the stored D is negated)
+        add2(dp[2], dp[3], dp[2], dp[3], d4.z, d4.w);
       }
-      sub2(dp[0], dp[1], dp[0], dp[1], d4.x, d4.y);
-      sub2(dp[2], dp[3], dp[2], dp[3], d4.z, d4.w);
       mul2(ds[0], ds[1], __uint_as_float(pv[e0]), __uint_as_float(pv[e0 + 1]), dp[0], dp[1]);
       mul2(ds[2], ds[3], __uint_as_float(pv[e0 + 2]), __uint_as_float(pv[e0 + 3]), dp[2], dp[3]);
       dw[2 * g] = pack_bf16(ds[0], ds[1]);

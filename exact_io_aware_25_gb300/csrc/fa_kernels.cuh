@@ -152,7 +152,7 @@ struct BwdArgs {
   const uint16_t *o;      // [B, H, N, d] bf16
   const uint16_t *dout;   // [B, H, N, d] bf16
   const float *lse;       // [B, H, N]
-  float *dsum;            // workspace D   [B*H, n_pad]
+  float *dsum;            // workspace -D  [B*H, n_pad] (D = rowsum(dO o O), negated)
   float *lse2;            // workspace lse * log2(e) [B*H, n_pad] (+inf in padding rows)
   float *dq_acc;          // workspace dQ accumulators [B*H, n_pad, d]
   int *col_cnt;           // workspace, block mask only: query tiles per key tile [nt]
