@@ -34,6 +34,10 @@
  *     launching while they finish (programmatic dependent launch); each reads
  *     its inputs only once the previous kernel has completed.  The one
  *     exception is fa_bwd's workspace (see there).
+ *   - fa_fwd and fa_bwd may be captured into a CUDA graph on `stream` and the
+ *     graph replayed (each replay resets the backward's counters in its
+ *     workspace); make one call on the shapes outside the capture first,
+ *     which configures the kernels.
  *   - Every argument is validated before anything is launched; a failed call
  *     launches nothing.  There is no CPU fallback and no other backend.
  */

@@ -1,7 +1,9 @@
 """More GPU edge cases against the fp64 oracle: masks combined with dropout
 at d = 128, an empty CSR mask, many tiny heads (the persistent backward's
 scheduler with hundreds of items per CTA), concurrent calls on two streams
-with their own workspaces, back-to-back backward calls sharing one workspace."""
+with their own workspaces, back-to-back backward calls sharing one workspace,
+either side of the backward's ahead-zeroing length, fwd + bwd replayed from a
+CUDA graph."""
 import numpy as np
 import pytest
 
@@ -214,3 +216,53 @@ def test_either_side_of_the_ahead_zeroing_length(H, oracle_mod, d, N, variant):
               x.kv_len, None, ws, nbytes, st)
     fa.fa_check(st)
     _check_all(H, oracle_mod, x, o, lse, grads)
+
+
+@pytest.mark.parametrize("d,masked", [(64, False), (64, True), (128, False)])
+def test_fwd_bwd_captured_in_a_cuda_graph(H, d, masked):
+    """fa_fwd + fa_bwd captured into a CUDA graph and replayed several times
+    (after one eager call on the shapes, which configures the kernels): each
+    replay gives the eager call's O, lse, dK and dV bit for bit and its dQ
+    within two bf16 ulps (fp32 partial sums in hardware order)."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    B, Hh, N = 2, 4, 1000
+    mask = None
+    if masked:
+        nb = -(-N // 128)
+        m = np.random.default_rng(170).random((nb, nb)) < 0.4
+        mask = (m | np.eye(nb, dtype=bool)).astype(np.uint8)
+    x = H.Inputs(W.make("tiny", seed=170 + d, d=d, B=B, H=Hh, N=N), block_mask=mask)
+    o_ref, lse_ref = H.run_fwd(x)
+    dq_ref, dk_ref, dv_ref = H.run_bwd(x, o_ref, lse_ref)
+    shape = (B, Hh, N, d)
+    o = H.nan_like_bf16(shape)
+    lse = torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (H.nan_like_bf16(shape) for _ in range(3))
+    nbytes = fa.fa_bwd_workspace_size(B, Hh, N, d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            st = torch.cuda.current_stream()
+            fa.fa_fwd(x.q, x.k, x.v, o, lse, B, Hh, N, d, x.scale, x.causal, x.kv_len, x.mask, st)
+            fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hh, N, d, x.scale, x.causal,
+                      x.kv_len, x.mask, ws, nbytes, st)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for t in (o, dq, dk, dv):
+            t.view(torch.int16).fill_(-1)
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        fa.fa_check(torch.cuda.current_stream())
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, lse_ref)
+        assert torch.equal(dk.view(torch.int16), dk_ref.view(torch.int16))
+        assert torch.equal(dv.view(torch.int16), dv_ref.view(torch.int16))
+        got, want = H.host_f64(dq), H.host_f64(dq_ref)
+        assert np.all(np.isfinite(got))
+        bound = 2.0 ** -6 * np.abs(want) + 1e-3 * np.abs(want).max()
+        assert not (np.abs(got - want) > bound).any()
