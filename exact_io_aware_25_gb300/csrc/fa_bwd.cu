@@ -542,17 +542,26 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           keep_b = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i * kTile + half * 64 + 32);
           asm volatile("" : "+r"(keep_a), "+r"(keep_b));  // evaluated here, before S^T / dP^T
         }
+        // causal: this warp's block (keys kr0..kr0+31, queries half*64..+63)
+        // holds a masked element iff its largest kr - qc exceeds the pair's
+        // delta.  Without dropout decided before the wait, off the path from
+        // S^T to its loads (with dropout, whose keep bits already sit there,
+        // that measured slower).
+        int delta = 0, kr_rel = 0;
+        bool diag = false, need_mask = false;
+        auto decide_mask = [&] {
+          delta = causal_delta(pr, i, itm.kt);
+          diag = pr.causal && ((warp & 3) * 32 + 31 - half * 64 > delta);
+          kr_rel = kr - delta;
+          need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+        };
+        if (!kDrop) decide_mask();
         if (!w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // causal: this warp's block (keys kr0..kr0+31, queries half*64..+63)
-        // holds a masked element iff its largest kr - qc exceeds the pair's delta
-        const int delta = causal_delta(pr, i, itm.kt);
-        const bool diag = pr.causal && ((warp & 3) * 32 + 31 - half * 64 > delta);
-        const int kr_rel = kr - delta;
-        const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+        if (kDrop) decide_mask();
         const uint32_t t_s = tmem + lane_base + kColST + half * 64;
         const uint32_t t_dp = tmem + lane_base + kColDPT + half * 64;
         uint32_t sa[32], da[32], sb[32], db[32];

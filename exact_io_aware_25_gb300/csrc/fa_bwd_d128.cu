@@ -309,19 +309,26 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           keep = keep_bits32(drop_kk, drop_sh, pr.drop_p8, i64 * kQStep + qc);
           asm volatile("" : "+r"(keep));  // evaluated here, before the step's registers fill
         }
+        // causal: query step i64 lies in query tile i64 / 2; this warp's block
+        // (keys kr0..kr0+31, tile columns qm..qm+31) holds a masked element iff
+        // its largest kr - qm exceeds the tile pair's delta.  Without dropout
+        // decided before the wait, off the path from S^T to its loads.
+        const int qm = (i64 & 1) * kQStep + qc;
+        int delta = 0, kr_rel = 0;
+        bool diag = false, need_mask = false;
+        auto decide_mask = [&] {
+          delta = causal_delta(pr, i64 >> 1, itm.kt);
+          diag = pr.causal && ((warp & 3) * 32 + 31 - qm > delta);
+          kr_rel = kr - delta;
+          need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+        };
+        if (!kDrop) decide_mask();
         if (!w_wait(&s.bar_s_full, g & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // causal: query step i64 lies in query tile i64 / 2; this warp's block
-        // (keys kr0..kr0+31, tile columns qm..qm+31) holds a masked element iff
-        // its largest kr - qm exceeds the tile pair's delta
-        const int qm = (i64 & 1) * kQStep + qc;
-        const int delta = causal_delta(pr, i64 >> 1, itm.kt);
-        const bool diag = pr.causal && ((warp & 3) * 32 + 31 - qm > delta);
-        const int kr_rel = kr - delta;
-        const bool need_mask = diag || !__all_sync(0xffffffffu, key_ok);
+        if (kDrop) decide_mask();
         uint32_t sa[32], da[32];
         tmem_ld32(tmem + lane_base + kColST + qc, sa);
         tmem_ld32(tmem + lane_base + kColDPT + qc, da);
