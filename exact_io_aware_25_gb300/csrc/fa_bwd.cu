@@ -508,9 +508,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     auto wg_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return named_bar_and(1, 256, mbar_wait_warp(bar, parity, pr.wait, &s.abort));
     };
-    // usually complete by the time a warp gets there: a non-blocking probe first
+    // usually complete by the time a warp gets there, else within a few
+    // hundred cycles: polled (waking from the hardware suspend measured slower)
     auto w_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return mbar_wait_warp_fast(bar, parity, pr.wait, &s.abort);
+      return mbar_spin_warp(bar, parity, pr.wait, &s.abort);
     };
     bool ok = true;
     int g = 0;          // step counter of this CTA

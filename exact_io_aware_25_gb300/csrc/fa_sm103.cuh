@@ -142,6 +142,32 @@ __device__ __forceinline__ bool mbar_wait_warp_fast(uint64_t *bar, uint32_t pari
   return __all_sync(0xffffffffu, ok);
 }
 
+// Warp-uniform wait that polls without the hardware suspend: for a warp on
+// the critical path whose phases complete within a few hundred cycles, where
+// waking from the suspend cost more than the issue slots the polling takes.
+// Same bound and abort flag as mbar_wait.
+__device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity, const WaitCtl &w,
+                                               volatile int *abort) {
+  const uint32_t a = smem_u32(bar);
+  bool ok = mbar_test_wait(a, parity);
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_test_wait(a, parity)) {
+        ok = true;
+        break;
+      }
+      if (*abort) break;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        record_error(w, kDevTimeout);
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
