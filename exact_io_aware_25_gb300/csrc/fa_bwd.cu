@@ -195,44 +195,57 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
   pdl_trigger();
 }
 
-// ---------------------------------------------------------------- main kernel
-
 // ---------------------------------------------------------------- block-sparse column lists
 
-// For key tile kt (one block each): the query tiles i >= i_begin with
-// block_mask[i][kt] != 0, ascending, and their count.  Built once per call;
-// the main kernel reads the list of the key tile it is working on.
+// For each key tile kt: the query tiles i >= i_begin with block_mask[i][kt]
+// != 0, ascending, and their count.  Built once per call; the main kernel
+// reads the list of the key tile it is working on.  A block takes
+// kColsPerBlock adjacent key tiles, one warp each.  It first copies the
+// mask's nt x kColsPerBlock byte slab for them into shared memory, all of its
+// loads issued before any is stored (a warp instruction reads four rows of
+// eight adjacent bytes), then each warp compacts its column 32 rows per
+// ballot.  Few blocks, so the launch may overlap the previous kernel's tail
+// without crowding it.
+constexpr int kColsPerBlock = 8;
+constexpr int kColsLoads = 16;  // slab bytes a thread loads per round
+
 __global__ void __launch_bounds__(256) fa_bwd_cols_kernel(const BwdArgs a) {
+  __shared__ uint8_t slab[kMaxMaskTiles * kColsPerBlock];
   pdl_wait();
   pdl_trigger();
-  __shared__ int warp_tot[8];
-  __shared__ int base;
   const Problem &pr = a.pr;
-  const int kt = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int i_begin = pr.causal ? kt : 0;
-  if (tid == 0) base = 0;
-  __syncthreads();
-  for (int chunk = 0; chunk < pr.nt; chunk += 256) {
-    const int i = chunk + tid;
-    const bool keep = i >= i_begin && i < pr.nt &&
-                      __ldg(pr.block_mask + static_cast<size_t>(i) * pr.nt + kt) != 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    int off = base;
-    for (int w = 0; w < warp; ++w) off += warp_tot[w];
-    if (keep)
-      a.col_idx[static_cast<size_t>(kt) * pr.nt + off + __popc(bal & ((1u << lane) - 1u))] =
-          static_cast<int16_t>(i);
-    __syncthreads();
-    if (tid == 0) {
-      int tot = 0;
-      for (int w = 0; w < 8; ++w) tot += warp_tot[w];
-      base += tot;
+  const int nt = pr.nt, c0 = static_cast<int>(blockIdx.x) * kColsPerBlock;
+  const int tid = threadIdx.x, c = tid & (kColsPerBlock - 1);
+  constexpr int kRowsPerPass = 256 / kColsPerBlock;
+  const bool col_ok = c0 + c < nt;
+  const uint8_t *src = pr.block_mask + c0 + c;
+  for (int r0 = tid / kColsPerBlock; r0 < nt; r0 += kRowsPerPass * kColsLoads) {
+    uint8_t v[kColsLoads];
+#pragma unroll
+    for (int u = 0; u < kColsLoads; ++u) {
+      const int r = r0 + u * kRowsPerPass;
+      v[u] = col_ok && r < nt ? __ldg(src + static_cast<size_t>(r) * nt) : 0;
     }
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kColsLoads; ++u) {
+      const int r = r0 + u * kRowsPerPass;
+      if (r < nt) slab[r * kColsPerBlock + c] = v[u];
+    }
   }
-  if (tid == 0) a.col_cnt[kt] = base;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, kt = c0 + warp;
+  if (kt >= nt) return;
+  const int i_begin = pr.causal ? kt : 0;
+  int16_t *out = a.col_idx + static_cast<size_t>(kt) * nt;
+  int cnt = 0;
+  for (int base = i_begin & ~31; base < nt; base += 32) {
+    const int i = base + lane;
+    const bool keep = i >= i_begin && i < nt && slab[i * kColsPerBlock + warp] != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) out[cnt + __popc(bal & ((1u << lane) - 1u))] = static_cast<int16_t>(i);
+    cnt += __popc(bal);
+  }
+  if (lane == 0) a.col_cnt[kt] = cnt;
 }
 
 // ---------------------------------------------------------------- main kernel
@@ -947,15 +960,18 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     configured_dev = dev;
   }
   if (a.pr.block_mask &&
-      (e = launch_ordered(fa_bwd_cols_kernel, dim3(a.pr.nt), dim3(256), 0, st, a)) != cudaSuccess)
+      (e = launch_pdl(fa_bwd_cols_kernel, dim3((a.pr.nt + kColsPerBlock - 1) / kColsPerBlock),
+                      dim3(256), 0, st, a)) != cudaSuccess)
     return e;
   // preprocess: n_pad / (32 rows x 4) blocks per head, which cover the padded
   // rows exactly, after the zeroing blocks (every padded row of every head)
-  // on sequences of up to kZeroAheadMaxN: the zeroing is O(N) work against an
-  // O(N^2) step, worth taking off the step's path only while N is short (on
-  // long sequences its stores mostly slow the previous kernel's last work)
+  // at d = 128 and, at d = 64, on sequences of up to kZeroAheadMaxN.  The
+  // zeroing blocks run during the previous kernel's tail; on long sequences
+  // behind the persistent d = 64 forward their stores evict the forward's K / V
+  // from L2 while its last units still read them (0.3% slower steps at 64K;
+  // behind the d = 128 forward, 0.9% faster at 4K)
   const size_t n4 = static_cast<size_t>(a.pr.B) * a.pr.H * a.n_pad * (a.pr.d / 4);
-  const unsigned n_zero = a.pr.N <= kZeroAheadMaxN
+  const unsigned n_zero = a.pr.N <= kZeroAheadMaxN || a.pr.d == kHeadDimWide
                               ? static_cast<unsigned>((n4 + kZeroPerBlock - 1) / kZeroPerBlock)
                               : 0u;
   const dim3 pre_grid(n_zero + static_cast<unsigned>(a.n_pad / (kRowsPerBlock * kRowsPerThread)) *

@@ -112,10 +112,11 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace      in : device scratch of >= fa_bwd_workspace_size() bytes,
  *                       16-byte aligned, owned by the caller; its contents
  *                       on entry do not matter and are garbage on return.
- *                       For N <= 2048 and no block mask, fa_bwd starts
- *                       zeroing part of it while the previous kernel on the
- *                       stream, if it is one of this library's, may still be
- *                       running: the workspace must not share memory with
+ *                       For d = 128, or N <= 2048, and no block mask,
+ *                       fa_bwd starts zeroing part of it while the previous
+ *                       kernel on the stream, if it is one of this
+ *                       library's, may still be running: the workspace must
+ *                       not share memory with
  *                       anything that call's kernels read or write (a
  *                       buffer released to a stream-ordered allocator after
  *                       that call and handed back as the workspace does).

@@ -146,18 +146,20 @@ def test_forwards_on_concurrent_streams_match_serial_runs(H, d):
 
 
 @pytest.mark.parametrize("d,masked,N", [(64, False, 2048), (64, True, 2048), (64, False, 4096),
-                                        (128, False, 2048), (128, True, 2048)])
+                                        (128, False, 2048), (128, True, 2048),
+                                        (128, False, 4096)])
 def test_backwards_back_to_back_share_a_workspace(H, d, masked, N):
     """Three backward calls on different inputs enqueued back to back on one
     stream, with no forward and no synchronisation between them, all sharing
-    one workspace.  Up to N = 2048 each call's zeroing of the dQ accumulators
-    starts without waiting for the previous kernel (above that the
-    preprocess zeroes after its wait), so it must not overtake the previous
-    call's dQ conversion (or its main kernel): every call's dK and dV equal,
-    bit for bit, and its dQ matches (within the gradient tolerance) the same
-    call run on its own: element by element within two bf16 ulps (the fp32
-    partial sums are added in hardware order) plus 1e-3 of the largest
-    magnitude, so that even one row with a lost or stale partial fails."""
+    one workspace.  At d = 128, and up to N = 2048 at d = 64, each call's
+    zeroing of the dQ accumulators starts without waiting for the previous
+    kernel (otherwise the preprocess zeroes after its wait), so it must not
+    overtake the previous call's dQ conversion (or its main kernel): every
+    call's dK and dV equal, bit for bit, and its dQ matches (within the
+    gradient tolerance) the same call run on its own: element by element
+    within two bf16 ulps (the fp32 partial sums are added in hardware order)
+    plus 1e-3 of the largest magnitude, so that even one row with a lost or
+    stale partial fails."""
     import exact_io_aware_25_gb300 as fa
     import workloads as W
     B, Hh = 2, 8
@@ -196,10 +198,10 @@ def test_backwards_back_to_back_share_a_workspace(H, d, masked, N):
 @pytest.mark.parametrize("N", [2048, 2049])
 @pytest.mark.parametrize("variant", ["causal", "kv_len"])
 def test_either_side_of_the_ahead_zeroing_length(H, oracle_mod, d, N, variant):
-    """The backward zeroes its dQ accumulators ahead of its wait for the
-    previous kernel up to N = 2048 and in the preprocess beyond: both sides
-    against the oracle (fwd and bwd run back to back, without a host
-    synchronisation between them)."""
+    """At d = 64 the backward zeroes its dQ accumulators ahead of its wait
+    for the previous kernel up to N = 2048 and in the preprocess beyond (at
+    d = 128 always ahead): both sides against the oracle (fwd and bwd run
+    back to back, without a host synchronisation between them)."""
     import exact_io_aware_25_gb300 as fa
     import workloads as W
     kw = {"causal": True} if variant == "causal" else {"kv_len": np.array([N - 300], np.int32)}
