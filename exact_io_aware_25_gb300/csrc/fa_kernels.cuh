@@ -220,20 +220,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
-// The same kernel launched without the overlap: it starts only once the
-// previous kernel on the stream has completed (its pdl_wait() returns at once).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_ordered(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                           cudaStream_t st, Args &&...args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
-}
-
 size_t fwd_smem_bytes();
 size_t bwd_smem_bytes();
 
