@@ -220,6 +220,53 @@ def test_either_side_of_the_ahead_zeroing_length(H, oracle_mod, d, N, variant):
     _check_all(H, oracle_mod, x, o, lse, grads)
 
 
+def test_several_head_groups_on_a_garbage_workspace(H, oracle_mod):
+    """The backward's main kernel hands out its items by head group (as many
+    heads as keep their Q, dO and dQ accumulators within about half of L2):
+    three groups here (36 heads of N = 8192 at d = 64, 16 per group), causal
+    with ragged key padding, on a workspace filled with 0x7F bytes (3.4e38
+    as fp32, so an accumulator row left unzeroed gives a huge dQ): dQ on rows
+    of every head against the oracle, dK and dV on sampled key tiles, and a
+    second call on the same workspace bit for bit in dK and dV and within two
+    bf16 ulps (plus 1e-3 of the largest magnitude) in dQ."""
+    import exact_io_aware_25_gb300 as fa
+    import workloads as W
+    B, Hh, N, d = 3, 12, 8192, 64
+    x = H.Inputs(W.make("tiny", seed=171, d=d, B=B, H=Hh, N=N), causal=True,
+                 kv_len=np.array([8192, 5000, 130], np.int32))
+    shape = (B, Hh, N, d)
+    st = torch.cuda.current_stream()
+    o = H.nan_like_bf16(shape)
+    lse = torch.full(shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(x.q, x.k, x.v, o, lse, B, Hh, N, d, x.scale, x.causal, x.kv_len, None, st)
+    nbytes = fa.fa_bwd_workspace_size(B, Hh, N, d)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    runs = []
+    for _ in range(2):
+        grads = tuple(H.nan_like_bf16(shape) for _ in range(3))
+        fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, *grads, B, Hh, N, d, x.scale, x.causal,
+                  x.kv_len, None, ws, nbytes, st)
+        fa.fa_check(st)
+        runs.append(grads)
+    rng = np.random.default_rng(172)
+    rows = W.sample_rows(rng, B, Hh, N, 12)
+    keys = W.sample_key_tiles(rng, B, Hh, N, 1)
+    q, k, v, do = x.f64("q"), x.f64("k"), x.f64("v"), x.f64("do")
+    dq_ref, dk_ref, dv_ref = oracle_mod.backward(q, k, v, do, x.scale, q_rows=rows, k_rows=keys,
+                                                 **x.oracle_kwargs())
+    dq, dk, dv = runs[0]
+    H.assert_grad(H.host_f64(dq).reshape(-1, d)[rows], dq_ref, "dQ")
+    H.assert_grad(H.host_f64(dk).reshape(-1, d)[keys], dk_ref, "dK")
+    H.assert_grad(H.host_f64(dv).reshape(-1, d)[keys], dv_ref, "dV")
+    assert np.all(np.isfinite(H.host_f64(dq)))
+    dq2, dk2, dv2 = runs[1]
+    assert torch.equal(dk.view(torch.int16), dk2.view(torch.int16))
+    assert torch.equal(dv.view(torch.int16), dv2.view(torch.int16))
+    got, want = H.host_f64(dq2), H.host_f64(dq)
+    bound = 2.0 ** -6 * np.abs(want) + 1e-3 * np.abs(want).max()
+    assert not (np.abs(got - want) > bound).any()
+
+
 @pytest.mark.parametrize("d,masked", [(64, False), (64, True), (128, False)])
 def test_fwd_bwd_captured_in_a_cuda_graph(H, d, masked):
     """fa_fwd + fa_bwd captured into a CUDA graph and replayed several times
