@@ -87,6 +87,29 @@ def test_sparse64k_sampled(H, oracle_mod):
                    key_tiles_per_head=2)
 
 
+@pytest.mark.parametrize("N,d,density,causal,kv,empty_cols", [
+    (131072, 64, 0.01, False, None, False),    # 1024 key tiles: the most a block mask may have
+    (100000, 128, 0.03, True, None, True),     # 782 tiles: a partial last group of columns
+    (66000, 64, 0.03, False, [40000], True),
+    (33000, 128, 0.05, True, [33000], False),
+])
+def test_block_mask_at_large_n(H, oracle_mod, N, d, density, causal, kv, empty_cols):
+    """Block masks past the 64K workload's 512 key tiles, up to the 1024-tile
+    maximum, with empty key columns, causal and key padding: the per-key-tile
+    query lists of the backward span several groups of columns and both rounds
+    of their mask loads.  Sampled rows and key tiles against the oracle."""
+    import workloads as W
+    rng = np.random.default_rng(N + d)
+    nb = -(-N // 128)
+    mask = (rng.random((nb, nb)) < density).astype(np.uint8)
+    if empty_cols:
+        mask[:, rng.choice(nb, size=nb // 4, replace=False)] = 0
+    w = W.make("tiny", seed=N % 1000 + d, d=d, B=1, H=1, N=N)
+    x = H.Inputs(w, causal=causal, block_mask=mask,
+                 kv_len=None if kv is None else np.array(kv, np.int32))
+    _sampled_check(H, oracle_mod, x, rows_per_head=48, key_tiles_per_head=3, seed=N)
+
+
 # ---------------------------------------------------------------- edge cases
 
 
