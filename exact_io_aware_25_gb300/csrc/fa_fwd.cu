@@ -402,12 +402,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       float m = -INFINITY;     // running max of S*scale*log2e
       float l = 0.f;           // running sum of 2^(S*scale*log2e - m)
       float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)
-      RowDrop rd{0u, 0u, 0u};
-      if (kDrop) {
-        rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
-        rd.shift = 16u * static_cast<uint32_t>(qrow & 1);
-        rd.p8 = pr.drop_p8;
-      }
+      RowDrop rd{0u};
+      if (kDrop) rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
       for (int it = 0; it < n; ++it) {
         const int gt = g + it;
         const int j = sparse ? static_cast<int>(s.tiles[slot][it]) : u.j_begin + it;
@@ -456,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
           const uint32_t jp0 = static_cast<uint32_t>(key0 >> 1);
-          exp_half<kDrop>(sv, half, sl2, m_use, rs8, pk, rd, jp0);  // exact zeros where masked
+          exp_half<kDrop>(sv, half, sl2, m_use, rs8, pk, rd, pr.drop_p8, jp0);  // exact zeros where masked
           if (half == 0 && it > 0) {
             if (!mbar_wait_warp_fast(&s.bar_o_done, (gt - 1) & 1, pr.wait, &s.abort)) {
               ok = false;

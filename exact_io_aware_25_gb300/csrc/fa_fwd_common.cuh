@@ -16,12 +16,12 @@ namespace fa {
 // Exact: O / l and lse use the same reference.
 constexpr float kLazyRescale = 8.f;
 
-// Dropout state of one query row: hash key with the row pair folded in, the
-// bit offset of the row's two bytes in each block word, the threshold.
+// Dropout state of one query row: the hash key with the row pair folded in.
+// (Which two bytes of each block word are the row's follows from the row's
+// parity, which is the parity of its thread; the threshold p8 is passed from
+// the kernel's parameters where it is used.)
 struct RowDrop {
-  uint32_t key;    // head key ^ ((i >> 1) << 16)
-  uint32_t shift;  // 16 * (i & 1)
-  uint32_t p8;
+  uint32_t key;  // head key ^ ((i >> 1) << 16)
 };
 
 // Exponentials of 64 consecutive S columns sv[0..64) of a row: sv[c] <-
@@ -31,13 +31,16 @@ struct RowDrop {
 // whose lanes hold consecutive rows, even rows in even lanes.
 template <bool kDrop>
 __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8)[8],
-                                      uint32_t (&pk)[32], const RowDrop &rd, uint32_t jp0) {
+                                      uint32_t (&pk)[32], const RowDrop &rd, uint32_t p8,
+                                      uint32_t jp0) {
   // byte x >= p8 (1..255) iff x + (256 - p8) carries out of the byte
-  const uint32_t qq = kDrop ? (256u - rd.p8) * 0x01010101u : 0u;
+  const uint32_t qq = kDrop ? (256u - p8) * 0x01010101u : 0u;
   // a row's keep bytes in each block word: bytes 0-1 (even row), 2-3 (odd);
-  // this row's, and its partner's in the adjacent lane
-  const uint32_t sel = rd.shift ? 0x7632u : 0x5410u;
-  const uint32_t sel_partner = rd.shift ? 0x5410u : 0x7632u;
+  // this row's, and its partner's in the adjacent lane (rows 2i and 2i + 1
+  // are threads 2i' and 2i' + 1)
+  const bool odd_row = (threadIdx.x & 1u) != 0u;
+  const uint32_t sel = odd_row ? 0x7632u : 0x5410u;
+  const uint32_t sel_partner = odd_row ? 0x5410u : 0x7632u;
 #pragma unroll
   for (int c = 0; c < 64; c += 8) {
     float x[8];
@@ -85,8 +88,8 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
 template <bool kDrop>
 __device__ __forceinline__ void exp_half(float (&sv)[kTile], int half, float sl2, float m,
                                          float (&rs8)[8], uint32_t (&pk)[32], const RowDrop &rd,
-                                         uint32_t jp0) {
-  exp64<kDrop>(sv + half * 64, sl2, m, rs8, pk, rd, jp0 + static_cast<uint32_t>(half * 32));
+                                         uint32_t p8, uint32_t jp0) {
+  exp64<kDrop>(sv + half * 64, sl2, m, rs8, pk, rd, p8, jp0 + static_cast<uint32_t>(half * 32));
 }
 
 

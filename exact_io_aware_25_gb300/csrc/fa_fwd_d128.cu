@@ -273,12 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;
     float l = 0.f;           // sum over this warp's columns
     float m_hi = -INFINITY;  // exact running row max (m may lag it by up to kLazyRescale)
-    RowDrop rd{0u, 0u, 0u};
-    if (kDrop) {
-      rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
-      rd.shift = 16u * static_cast<uint32_t>(qrow & 1);
-      rd.p8 = pr.drop_p8;
-    }
+    RowDrop rd{0u};
+    if (kDrop) rd.key = drop_head_key(pr, bh) ^ (static_cast<uint32_t>(qrow >> 1) << 16);
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int bf = it & 1;
@@ -321,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t pk[32];
         const uint32_t jp0 = static_cast<uint32_t>(kc0 >> 1);
-        exp64<kDrop>(sv, sl2, m_use, rs8, pk, rd, jp0);
+        exp64<kDrop>(sv, sl2, m_use, rs8, pk, rd, pr.drop_p8, jp0);
         tmem_st32(tmem + lane_base + kColP + static_cast<uint32_t>(bf) * 64 + ch * 32, pk);
       }
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
