@@ -49,9 +49,13 @@ __device__ __forceinline__ void exp64(float *sv, float sl2, float m, float (&rs8
       fma2(x[u], x[u + 1], sv[c + u], sv[c + u + 1], sl2, sl2, -m, -m);
 #pragma unroll
     for (int u = 0; u < 8; ++u) sv[c + u] = ex2_approx(x[u]);
+    // (the dropout instantiation sums into four partials, not eight: its
+    // hashing needs the registers)
 #pragma unroll
-    for (int u = 0; u < 8; u += 2)
-      add2(rs8[u], rs8[u + 1], rs8[u], rs8[u + 1], sv[c + u], sv[c + u + 1]);
+    for (int u = 0; u < 8; u += 2) {
+      const int r = kDrop ? (u & 2) : u;
+      add2(rs8[r], rs8[r + 1], rs8[r], rs8[r + 1], sv[c + u], sv[c + u + 1]);
+    }
     // the block words of key pairs (c >> 1) + 0..3 (keys c + u and c + u + 1
     // share one): rows 2i and 2i + 1 sit in adjacent lanes and draw on the
     // same words, so each lane of the pair hashes two of the four (the even
